@@ -1,0 +1,152 @@
+/* libmoe — the routed mixture-of-experts expert layer of a Kolibri-style model on one
+ * NVIDIA GB300 (sm_103a), as a C ABI over hand-written CUDA kernels.
+ *
+ * The layer (page "We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.",
+ * section "The gate", and section 1 for the bias and the forced ids; section 3 for the
+ * SwitchGLU expert layer): for every token a float32 router scores the routed experts
+ * (384 in Kolibri-1), the top k = 6 are selected and weighted, one shared expert runs for
+ * every token, and the weighted expert outputs are summed.  The expert choices can instead
+ * be forced from a supplied id tensor (page "We Stopped the Kolibri Benchmark Before Scoring
+ * One Answer", section "The gate, forced").  Numerical recipe of this library (the pages
+ * leave it open):
+ *   logits[t,e] = sum_k x[t,k] Wr[e,k] + b[e]                       (fp32)
+ *   ids[t]      = the k largest softmax probabilities, lowest index on ties, in descending
+ *                 order;  w[t,i] = p[ids_i] / sum_j p[ids_j]
+ *   expert e    = W8A8 SwiGLU: x is quantised per token to E4M3 (scale max|x|/448),
+ *                 g = (qx . Wg[e,n]) sx sg[e,n], u likewise, h = silu(g) u, h quantised per
+ *                 row the same way, y_e[m] = (qh . Wd[e,m]) sh sd[e,m]
+ *   y[t]        = y_shared[t] + sum_{i=0..k-1} w[t,i] y_{ids_i}[t]  (slot order)
+ * With fp32 weights (MOE_F32) the experts run in fp32 without quantisation.
+ *
+ * Conventions for every call:
+ *  - Every pointer argument is device memory owned by the caller, unless stated.  The
+ *    library allocates nothing and keeps no state between calls.
+ *  - Calls are asynchronous on `stream`; host-side validation errors return at once and
+ *    launch nothing.  Device-side errors (bad forced ids, a wait that timed out) are
+ *    recorded in the workspace and reported by moe_get_status().  Nothing traps.
+ *  - T == 0 is a no-op returning MOE_OK.
+ *  - Alignment: x, y, weights, scales and the workspace 16-byte aligned.
+ *  - Shapes: top_k == 6 (else MOE_ERR_UNSUPPORTED), n_experts <= 1024, T <= 2^20,
+ *    d_model % 256 == 0 and ffn % 64 == 0 for E4M3 weights; d_model % 32 == 0 and
+ *    ffn % 32 == 0 for fp32 weights.
+ *  - Layout: row-major, last index contiguous.
+ */
+#ifndef LIBMOE_H
+#define LIBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (0 = the legacy default stream). */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad dtype or shape */
+  MOE_ERR_UNSUPPORTED = -2,   /* valid request this build does not implement (e.g. k != 6) */
+  MOE_ERR_WORKSPACE = -3,     /* ws_bytes < moe_workspace_bytes() */
+  MOE_ERR_BAD_FORCED_ID = -4, /* a forced id was out of range or repeated within a token */
+  MOE_ERR_TIMEOUT = -5,       /* a device-side wait gave up */
+  MOE_ERR_CUDA = -6           /* a CUDA runtime call failed */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+
+/* One layer: borrowed device pointers.  Shapes with d = d_model, F = ffn, E = n_experts.
+ *   w_router     [E, d]  fp32            router_bias [E] fp32 or NULL
+ *   w_gate_up    [E, 2, F, d]            gate rows (index 0) then up rows (index 1)
+ *   s_gate_up    [E, 2, F] fp32          per-output-row scales (E4M3 only, else NULL)
+ *   w_down       [E, d, F]               s_down [E, d] fp32 (E4M3 only)
+ *   sh_gate_up   [2, F, d]               sh_s_gate_up [2, F] (E4M3 only)
+ *   sh_down      [d, F]                  sh_s_down [d] (E4M3 only)
+ * Weights are E4M3 codes (w_dtype = MOE_E4M3, one byte each) or fp32 (MOE_F32). */
+typedef struct {
+  int d_model, ffn, n_experts, top_k;
+  moe_dtype w_dtype;
+  const float* w_router;
+  const float* router_bias;
+  const void* w_gate_up;
+  const float* s_gate_up;
+  const void* w_down;
+  const float* s_down;
+  const void* sh_gate_up;
+  const float* sh_s_gate_up;
+  const void* sh_down;
+  const float* sh_s_down;
+} moe_layer;
+
+/* Flags for moe_forward / moe_forward_stack: which expert kernels run.  0 = automatic. */
+#define MOE_PATH_AUTO 0u
+#define MOE_PATH_STREAM 1u /* weight-streaming kernels (any T; sized for decode) */
+#define MOE_PATH_TC 2u     /* tcgen05 grouped GEMM (prefill-sized groups) */
+
+/* Bytes of workspace the calls below need for T tokens of this layer (host only). */
+size_t moe_workspace_bytes(const moe_layer* layer, int T);
+
+/* Clears the workspace's status record.  Call once after allocating a workspace (or use
+ * zero-filled memory).  Asynchronous on `stream`. */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Router and selection (free routing) for T tokens.
+ *   x           [T, d]  bf16 or fp32 (x_dtype)
+ *   k           must equal layer->top_k (6)
+ *   ids_out     [T, k] int32: selected experts, descending probability, lowest index on ties
+ *   w_out       [T, k] fp32: renormalised softmax weights of the selected experts
+ *   logits_out  [T, E] fp32 router logits (bias included), or NULL */
+moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, int k,
+                     int32_t* ids_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes,
+                     moe_stream_t stream);
+
+/* Grouping of the T*k routed (token, slot) rows by expert, shared expert last:
+ *   counts  [E + 1]   rows per expert; counts[E] = T (the shared expert's rows)
+ *   offsets [E + 2]   exclusive prefix sum of counts; offsets[E] = T*k, offsets[E+1] = T*k + T
+ *   perm    [T*k + T] token of each row; tokens ascend within each expert (stable)
+ *   pos     [T, k]    row holding (token t, slot i)
+ * ids [T, k] must be valid (distinct within a token, in [0, E)). */
+moe_status moe_dispatch(const int32_t* ids, int T, int n_experts, int k, int32_t* counts, int32_t* offsets,
+                        int32_t* perm, int32_t* pos, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer for T tokens.
+ *   x            [T, d] bf16 or fp32 (x_dtype)
+ *   forced_ids   [T, k] int32 or NULL: use these experts in this order instead of selecting.
+ *                Ids out of range or repeated within a token contribute nothing and set
+ *                MOE_ERR_BAD_FORCED_ID in the status record.
+ *   forced_w     [T, k] fp32 or NULL (only with forced_ids): use these weights as given;
+ *                without it the weights are the renormalised softmax over the forced ids.
+ *   ids_out, w_out  [T, k] or NULL: the ids and weights used
+ *   y            [T, d] bf16 or fp32 (y_dtype)
+ *   flags        MOE_PATH_* */
+moe_status moe_forward(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer,
+                       const int32_t* forced_ids, const float* forced_w, int32_t* ids_out, float* w_out,
+                       void* y, moe_dtype y_dtype, unsigned flags, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* L layers on a bf16 residual stream, free routing: for l = 0..L-1,
+ * r <- bf16_round_nearest_even(r + layer_l(r)).
+ *   layers    host array of L layer descriptors (read during the call only)
+ *   residual  [T, d] bf16, updated in place
+ *   ids_out   [L, T, k] int32 or NULL: the experts each layer selected
+ * ws must hold moe_workspace_bytes() of the largest layer; layers share it in turn. */
+moe_status moe_forward_stack(const moe_layer* layers, int L, void* residual, int T, int32_t* ids_out,
+                             unsigned flags, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, returns the first device-side error recorded in the workspace
+ * since the last call (MOE_OK if none) and clears the record. */
+moe_status moe_get_status(void* ws, moe_stream_t stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status status);
+
+/* The device E4M3 encoder the kernels use (round to nearest even, saturating at +-448),
+ * on n fp32 values: out[i] = code(in[i]).  For codec tests. */
+moe_status moe_e4m3_encode(const float* in, uint8_t* out, int64_t n, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMOE_H */

@@ -1,0 +1,209 @@
+"""Python binding of libmoe (ctypes): argument marshalling only.
+
+Every step of the layer runs in libmoe's CUDA kernels; this module turns torch tensors into
+device pointers, passes torch's current CUDA stream, and raises on a non-OK status.  There is
+no fallback: without the compiled library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
+PATH_AUTO, PATH_STREAM, PATH_TC = 0, 1, 2
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
+          -4: "MOE_ERR_BAD_FORCED_ID", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_CUDA"}
+
+# every entry point include/libmoe.h declares
+EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward",
+           "moe_forward_stack", "moe_get_status", "moe_status_string", "moe_e4m3_encode")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+class MoeLayerC(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("ffn", ctypes.c_int), ("n_experts", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("w_dtype", ctypes.c_int),
+                ("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("w_gate_up", ctypes.c_void_p), ("s_gate_up", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+                ("sh_gate_up", ctypes.c_void_p), ("sh_s_gate_up", ctypes.c_void_p),
+                ("sh_down", ctypes.c_void_p), ("sh_s_down", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libmoe.so.  Raises if it has not been built (no CPU fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libmoe.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint
+        L.moe_workspace_bytes.argtypes = [vp, i32]
+        L.moe_workspace_bytes.restype = sz
+        L.moe_workspace_init.argtypes = [vp, sz, vp]
+        L.moe_route.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.moe_dispatch.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_forward.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, u32, vp, sz, vp]
+        L.moe_forward_stack.argtypes = [vp, i32, vp, i32, vp, u32, vp, sz, vp]
+        L.moe_get_status.argtypes = [vp, vp]
+        L.moe_status_string.argtypes = [i32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_e4m3_encode.argtypes = [vp, vp, i64, vp]
+        for f in ("moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward", "moe_forward_stack",
+                  "moe_get_status", "moe_e4m3_encode"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().moe_status_string(status).decode()
+    except ImportError:
+        return STATUS.get(status, "unknown")
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise MoeError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmoe takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MOE_F32
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    raise ValueError(f"unsupported activation dtype {t.dtype}")
+
+
+class Layer:
+    """One layer's weights as device tensors, plus the C descriptor that borrows them.
+
+    FP8 layers take uint8 E4M3 codes (or torch.float8_e4m3fn tensors) and fp32 scales."""
+
+    def __init__(self, w_router, router_bias, w_gate_up, w_down, sh_gate_up, sh_down,
+                 s_gate_up=None, s_down=None, sh_s_gate_up=None, sh_s_down=None, top_k: int = 6):
+        self.tensors = dict(w_router=w_router, router_bias=router_bias, w_gate_up=w_gate_up, w_down=w_down,
+                            sh_gate_up=sh_gate_up, sh_down=sh_down, s_gate_up=s_gate_up, s_down=s_down,
+                            sh_s_gate_up=sh_s_gate_up, sh_s_down=sh_s_down)
+        E, two, F, d = w_gate_up.shape
+        assert two == 2
+        fp8 = w_gate_up.dtype in (torch.uint8, torch.float8_e4m3fn)
+        self.d, self.F, self.E, self.k, self.fp8 = d, F, E, top_k, fp8
+        self.c = MoeLayerC(d, F, E, top_k, MOE_E4M3 if fp8 else MOE_F32,
+                           _ptr(w_router), _ptr(router_bias), _ptr(w_gate_up), _ptr(s_gate_up), _ptr(w_down),
+                           _ptr(s_down), _ptr(sh_gate_up), _ptr(sh_s_gate_up), _ptr(sh_down), _ptr(sh_s_down))
+
+    @classmethod
+    def from_host(cls, w, device="cuda", top_k: int = 6):
+        """From a gen.moegen.LayerWeights-like object of numpy arrays."""
+        def dev(a):
+            return None if a is None else torch.from_numpy(a).to(device)
+        return cls(dev(w.Wr), dev(w.bias), dev(w.Wgu), dev(w.Wd), dev(w.sh_Wgu), dev(w.sh_Wd),
+                   dev(w.sgu), dev(w.sd), dev(w.sh_sgu), dev(w.sh_sd), top_k=top_k)
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def workspace_bytes(layer: Layer, T: int) -> int:
+    return int(lib().moe_workspace_bytes(layer.ref, T))
+
+
+def workspace(layer: Layer, T: int, device="cuda") -> torch.Tensor:
+    n = max(workspace_bytes(layer, T), 256)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(lib().moe_workspace_init(_ptr(ws), n, _stream()), "moe_workspace_init")
+    return ws
+
+
+def route(x: torch.Tensor, layer: Layer, ws: torch.Tensor, logits: bool = False):
+    """Free routing.  Returns (ids [T,k] int32, w [T,k] fp32, logits [T,E] or None)."""
+    T = x.shape[0]
+    ids = torch.empty((T, layer.k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, layer.k), dtype=torch.float32, device=x.device)
+    lg = torch.empty((T, layer.E), dtype=torch.float32, device=x.device) if logits else None
+    _check(lib().moe_route(_ptr(x), _dtype_code(x), T, layer.ref, layer.k, _ptr(ids), _ptr(w), _ptr(lg), _ptr(ws),
+                           ws.numel(), _stream()), "moe_route")
+    return ids, w, lg
+
+
+def dispatch(ids: torch.Tensor, n_experts: int, ws: torch.Tensor):
+    T, k = ids.shape
+    dev = ids.device
+    counts = torch.empty(n_experts + 1, dtype=torch.int32, device=dev)
+    offsets = torch.empty(n_experts + 2, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k + T, dtype=torch.int32, device=dev)
+    pos = torch.empty((T, k), dtype=torch.int32, device=dev)
+    _check(lib().moe_dispatch(_ptr(ids), T, n_experts, k, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(pos),
+                              _ptr(ws), ws.numel(), _stream()), "moe_dispatch")
+    return dict(counts=counts, offsets=offsets, perm=perm, pos=pos)
+
+
+def forward(x: torch.Tensor, layer: Layer, ws: torch.Tensor, forced_ids=None, forced_w=None,
+            y_dtype=torch.float32, flags: int = PATH_AUTO, out=None):
+    """The layer.  Returns (y [T,d], ids [T,k], w [T,k])."""
+    T = x.shape[0]
+    ids = torch.empty((T, layer.k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, layer.k), dtype=torch.float32, device=x.device)
+    y = out if out is not None else torch.empty((T, layer.d), dtype=y_dtype, device=x.device)
+    _check(lib().moe_forward(_ptr(x), _dtype_code(x), T, layer.ref, _ptr(forced_ids), _ptr(forced_w), _ptr(ids),
+                             _ptr(w), _ptr(y), _dtype_code(y), flags, _ptr(ws), ws.numel(), _stream()),
+           "moe_forward")
+    return y, ids, w
+
+
+def layer_array(layers: Sequence[Layer]):
+    arr = (MoeLayerC * len(layers))(*[l.c for l in layers])
+    return arr
+
+
+def forward_stack(layers: Sequence[Layer], residual: torch.Tensor, ws: torch.Tensor, ids_out=None,
+                  flags: int = PATH_AUTO, layer_arr=None):
+    """residual [T, d] bf16, updated in place.  ids_out [L, T, k] int32 or None."""
+    arr = layer_arr if layer_arr is not None else layer_array(layers)
+    T = residual.shape[0]
+    _check(lib().moe_forward_stack(arr, len(layers), _ptr(residual), T, _ptr(ids_out), flags, _ptr(ws), ws.numel(),
+                                   _stream()), "moe_forward_stack")
+    return residual
+
+
+def get_status(ws: torch.Tensor) -> int:
+    """Synchronises the current stream; returns (and clears) the device-side status code."""
+    return int(lib().moe_get_status(_ptr(ws), _stream()))
+
+
+def e4m3_encode(v: torch.Tensor) -> torch.Tensor:
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(lib().moe_e4m3_encode(_ptr(v), _ptr(out), v.numel(), _stream()), "moe_e4m3_encode")
+    return out

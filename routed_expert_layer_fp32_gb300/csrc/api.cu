@@ -1,0 +1,215 @@
+// libmoe C ABI: validation, workspace carving and the launch sequence of one layer.
+// The call names and the problem statement follow the pages' description of the layer
+// ("We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.", sections "The gate",
+// 1 and 3): route (router + top-k), the forced variant, and a stack of layers on a residual.
+#include <cstring>
+
+#include "common.cuh"
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_layer(const moe_layer* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (L->top_k != kTopK) return MOE_ERR_UNSUPPORTED;
+  if (L->n_experts < kTopK || L->n_experts > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (L->d_model <= 0 || L->ffn <= 0) return MOE_ERR_INVALID_ARG;
+  if (!L->w_router || !L->w_gate_up || !L->w_down || !L->sh_gate_up || !L->sh_down) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(L->w_router) || !aligned16(L->w_gate_up) || !aligned16(L->w_down) || !aligned16(L->sh_gate_up) ||
+      !aligned16(L->sh_down))
+    return MOE_ERR_INVALID_ARG;
+  if (L->w_dtype == MOE_E4M3) {
+    if (!L->s_gate_up || !L->s_down || !L->sh_s_gate_up || !L->sh_s_down) return MOE_ERR_INVALID_ARG;
+    if (L->d_model % 256 != 0 || L->ffn % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  } else if (L->w_dtype == MOE_F32) {
+    if (L->d_model % 128 != 0 || L->ffn % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+LayerDev to_dev(const moe_layer* L) {
+  LayerDev d;
+  d.d = L->d_model;
+  d.F = L->ffn;
+  d.E = L->n_experts;
+  d.k = L->top_k;
+  d.fp8 = L->w_dtype == MOE_E4M3;
+  d.Wr = L->w_router;
+  d.bias = L->router_bias;
+  d.wgu = static_cast<const uint8_t*>(L->w_gate_up);
+  d.sgu = L->s_gate_up;
+  d.wd = static_cast<const uint8_t*>(L->w_down);
+  d.sd = L->s_down;
+  d.sh_wgu = static_cast<const uint8_t*>(L->sh_gate_up);
+  d.sh_sgu = L->sh_s_gate_up;
+  d.sh_wd = static_cast<const uint8_t*>(L->sh_down);
+  d.sh_sd = L->sh_s_down;
+  return d;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                          \
+  do {                                         \
+    cudaError_t err__ = (expr);                \
+    if (err__ != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+// One layer on device buffers.  `residual_add`: y is the bf16 residual, updated in place.
+moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* Lh, const int32_t* forced_ids,
+                     const float* forced_w, int32_t* ids_out, float* w_out, void* y, moe_dtype y_dtype,
+                     bool residual_add, unsigned flags, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const LayerDev L = to_dev(Lh);
+  const WsLayout lay = ws_layout(*Lh, T);
+  if (ws_bytes < lay.total) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  DevStatus* st = reinterpret_cast<DevStatus*>(base + lay.status);
+  float* logits = reinterpret_cast<float*>(base + lay.logits);
+  int32_t* ids = ids_out ? ids_out : reinterpret_cast<int32_t*>(base + lay.ids);
+  float* w = w_out ? w_out : reinterpret_cast<float*>(base + lay.w);
+  int32_t* counts = reinterpret_cast<int32_t*>(base + lay.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + lay.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + lay.perm);
+  int32_t* pos = reinterpret_cast<int32_t*>(base + lay.pos);
+  const bool x_bf16 = x_dtype == MOE_BF16;
+  (void)flags;
+  if (!(forced_ids && forced_w)) MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
+  MOE_TRY(launch_select(logits, forced_ids, forced_w, T, L, ids, w, st, s));
+  MOE_TRY(launch_dispatch(ids, T, L.E, L.k, kStreamRows, lay, base, counts, offsets, perm, pos, s));
+  MOE_TRY(launch_act_quant(x, x_bf16, T, L, pos, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
+  MOE_TRY(launch_experts_stream(L, T, lay, base, s));
+  MOE_TRY(launch_combine(reinterpret_cast<const float*>(base + lay.y_rows), pos, w, T, L, y, y_dtype, residual_add, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_layer* layer, int T) {
+  if (!layer || T < 0 || check_layer(layer) != MOE_OK) return 0;
+  return ws_layout(*layer, T).total;
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || !aligned16(ws) || ws_bytes < sizeof(DevStatus)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(DevStatus), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, int k, int32_t* ids_out,
+                     float* w_out, float* logits_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status rc = check_layer(layer);
+  if (rc != MOE_OK) return rc;
+  if (k != layer->top_k) return MOE_ERR_UNSUPPORTED;
+  if (T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !ids_out || !w_out || !ws || !aligned16(x) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  const WsLayout lay = ws_layout(*layer, T);
+  if (ws_bytes < lay.total) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const LayerDev L = to_dev(layer);
+  float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + lay.logits);
+  MOE_TRY(launch_router_logits(x, x_dtype == MOE_BF16, T, L, logits, s));
+  MOE_TRY(launch_select(logits, nullptr, nullptr, T, L, ids_out, w_out, reinterpret_cast<DevStatus*>(base + lay.status), s));
+  return MOE_OK;
+}
+
+moe_status moe_dispatch(const int32_t* ids, int T, int n_experts, int k, int32_t* counts, int32_t* offsets,
+                        int32_t* perm, int32_t* pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (k != kTopK) return MOE_ERR_UNSUPPORTED;
+  if (n_experts < k || n_experts > kMaxExperts || T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ids || !counts || !offsets || !perm || !pos || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  moe_layer shape{};
+  shape.d_model = 256;
+  shape.ffn = 64;
+  shape.n_experts = n_experts;
+  shape.top_k = k;
+  shape.w_dtype = MOE_E4M3;
+  const WsLayout lay = ws_layout(shape, T);
+  if (ws_bytes < lay.total) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_dispatch(ids, T, n_experts, k, kStreamRows, lay, static_cast<char*>(ws), counts, offsets,
+                                     perm, pos, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, const int32_t* forced_ids,
+                       const float* forced_w, int32_t* ids_out, float* w_out, void* y, moe_dtype y_dtype,
+                       unsigned flags, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status rc = check_layer(layer);
+  if (rc != MOE_OK) return rc;
+  if (T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !y || !ws || !aligned16(x) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (y_dtype != MOE_F32 && y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (forced_w && !forced_ids) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_PATH_STREAM | MOE_PATH_TC)) return MOE_ERR_INVALID_ARG;
+  if (flags & MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;
+  return run_layer(x, x_dtype, T, layer, forced_ids, forced_w, ids_out, w_out, y, y_dtype, false, flags, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_stack(const moe_layer* layers, int L, void* residual, int T, int32_t* ids_out, unsigned flags,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!layers || L <= 0) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l) {
+    moe_status rc = check_layer(&layers[l]);
+    if (rc != MOE_OK) return rc;
+    if (layers[l].d_model != layers[0].d_model || layers[l].top_k != layers[0].top_k) return MOE_ERR_INVALID_ARG;
+  }
+  if (T == 0) return MOE_OK;
+  if (!residual || !ws || !aligned16(residual) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_PATH_STREAM | MOE_PATH_TC)) return MOE_ERR_INVALID_ARG;
+  if (flags & MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;
+  for (int l = 0; l < L; ++l)
+    if (ws_bytes < ws_layout(layers[l], T).total) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t per_layer_ids = size_t(T) * layers[0].top_k;
+  for (int l = 0; l < L; ++l) {
+    moe_status rc = run_layer(residual, MOE_BF16, T, &layers[l], nullptr, nullptr,
+                              ids_out ? ids_out + size_t(l) * per_layer_ids : nullptr, nullptr, residual, MOE_BF16,
+                              true, flags, ws, ws_bytes, s);
+    if (rc != MOE_OK) return rc;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_get_status(void* ws, moe_stream_t stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevStatus h;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(DevStatus)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h.flags & kFlagBadForced) return MOE_ERR_BAD_FORCED_ID;
+  if (h.flags & kFlagTimeout) return MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad dtype or shape)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported by this build (e.g. top_k != 6)";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_bytes()";
+    case MOE_ERR_BAD_FORCED_ID: return "a forced expert id was out of range or repeated within a token";
+    case MOE_ERR_TIMEOUT: return "a device-side wait timed out";
+    case MOE_ERR_CUDA: return "a CUDA runtime call failed";
+  }
+  return "unknown status";
+}
+
+moe_status moe_e4m3_encode(const float* in, uint8_t* out, int64_t n, moe_stream_t stream) {
+  if (n < 0 || (n > 0 && (!in || !out))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_e4m3_encode(in, out, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+// Dispatch: group the T*k routed (token, slot) rows by expert, stably (tokens ascend within
+// an expert), append the shared expert's T rows, and cut every group into row tiles for the
+// expert kernels.  This is the "sorted" grouping that the batched expert layer relies on
+// ("We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.", section 3: the
+// sorted gather path, used once a call has 64 or more (token, expert) rows).
+//
+// Each warp owns a run of consecutive tokens and walks it in steps of 32/k tokens, one lane
+// per (token, slot).  __match_any_sync groups the lanes that name the same expert; a lane's
+// rank is its warp-private counter plus the number of lower lanes in its group (lower lane =
+// earlier token, so the order is stable), and the group's highest lane advances the counter.
+// The per-warp counts are combined by prefix sums across warps, CTAs and experts.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 32;  // warps per dispatch CTA (1024 threads)
+constexpr int kTokensPerWarp = kDispatchChunk / kWarps;
+
+template <class F>
+__device__ __forceinline__ void warp_walk(const int32_t* __restrict__ ids, int t0, int t1, int k, int E, int* cnt,
+                                          F f) {
+  const int lane = threadIdx.x & 31;
+  const int tpi = 32 / k;
+  const int tl = lane / k, s = lane - (lane / k) * k;
+  for (int base = t0; base < t1; base += tpi) {
+    const int t = base + tl;
+    int e = (tl < tpi && t < t1) ? ids[size_t(t) * k + s] : -1;
+    if (e >= E) e = -1;  // out-of-range ids get no row
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) f(t, s, cnt[e] + __popc(m & ((1u << lane) - 1u)));
+    __syncwarp();
+    if (e >= 0 && (31 - __clz(m)) == lane) cnt[e] += __popc(m);
+    __syncwarp();
+  }
+}
+
+// Exclusive scan of n <= 2 * blockDim ints in shared memory (blockDim = 1024).  Returns the
+// total to every thread.
+__device__ int block_exclusive_scan(int* a, int n, int* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = 2 * tid, i1 = 2 * tid + 1;
+  const int v0 = i0 < n ? a[i0] : 0, v1 = i1 < n ? a[i1] : 0;
+  int s = v0 + v1, incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int wt = lane < (blockDim.x >> 5) ? warp_tot[lane] : 0, wi = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - wt;  // exclusive warp offsets
+    if (lane == 31) warp_tot[32] = wi;
+  }
+  __syncthreads();
+  const int ex = warp_tot[warp] + incl - s;
+  const int total = warp_tot[32];
+  __syncthreads();
+  if (i0 < n) a[i0] = ex;
+  if (i1 < n) a[i1] = ex + v0;
+  __syncthreads();
+  return total;
+}
+
+struct DispatchOut {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* pos;
+  int32_t* chunk_base;  // [n_chunks, E]: counts per chunk, then their exclusive prefix
+  Tile* tiles;
+  int32_t* n_tiles;
+};
+
+// Phase 1 (per CTA): per-warp counts of the chunk -> chunk totals [chunk][e].
+__device__ void count_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, int32_t* chunk_row) {
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kDispatchChunk + warp * kTokensPerWarp;
+  const int t1 = min(T, t0 + kTokensPerWarp);
+  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int w = 0; w < kWarps; ++w) s += wcnt[w * E + e];
+    chunk_row[e] = s;
+  }
+}
+
+// Scan across chunks and experts, and the tile list (shared expert's tiles first).
+__device__ void scan_and_tiles(int T, int E, int k, int n_chunks, int rows_per_tile, const DispatchOut& o,
+                               int* sm_a, int* warp_tot) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      int v = o.chunk_base[size_t(c) * E + e];
+      o.chunk_base[size_t(c) * E + e] = run;
+      run += v;
+    }
+    sm_a[e] = run;
+    o.counts[e] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan(sm_a, E, warp_tot);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) o.offsets[e] = sm_a[e];
+  if (threadIdx.x == 0) {
+    o.counts[E] = T;
+    o.offsets[E] = k * T;
+    o.offsets[E + 1] = (k + 1) * T;
+  }
+  __syncthreads();
+  // tiles: group order shared (E), 0, 1, ..., E-1
+  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
+    const int g = q == 0 ? E : q - 1;
+    const int c = g == E ? T : o.counts[g];
+    sm_a[q] = (c + rows_per_tile - 1) / rows_per_tile;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(sm_a, E + 1, warp_tot);
+  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
+    const int g = q == 0 ? E : q - 1;
+    const int c = g == E ? T : o.counts[g];
+    const int base_row = g == E ? k * T : o.offsets[g];
+    int ti = sm_a[q];
+    for (int r = 0; r < c; r += rows_per_tile, ++ti) {
+      Tile t;
+      t.group = g;
+      t.row0 = base_row + r;
+      t.nrows = min(rows_per_tile, c - r);
+      t.pad = 0;
+      o.tiles[ti] = t;
+    }
+  }
+  if (threadIdx.x == 0) *o.n_tiles = total;
+}
+
+// Phase 3 (per CTA): ranks again, now offset by the rows of earlier warps, chunks and
+// experts; writes perm and pos, plus the shared expert's rows.
+__device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, const DispatchOut& o) {
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kDispatchChunk + warp * kTokensPerWarp;
+  const int t1 = min(T, t0 + kTokensPerWarp);
+  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = o.offsets[e] + o.chunk_base[size_t(blockIdx.x) * E + e];
+    for (int w = 0; w < kWarps; ++w) {
+      int v = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  int32_t* perm = o.perm;
+  int32_t* pos = o.pos;
+  // invalid slots (id < 0) get no row
+  for (int i = (threadIdx.x & 31); i < (t1 - t0) * k; i += 32) {
+    const int t = t0 + i / k;
+    const int e = ids[size_t(t) * k + (i % k)];
+    if (e < 0 || e >= E) pos[size_t(t) * k + (i % k)] = -1;
+  }
+  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [&](int t, int s, int row) {
+    perm[row] = t;
+    pos[size_t(t) * k + s] = row;
+  });
+  for (int t = blockIdx.x * kDispatchChunk + threadIdx.x; t < min(T, (blockIdx.x + 1) * kDispatchChunk); t += blockDim.x)
+    perm[size_t(k) * T + t] = t;
+}
+
+__global__ void __launch_bounds__(1024) k_dispatch_count(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                         DispatchOut o) {
+  extern __shared__ int smem[];
+  count_chunk(ids, T, E, k, smem, o.chunk_base + size_t(blockIdx.x) * E);
+}
+
+__global__ void __launch_bounds__(1024) k_dispatch_scan(int T, int E, int k, int n_chunks, int rows_per_tile,
+                                                        DispatchOut o) {
+  __shared__ int sm_a[kMaxExperts + 1];
+  __shared__ int warp_tot[33];
+  scan_and_tiles(T, E, k, n_chunks, rows_per_tile, o, sm_a, warp_tot);
+}
+
+__global__ void __launch_bounds__(1024) k_dispatch_scatter(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                           DispatchOut o) {
+  extern __shared__ int smem[];
+  scatter_chunk(ids, T, E, k, smem, o);
+}
+
+// T <= one chunk: the three phases in one CTA.
+__global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                         int rows_per_tile, DispatchOut o) {
+  extern __shared__ int smem[];
+  __shared__ int sm_a[kMaxExperts + 1];
+  __shared__ int warp_tot[33];
+  count_chunk(ids, T, E, k, smem, o.chunk_base);
+  __threadfence_block();
+  __syncthreads();
+  scan_and_tiles(T, E, k, 1, rows_per_tile, o, sm_a, warp_tot);
+  __threadfence_block();
+  __syncthreads();
+  scatter_chunk(ids, T, E, k, smem, o);
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_per_tile, const WsLayout& ws, char* base,
+                            int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos, cudaStream_t s) {
+  DispatchOut o;
+  o.counts = counts;
+  o.offsets = offsets;
+  o.perm = perm;
+  o.pos = pos;
+  o.chunk_base = reinterpret_cast<int32_t*>(base + ws.chunk_counts);
+  o.tiles = reinterpret_cast<Tile*>(base + ws.tiles);
+  o.n_tiles = reinterpret_cast<int32_t*>(base + ws.n_tiles);
+  const size_t smem = size_t(kWarps) * E * sizeof(int);
+  const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  cudaError_t err;
+  if (n_chunks == 1) {
+    err = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (err != cudaSuccess) return err;
+    k_dispatch_small<<<1, 1024, smem, s>>>(ids, T, E, k, rows_per_tile, o);
+    return cudaGetLastError();
+  }
+  err = cudaFuncSetAttribute(k_dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(k_dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (err != cudaSuccess) return err;
+  k_dispatch_count<<<n_chunks, 1024, smem, s>>>(ids, T, E, k, o);
+  k_dispatch_scan<<<1, 1024, 0, s>>>(T, E, k, n_chunks, rows_per_tile, o);
+  k_dispatch_scatter<<<n_chunks, 1024, smem, s>>>(ids, T, E, k, o);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

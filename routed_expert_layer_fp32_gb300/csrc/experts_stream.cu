@@ -1,0 +1,500 @@
+// Expert compute on the weight-streaming path, plus activation quantisation and combine.
+//
+// SwitchGLU experts ("We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.",
+// section 3) with FP8 E4M3 weights and one fp32 scale per output row; activations are
+// quantised per row to E4M3 (scale max|v|/448) before each FP8 contraction (W8A8).
+//
+// At decode sizes the layer is a read of the selected experts' weights.  Each warp streams
+// 16 weight rows with 128-bit loads straight into registers and multiplies them by up to 32
+// activation rows with m16n8k32 E4M3 warp MMAs.  A thread's 16 contiguous bytes of a weight
+// row feed two MMAs: since a dot product does not depend on the order of its k terms, the
+// bytes are assigned to MMA k-slots in load order, and the activation fragment (16 bytes of
+// the same k range, same assignment) follows it.  No shared-memory staging is needed.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------ activation quantisation -----
+// One CTA per token: sx = max|x| / 448 (1 if the row is zero), q = E4M3(x / sx), written to
+// the token's k routed rows (pos) and to its shared-expert row k*T + t.
+template <typename XT>
+__device__ __forceinline__ void load8(const XT* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <typename XT, bool kFp8>
+__global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, int k,
+                                                   const int32_t* __restrict__ pos, void* __restrict__ xq,
+                                                   float* __restrict__ sx) {
+  __shared__ float red[8];
+  const int t = blockIdx.x;
+  const XT* xr = x + size_t(t) * d;
+  float amax = 0.0f;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float v[8];
+    load8(xr + c, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+    m = warp_max(m);
+    if (threadIdx.x == 0) red[0] = m;
+  }
+  __syncthreads();
+  amax = red[0];
+  const float s = kFp8 ? (amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f) : 1.0f;
+  int rows[kTopK + 1];
+  int nr = 0;
+  for (int i = 0; i < k; ++i) {
+    int r = pos[size_t(t) * k + i];
+    if (r >= 0) rows[nr++] = r;
+  }
+  rows[nr++] = k * T + t;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float v[8];
+    load8(xr + c, v);
+    if (kFp8) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        lo |= uint32_t(e4m3_code2(__fdiv_rn(v[i], s), __fdiv_rn(v[i + 1], s))) << (8 * i);
+        hi |= uint32_t(e4m3_code2(__fdiv_rn(v[4 + i], s), __fdiv_rn(v[5 + i], s))) << (8 * i);
+      }
+      for (int j = 0; j < nr; ++j)
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(xq) + size_t(rows[j]) * d + c) = make_uint2(lo, hi);
+    } else {
+      for (int j = 0; j < nr; ++j) {
+        float* dst = reinterpret_cast<float*>(xq) + size_t(rows[j]) * d + c;
+        *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    }
+  }
+  if (threadIdx.x == 0)
+    for (int j = 0; j < nr; ++j) sx[rows[j]] = s;
+}
+
+// ------------------------------------------------------------ gate/up, FP8 -----------------
+struct ExpertArgs {
+  int d, F, E;
+  const uint8_t* wgu;
+  const float* sgu;
+  const uint8_t* wd;
+  const float* sd;
+  const uint8_t* sh_wgu;
+  const float* sh_sgu;
+  const uint8_t* sh_wd;
+  const float* sh_sd;
+  const Tile* tiles;
+  const int* n_tiles;
+  const uint8_t* xq;  // [R, d] E4M3 (or fp32 for the fp32 path)
+  const float* sx;    // [R]
+  float* h;           // [R, F]
+  uint8_t* qh;        // [R, F]
+  float* sh;          // [R]
+  float* y_rows;      // [R, d]
+};
+
+constexpr int kKSplit = 4;  // warps per gate/up CTA, each one quarter of d
+
+// CTA = (tile of <= 32 rows, 16 output columns n of gate and of up); warp w covers
+// k in [w*d/4, (w+1)*d/4).  The four partial sums meet in shared memory.
+__global__ void __launch_bounds__(128) k_gateup_fp8(ExpertArgs a) {
+  __shared__ float red[kKSplit][4][2][4][32];
+  const int n_tiles = *a.n_tiles;
+  const int nblk = a.F / 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tig = lane & 3;
+  const int kq = a.d / kKSplit;
+  for (int item = blockIdx.x; item < n_tiles * nblk; item += gridDim.x) {
+    const Tile tl = a.tiles[item / nblk];
+    const int n0 = (item % nblk) * 16;
+    const bool shared = tl.group == a.E;
+    const uint8_t* Wg = shared ? a.sh_wgu : a.wgu + size_t(tl.group) * 2 * a.F * a.d;
+    const uint8_t* Wu = Wg + size_t(a.F) * a.d;
+    const size_t koff = size_t(warp) * kq + tig * 16;
+    const uint8_t* pg0 = Wg + size_t(n0 + gq) * a.d + koff;
+    const uint8_t* pg1 = pg0 + size_t(8) * a.d;
+    const uint8_t* pu0 = Wu + size_t(n0 + gq) * a.d + koff;
+    const uint8_t* pu1 = pu0 + size_t(8) * a.d;
+    const int ntg = (tl.nrows + 7) >> 3;
+    const uint8_t* px[4];
+    bool vx[4];
+#pragma unroll
+    for (int tg = 0; tg < 4; ++tg) {
+      const int r = tg * 8 + gq;
+      vx[tg] = r < tl.nrows;
+      px[tg] = a.xq + size_t(tl.row0 + (vx[tg] ? r : 0)) * a.d + koff;
+    }
+    float acc[4][2][4];
+#pragma unroll
+    for (int tg = 0; tg < 4; ++tg)
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[tg][j][c] = 0.0f;
+    for (int ks = 0; ks < kq; ks += 4 * 64) {
+      uint4 wg0[4], wg1[4], wu0[4], wu1[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (ks + j * 64 < kq) {
+          wg0[j] = ld_stream_u4(pg0 + ks + j * 64);
+          wg1[j] = ld_stream_u4(pg1 + ks + j * 64);
+          wu0[j] = ld_stream_u4(pu0 + ks + j * 64);
+          wu1[j] = ld_stream_u4(pu1 + ks + j * 64);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (ks + j * 64 >= kq) break;
+#pragma unroll
+        for (int tg = 0; tg < 4; ++tg) {
+          if (tg < ntg) {
+            const uint4 xa = vx[tg] ? __ldg(reinterpret_cast<const uint4*>(px[tg] + ks + j * 64)) : make_uint4(0, 0, 0, 0);
+            mma_e4m3_16x8x32(acc[tg][0], wg0[j].x, wg1[j].x, wg0[j].y, wg1[j].y, xa.x, xa.y);
+            mma_e4m3_16x8x32(acc[tg][0], wg0[j].z, wg1[j].z, wg0[j].w, wg1[j].w, xa.z, xa.w);
+            mma_e4m3_16x8x32(acc[tg][1], wu0[j].x, wu1[j].x, wu0[j].y, wu1[j].y, xa.x, xa.y);
+            mma_e4m3_16x8x32(acc[tg][1], wu0[j].z, wu1[j].z, wu0[j].w, wu1[j].w, xa.z, xa.w);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int tg = 0; tg < 4; ++tg)
+      if (tg < ntg)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) red[warp][tg][j][c][lane] = acc[tg][j][c];
+    __syncthreads();
+    const int tg = warp;
+    if (tg < ntg) {
+      const float* sg = shared ? a.sh_sgu : a.sgu + size_t(tl.group) * 2 * a.F;
+      const float* su = sg + a.F;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float gsum = 0.0f, usum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kKSplit; ++w) {
+          gsum += red[w][tg][0][c][lane];
+          usum += red[w][tg][1][c][lane];
+        }
+        const int r = tg * 8 + tig * 2 + (c & 1);
+        const int n = n0 + gq + ((c & 2) ? 8 : 0);
+        if (r < tl.nrows) {
+          const int row = tl.row0 + r;
+          const float s = a.sx[row];
+          const float gv = gsum * s * sg[n];
+          const float uv = usum * s * su[n];
+          a.h[size_t(row) * a.F + n] = silu(gv) * uv;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------ h quantisation ---------------
+// One warp per row of a tile: sh = max|h| / 448 (1 if zero), qh = E4M3(h / sh).
+__global__ void __launch_bounds__(256) k_hquant(ExpertArgs a, int rows_per_tile) {
+  const int n_tiles = *a.n_tiles;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int item = warp; item < n_tiles * rows_per_tile; item += nwarps) {
+    const Tile tl = a.tiles[item / rows_per_tile];
+    const int r = item % rows_per_tile;
+    if (r >= tl.nrows) continue;
+    const int row = tl.row0 + r;
+    const float* hr = a.h + size_t(row) * a.F;
+    float amax = 0.0f;
+    for (int n = lane * 4; n < a.F; n += 128) {
+      float4 v = *reinterpret_cast<const float4*>(hr + n);
+      amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fmaxf(fabsf(v.z), fabsf(v.w)), amax));
+    }
+    amax = warp_max(amax);
+    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    for (int n = lane * 4; n < a.F; n += 128) {
+      float4 v = *reinterpret_cast<const float4*>(hr + n);
+      uint32_t q = uint32_t(e4m3_code2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))) |
+                   (uint32_t(e4m3_code2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s))) << 16);
+      *reinterpret_cast<uint32_t*>(a.qh + size_t(row) * a.F + n) = q;
+    }
+    if (lane == 0) a.sh[row] = s;
+  }
+}
+
+// ------------------------------------------------------------ down, FP8 --------------------
+// CTA = (tile of <= 32 rows, 64 output columns m); warp w owns 16 of the m columns and the
+// whole k = ffn range.
+__global__ void __launch_bounds__(128) k_down_fp8(ExpertArgs a) {
+  const int n_tiles = *a.n_tiles;
+  const int nblk = a.d / 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tig = lane & 3;
+  for (int item = blockIdx.x; item < n_tiles * nblk; item += gridDim.x) {
+    const Tile tl = a.tiles[item / nblk];
+    const int m0 = (item % nblk) * 64 + warp * 16;
+    const bool shared = tl.group == a.E;
+    const uint8_t* W = shared ? a.sh_wd : a.wd + size_t(tl.group) * a.d * a.F;
+    const float* sdn = shared ? a.sh_sd : a.sd + size_t(tl.group) * a.d;
+    const uint8_t* p0 = W + size_t(m0 + gq) * a.F + tig * 16;
+    const uint8_t* p1 = p0 + size_t(8) * a.F;
+    const int ntg = (tl.nrows + 7) >> 3;
+    const uint8_t* px[4];
+    bool vx[4];
+#pragma unroll
+    for (int tg = 0; tg < 4; ++tg) {
+      const int r = tg * 8 + gq;
+      vx[tg] = r < tl.nrows;
+      px[tg] = a.qh + size_t(tl.row0 + (vx[tg] ? r : 0)) * a.F + tig * 16;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int tg = 0; tg < 4; ++tg)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[tg][c] = 0.0f;
+    for (int ks = 0; ks < a.F; ks += 5 * 64) {
+      uint4 w0[5], w1[5];
+#pragma unroll
+      for (int j = 0; j < 5; ++j)
+        if (ks + j * 64 < a.F) {
+          w0[j] = ld_stream_u4(p0 + ks + j * 64);
+          w1[j] = ld_stream_u4(p1 + ks + j * 64);
+        }
+#pragma unroll
+      for (int j = 0; j < 5; ++j) {
+        if (ks + j * 64 >= a.F) break;
+#pragma unroll
+        for (int tg = 0; tg < 4; ++tg) {
+          if (tg < ntg) {
+            const uint4 xa = vx[tg] ? __ldg(reinterpret_cast<const uint4*>(px[tg] + ks + j * 64)) : make_uint4(0, 0, 0, 0);
+            mma_e4m3_16x8x32(acc[tg], w0[j].x, w1[j].x, w0[j].y, w1[j].y, xa.x, xa.y);
+            mma_e4m3_16x8x32(acc[tg], w0[j].z, w1[j].z, w0[j].w, w1[j].w, xa.z, xa.w);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int tg = 0; tg < 4; ++tg) {
+      if (tg >= ntg) continue;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int r = tg * 8 + tig * 2 + (c & 1);
+        const int m = m0 + gq + ((c & 2) ? 8 : 0);
+        if (r < tl.nrows) {
+          const int row = tl.row0 + r;
+          a.y_rows[size_t(row) * a.d + m] = acc[tg][c] * a.sh[row] * sdn[m];
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ fp32 experts -----------------
+// fp32 weights and activations (no quantisation): one warp per (tile, output column),
+// lanes split k, for every row of the tile.
+__global__ void __launch_bounds__(256) k_gateup_f32(ExpertArgs a) {
+  const int n_tiles = *a.n_tiles;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const float* xf = reinterpret_cast<const float*>(a.xq);
+  for (int item = warp; item < n_tiles * a.F; item += nwarps) {
+    const Tile tl = a.tiles[item / a.F];
+    const int n = item % a.F;
+    const float* Wg = tl.group == a.E ? reinterpret_cast<const float*>(a.sh_wgu)
+                                      : reinterpret_cast<const float*>(a.wgu) + size_t(tl.group) * 2 * a.F * a.d;
+    const float* wg = Wg + size_t(n) * a.d;
+    const float* wu = Wg + size_t(a.F + n) * a.d;
+    for (int r = 0; r < tl.nrows; ++r) {
+      const float* xr = xf + size_t(tl.row0 + r) * a.d;
+      float gs = 0.0f, us = 0.0f;
+      for (int k = lane; k < a.d; k += 32) {
+        gs = fmaf(xr[k], wg[k], gs);
+        us = fmaf(xr[k], wu[k], us);
+      }
+      gs = warp_sum(gs);
+      us = warp_sum(us);
+      if (lane == 0) a.h[size_t(tl.row0 + r) * a.F + n] = silu(gs) * us;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_down_f32(ExpertArgs a) {
+  const int n_tiles = *a.n_tiles;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int item = warp; item < n_tiles * a.d; item += nwarps) {
+    const Tile tl = a.tiles[item / a.d];
+    const int m = item % a.d;
+    const float* W = tl.group == a.E ? reinterpret_cast<const float*>(a.sh_wd)
+                                     : reinterpret_cast<const float*>(a.wd) + size_t(tl.group) * a.d * a.F;
+    const float* wr = W + size_t(m) * a.F;
+    for (int r = 0; r < tl.nrows; ++r) {
+      const float* hr = a.h + size_t(tl.row0 + r) * a.F;
+      float s = 0.0f;
+      for (int n = lane; n < a.F; n += 32) s = fmaf(hr[n], wr[n], s);
+      s = warp_sum(s);
+      if (lane == 0) a.y_rows[size_t(tl.row0 + r) * a.d + m] = s;
+    }
+  }
+}
+
+// ------------------------------------------------------------ combine ----------------------
+// y[t] = Y[shared row of t] + sum_i w[t,i] Y[pos[t,i]] in slot order; optionally
+// r <- bf16(r + y) on a bf16 residual held in `out`.
+template <typename OT, bool kResidual>
+__global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_rows, const int32_t* __restrict__ pos,
+                                                 const float* __restrict__ w, int T, int d, int k, OT* __restrict__ out) {
+  const int t = blockIdx.x;
+  int rows[kTopK];
+  float wt[kTopK];
+  for (int i = 0; i < k; ++i) {
+    rows[i] = pos[size_t(t) * k + i];
+    wt[i] = w[size_t(t) * k + i];
+  }
+  const float* ysh = y_rows + (size_t(k) * T + t) * d;
+  for (int m = threadIdx.x * 4; m < d; m += blockDim.x * 4) {
+    float4 acc = *reinterpret_cast<const float4*>(ysh + m);
+    for (int i = 0; i < k; ++i) {
+      if (rows[i] < 0) continue;
+      const float4 v = *reinterpret_cast<const float4*>(y_rows + size_t(rows[i]) * d + m);
+      acc.x = fmaf(wt[i], v.x, acc.x);
+      acc.y = fmaf(wt[i], v.y, acc.y);
+      acc.z = fmaf(wt[i], v.z, acc.z);
+      acc.w = fmaf(wt[i], v.w, acc.w);
+    }
+    OT* o = out + size_t(t) * d + m;
+    if constexpr (sizeof(OT) == 4) {
+      *reinterpret_cast<float4*>(o) = acc;
+    } else {
+      if (kResidual) {
+        const uint2 r = *reinterpret_cast<const uint2*>(o);
+        acc.x += __uint_as_float(r.x << 16);
+        acc.y += __uint_as_float(r.x & 0xffff0000u);
+        acc.z += __uint_as_float(r.y << 16);
+        acc.w += __uint_as_float(r.y & 0xffff0000u);
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(o) = u;
+    }
+  }
+}
+
+__global__ void k_e4m3_encode(const float* __restrict__ in, uint8_t* __restrict__ out, int64_t n) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
+    out[i] = e4m3_code(in[i]);
+}
+
+int num_sms() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
+                             float* sx, cudaStream_t s) {
+  if (x_bf16) {
+    if (L.fp8) k_act_quant<__nv_bfloat16, true><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
+    else k_act_quant<__nv_bfloat16, false><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
+  } else {
+    if (L.fp8) k_act_quant<float, true><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
+    else k_act_quant<float, false><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_experts_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  ExpertArgs a;
+  a.d = L.d;
+  a.F = L.F;
+  a.E = L.E;
+  a.wgu = L.wgu;
+  a.sgu = L.sgu;
+  a.wd = L.wd;
+  a.sd = L.sd;
+  a.sh_wgu = L.sh_wgu;
+  a.sh_sgu = L.sh_sgu;
+  a.sh_wd = L.sh_wd;
+  a.sh_sd = L.sh_sd;
+  a.tiles = reinterpret_cast<const Tile*>(base + ws.tiles);
+  a.n_tiles = reinterpret_cast<const int*>(base + ws.n_tiles);
+  a.xq = reinterpret_cast<const uint8_t*>(base + ws.xq);
+  a.sx = reinterpret_cast<const float*>(base + ws.sx);
+  a.h = reinterpret_cast<float*>(base + ws.h);
+  a.qh = reinterpret_cast<uint8_t*>(base + ws.qh);
+  a.sh = reinterpret_cast<float*>(base + ws.sh);
+  a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
+  // upper bound of the tile count: one partial tile per non-empty group plus full tiles
+  const long long R = (long long)T * (L.k + 1);
+  const long long max_tiles = std::min<long long>(R, L.E + 1) + R / kStreamRows;
+  const int sms = num_sms();
+  if (L.fp8) {
+    long long items = max_tiles * (L.F / 16);
+    int grid = int(std::min<long long>(items, (long long)sms * 16));
+    k_gateup_fp8<<<grid, 128, 0, s>>>(a);
+    long long hitems = max_tiles * kStreamRows / 8;
+    k_hquant<<<int(std::min<long long>(hitems, (long long)sms * 8)), 256, 0, s>>>(a, kStreamRows);
+    items = max_tiles * (L.d / 64);
+    grid = int(std::min<long long>(items, (long long)sms * 16));
+    k_down_fp8<<<grid, 128, 0, s>>>(a);
+  } else {
+    long long items = max_tiles * L.F / 8;
+    k_gateup_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
+    items = max_tiles * L.d / 8;
+    k_down_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
+                           moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+  if (y_dtype == MOE_F32)
+    k_combine<float, false><<<T, 256, 0, s>>>(y_rows, pos, w, T, L.d, L.k, (float*)y);
+  else if (residual_add)
+    k_combine<__nv_bfloat16, true><<<T, 256, 0, s>>>(y_rows, pos, w, T, L.d, L.k, (__nv_bfloat16*)y);
+  else
+    k_combine<__nv_bfloat16, false><<<T, 256, 0, s>>>(y_rows, pos, w, T, L.d, L.k, (__nv_bfloat16*)y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int grid = int(std::min<int64_t>((n + 255) / 256, int64_t(num_sms()) * 32));
+  k_e4m3_encode<<<grid, 256, 0, s>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,273 @@
+"""GPU parity: libmoe through its C ABI against the CPU oracle on the same seeded inputs.
+
+Acceptance (the layer's stated tolerances): forced ids bit-exact; free ids exact except at
+near-ties (reference probabilities within 1e-4, exact ties to the lowest index); outputs
+within max|err| <= 2e-2 max|y_ref| and relative L2 <= 5e-3 of the oracle.  Where free
+routing flips a near-tie, the outputs are compared with the oracle run on the GPU's ids.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gen import moegen as g
+from oracle import oracle as o
+from tests import parity
+from tests.gpu_helpers import check_forced_layer, check_free_layer, oracle_route, to_dev_x, to_host_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__.build()
+    import routed_expert_layer_fp32_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+@pytest.fixture(scope="module")
+def kolibri(moe):
+    w = g.kolibri_layer(g.SEED_DECODE)
+    return w, moe.Layer.from_host(w)
+
+
+@pytest.fixture(scope="module")
+def tiny(moe):
+    w = g.tiny_layer()
+    return w, moe.Layer.from_host(w)
+
+
+# ------------------------------------------------------------------------ codec ----------
+
+def test_device_e4m3_encoder_matches_oracle(moe):
+    dec = o.e4m3_decode_all()[:0x7F].astype(np.float64)
+    mids = ((dec[:-1] + dec[1:]) / 2).astype(np.float32)
+    rng = np.random.default_rng(0)
+    v = np.concatenate([mids, np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(0)),
+                        -mids, np.array([0, 448, 449, 464, 480, 1e6, 3e38, 1e-30, 2 ** -10, 2 ** -11], np.float32),
+                        (rng.standard_normal(2_000_000) * rng.choice([1e-3, 1, 100, 1000], 2_000_000)).astype(np.float32)])
+    v = np.concatenate([v, -v]).astype(np.float32)
+    got = moe.e4m3_encode(torch.from_numpy(v).cuda()).cpu().numpy()
+    ref = o.e4m3_encode(v)
+    # -0 and +0 are the same value; compare codes after folding the zero codes
+    got0 = np.where(got == 0x80, 0, got)
+    ref0 = np.where(ref == 0x80, 0, ref)
+    bad = np.nonzero(got0 != ref0)[0]
+    assert bad.size == 0, [(float(v[i]), int(got[i]), int(ref[i])) for i in bad[:10]]
+
+
+# ------------------------------------------------------------------------ router ---------
+
+@pytest.mark.parametrize("T", [1, 8, 33, 64, 2048])
+def test_router_logits_ids_weights(moe, kolibri, T):
+    w, L = kolibri
+    x = g.make_x(g.SEED_DECODE, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    ids, wt, lg = moe.route(to_dev_x(x), L, ws, logits=True)
+    ref = oracle_route(w, x)
+    lg = lg.cpu().numpy()
+    err = np.max(np.abs(lg - ref["logits"]), axis=1) / np.max(np.abs(ref["logits"]), axis=1)
+    assert err.max() < 1e-5, err.max()
+    ok, bad, ndiff = parity.ids_ok(ids.cpu().numpy(), ref["ids"], ref["p"], w.E)
+    assert ok, bad
+    same = np.all(ids.cpu().numpy() == ref["ids"], axis=1)
+    assert np.max(np.abs(wt.cpu().numpy()[same] - ref["w"][same])) < 1e-5
+    assert moe.get_status(ws) == 0
+
+
+def test_router_fp32_tiny(moe, tiny):
+    w, L = tiny
+    x = g.make_x(g.SEED_TINY, 32, w.d, bf16=False)
+    ws = moe.workspace(L, 32)
+    ids, wt, lg = moe.route(to_dev_x(x), L, ws, logits=True)
+    ref = o.layer_forward(o.Layer(w), x, want_probs=True)
+    assert np.max(np.abs(lg.cpu().numpy() - ref["logits"])) < 1e-5 * np.max(np.abs(ref["logits"]))
+    ok, bad, _ = parity.ids_ok(ids.cpu().numpy(), ref["ids"], ref["p"], w.E)
+    assert ok, bad
+
+
+def test_exact_ties_pick_lowest_index(moe):
+    w = g.make_layer(21, 256, 64, 384, fp8=True, bias_var=0.5)
+    w.Wr[1::2] = w.Wr[0::2]
+    w.bias[1::2] = w.bias[0::2]
+    L = moe.Layer.from_host(w)
+    x = g.make_x(22, 64, 256, bf16=True)
+    ws = moe.workspace(L, 64)
+    ids, _, _ = moe.route(to_dev_x(x), L, ws)
+    ids = ids.cpu().numpy()
+    ref = o.layer_forward(o.Layer(w), x, want_probs=True)
+    ok, bad, _ = parity.ids_ok(ids, ref["ids"], ref["p"], w.E)
+    assert ok, bad
+    # wherever both members of a tied pair are chosen, the even (lower) one comes first
+    for t in range(64):
+        for i in range(6):
+            e = ids[t, i]
+            if e % 2 == 1 and e - 1 in ids[t]:
+                assert list(ids[t]).index(e - 1) < i
+
+
+# ----------------------------------------------------------------------- dispatch --------
+
+@pytest.fixture(scope="module")
+def shape_layer(moe):
+    return moe.Layer.from_host(g.make_layer(1, 256, 64, 384, fp8=True, bias_var=None))
+
+
+@pytest.mark.parametrize("T,mode", [(1, "rand"), (5, "rand"), (64, "rand"), (1023, "rand"), (1024, "rand"),
+                                    (1025, "rand"), (5462, "rand"), (8792, "rand"), (8792, "one_expert_set"),
+                                    (32769, "one_expert_set")])
+def test_dispatch_exact(moe, shape_layer, T, mode):
+    rng = np.random.default_rng(T)
+    if mode == "rand":
+        ids = np.argsort(rng.random((T, 384)), axis=1)[:, :6].astype(np.int32)
+    else:
+        ids = np.tile(np.array([5, 17, 3, 200, 383, 0], np.int32), (T, 1))
+    ref = o.dispatch(ids, 384)
+    ws = moe.workspace(shape_layer, T)
+    got = moe.dispatch(torch.from_numpy(ids).cuda(), 384, ws)
+    for key in ("counts", "offsets", "perm", "pos"):
+        assert np.array_equal(got[key].cpu().numpy().reshape(ref[key].shape), ref[key]), key
+
+
+# ------------------------------------------------------------------------- layer ---------
+
+def test_tiny_fp32_layer_free_then_forced(moe, tiny):
+    w, L = tiny
+    x = g.make_x(g.SEED_TINY, 32, w.d, bf16=False)
+    ws = moe.workspace(L, 32)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    _, msg, _ = check_free_layer(w, x, y, ids, wt, where="tiny free")
+    y2, ids2, _ = moe.forward(to_dev_x(x), L, ws, forced_ids=ids)
+    check_forced_layer(w, x, ids.cpu().numpy(), None, y2, ids2, where="tiny forced")
+    assert torch.equal(y2, y), "forced with the recorded ids must reproduce the free run bit for bit"
+    assert moe.get_status(ws) == 0
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_decode_layer(moe, kolibri, T):
+    w, L = kolibri
+    x = g.make_x(g.SEED_DECODE, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    _, msg, _ = check_free_layer(w, x, y, ids, wt, where=f"decode T={T}")
+    print(f"T={T}: {msg}")
+    y_bf, _, _ = moe.forward(to_dev_x(x), L, ws, y_dtype=torch.bfloat16)
+    assert torch.allclose(y_bf.float(), y, rtol=1e-2, atol=1e-2 * y.abs().max().item())
+    assert moe.get_status(ws) == 0
+
+
+def test_prefill_2048_free_then_4x512_forced(moe, kolibri):
+    w, L = kolibri
+    T = 2048
+    x = g.make_x(g.SEED_PREFILL, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    check_free_layer(w, x, y, ids, wt, where="prefill 2048 free")
+    ys = []
+    for c in range(4):
+        sl = slice(512 * c, 512 * (c + 1))
+        yc, idc, _ = moe.forward(to_dev_x(x[sl]), L, ws, forced_ids=ids[sl].contiguous())
+        assert torch.equal(idc, ids[sl]), "forced ids must be used bit-exactly"
+        ys.append(yc)
+    ych = torch.cat(ys)
+    ok, msg = parity.outputs_ok(ych.cpu().numpy(), y.cpu().numpy())
+    assert ok, f"4x512 forced vs 2048 free: {msg}"
+    check_forced_layer(w, x, ids.cpu().numpy(), None, ych, ids, where="prefill 4x512 forced")
+
+
+def test_batched_decode_zipf_forced(moe, kolibri):
+    w, L = kolibri
+    T = 128
+    x = g.make_x(g.SEED_ZIPF, T, w.d, bf16=True)
+    fid = g.zipf_ids(g.SEED_ZIPF, 0, T, 384, 6, 1.1)
+    fw = g.dirichlet_w(g.SEED_ZIPF, 0, T, 6)
+    ws = moe.workspace(L, T)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws, forced_ids=torch.from_numpy(fid).cuda(),
+                             forced_w=torch.from_numpy(fw).cuda())
+    assert np.array_equal(wt.cpu().numpy(), fw)
+    _, msg = check_forced_layer(w, x, fid, fw, y, ids, where="zipf T=128")
+    print(msg)
+
+
+@pytest.mark.parametrize("T", [0, 37, 333])
+def test_ragged_token_counts(moe, kolibri, T):
+    w, L = kolibri
+    x = g.make_x(77, max(T, 1), w.d, bf16=True)[:T]
+    ws = moe.workspace(L, max(T, 1))
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    if T == 0:
+        assert y.shape == (0, w.d)
+        return
+    check_free_layer(w, x, y, ids, wt, where=f"ragged T={T}")
+
+
+def test_bad_forced_ids_are_reported_and_skipped(moe, kolibri):
+    w, L = kolibri
+    T = 4
+    x = g.make_x(78, T, w.d, bf16=True)
+    fid = np.array([[1, 2, 3, 4, 5, 6], [1, 1, 3, 4, 5, 6], [1, 2, 3, 4, 5, 999], [7, 8, 9, 10, 11, -3]], np.int32)
+    fw = np.full((T, 6), 1 / 6, np.float32)
+    ws = moe.workspace(L, T)
+    y, ids, _ = moe.forward(to_dev_x(x), L, ws, forced_ids=torch.from_numpy(fid).cuda(),
+                            forced_w=torch.from_numpy(fw).cuda())
+    assert moe.get_status(ws) == -4
+    assert moe.get_status(ws) == 0  # cleared
+    ids = ids.cpu().numpy()
+    assert ids[1, 1] == -1 and ids[2, 5] == -1 and ids[3, 5] == -1 and np.all(ids[0] == fid[0])
+    # a rejected slot contributes nothing: compare with the oracle on zero weight there
+    fw2 = fw.copy()
+    fid2 = fid.copy()
+    for t, i in ((1, 1), (2, 5), (3, 5)):
+        fw2[t, i] = 0
+        fid2[t, i] = 100 + t  # any valid unused id with weight 0
+    ref = o.layer_forward(o.Layer(w), x, forced_ids=fid2, forced_w=fw2)
+    ok, msg = parity.outputs_ok(y.cpu().numpy(), ref["y"])
+    assert ok, msg
+
+
+def test_rows_do_not_depend_on_other_rows(moe, kolibri):
+    """Batch parity: a token's output is the same alone, in a batch, and in a permuted batch
+    (the batched expert layer on the pages returned wrong rows depending on the batch)."""
+    w, L = kolibri
+    T = 96
+    x = g.make_x(79, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, _ = moe.forward(to_dev_x(x), L, ws)
+    perm = np.random.default_rng(0).permutation(T)
+    yp, idp, _ = moe.forward(to_dev_x(x[perm]), L, ws)
+    assert torch.equal(idp, ids[perm])
+    ok, msg = parity.outputs_ok(yp.cpu().numpy(), y[perm].cpu().numpy(), max_frac=1e-4, rl2=1e-5)
+    assert ok, msg
+    for t in (0, 50, 95):
+        y1, id1, _ = moe.forward(to_dev_x(x[t:t + 1]), L, ws)
+        assert torch.equal(id1[0], ids[t])
+        ok, msg = parity.outputs_ok(y1.cpu().numpy(), y[t:t + 1].cpu().numpy(), max_frac=1e-4, rl2=1e-5)
+        assert ok, msg
+
+
+@pytest.mark.parametrize("name", ["unbiased_select", "no_renorm", "no_shared", "swap_gate_up", "scale_axis",
+                                  "bf16_router"])
+def test_planted_oracle_mistakes_fail_against_the_gpu(moe, kolibri, name):
+    """Controls: the GPU result must FAIL parity against an oracle with a planted mistake."""
+    w, L = kolibri
+    T = 64
+    x = g.make_x(80, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    _, _, lg = moe.route(to_dev_x(x), L, ws, logits=True)
+    mut = o.Layer(w, mutant=o.MUTANTS[name])
+    ref = o.layer_forward(mut, x, want_probs=True, nthreads=o.default_threads())
+    fails = []
+    if np.max(np.abs(lg.cpu().numpy() - ref["logits"])) > 1e-5 * np.max(np.abs(ref["logits"])):
+        fails.append("logits")
+    ok, _, _ = parity.ids_ok(ids.cpu().numpy(), ref["ids"], ref["p"], w.E)
+    if not ok:
+        fails.append("ids")
+    same = np.all(ids.cpu().numpy() == ref["ids"], axis=1)
+    if same.any():
+        if not parity.weights_ok(wt.cpu().numpy()[same], ref["w"][same])[0]:
+            fails.append("weights")
+        if not parity.outputs_ok(y.cpu().numpy()[same], ref["y"][same])[0]:
+            fails.append("outputs")
+    assert fails, f"planted mistake {name} went unnoticed"
