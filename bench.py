@@ -1,0 +1,361 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE expert layer (libmoe) on GB300: MoE-layer tokens/s and the
+fraction of the HBM roofline of the selected experts' bytes.
+
+Workload (headline): one Kolibri-1-shaped MoE layer (d_model 2048, ffn 640, 384 E4M3 experts
+with per-row fp32 scales, top-6 + 1 shared, fp32 router with a N(0, 0.5) per-expert bias),
+decode batch of 64 bf16 tokens, free routing.  A step is one moe_forward over the batch.
+The same layer at batch 1 and 8 is reported under "extra".  Inputs are synthetic (seeded
+counter-based generator).  Eight copies of the layer's weights are rotated across steps so
+that consecutive steps never find their experts in L2 (inputs larger than L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica (the layer has
+no cross-token exchange); the time is the maximum over ranks and the value counts the
+tokens of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+D, FFN, E, K = 2048, 640, 384, 6
+EXPERT_BYTES = 3 * D * FFN + (2 * FFN + D) * 4          # E4M3 codes + fp32 row scales
+ROUTER_BYTES = E * D * 4 + E * 4                         # fp32 router weights + bias
+GATEUP_EXPERT_BYTES = 2 * FFN * D + 2 * FFN * 4
+N_COPIES = 8
+HEADLINE_T = 64
+KERNELS_PER_FORWARD = 8  # router, select, dispatch, act_quant, gate_up, h_quant, down, combine (T <= 1024)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=HEADLINE_T)
+    ap.add_argument("--no-extra", action="store_true", help="skip the batch-1/8 extras")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=N_COPIES, help="weight copies rotated across steps")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self):
+        self.file.seek(0)
+        rows = [l.strip().split(",") for l in self.file.read().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def layer_bytes(ids: np.ndarray, T: int):
+    """Algorithmic HBM bytes of one forward: the used experts (and the shared one) once, the
+    router once, x read and y written in bf16."""
+    U = len(np.unique(ids[ids >= 0]))
+    return (U + 1) * EXPERT_BYTES + ROUTER_BYTES + 4 * T * D, U
+
+
+def gateup_bytes(U: int, T: int):
+    """Algorithmic bytes of one gate/up launch: the used experts' gate/up codes and scales,
+    the E4M3 activation rows once, h written once in fp32."""
+    R = (K + 1) * T
+    return (U + 1) * GATEUP_EXPERT_BYTES + R * D + R * FFN * 4
+
+
+# ------------------------------------------------------------------------------ ours ------
+
+def run_ours(args):
+    import torch
+    import __graft_entry__
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    import routed_expert_layer_fp32_gb300 as moe
+    from gen import moegen as g
+
+    hbm_peak, peak_kind = peaks()
+    w = g.kolibri_layer(g.SEED_DECODE)
+    base = moe.Layer.from_host(w)
+    layers = [base]
+    for _ in range(args.copies - 1):  # copies at other addresses: same values, no L2 reuse between steps
+        layers.append(moe.Layer(**{k: (v.clone() if v is not None else None) for k, v in base.tensors.items()}))
+    T = args.tokens
+    x_host = g.make_x(g.SEED_DECODE, T, D, bf16=True)
+    x = torch.from_numpy(x_host.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    ws = moe.workspace(base, T)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        moe.forward(x, layers[i % len(layers)], ws, out=y, ids=ids, w=wt, events=ev)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.binding.TRACE_POINTS)] for _ in range(args.steps)]
+    for row in evs:  # torch creates an event's CUDA handle at its first record()
+        for e in row:
+            e.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    clocks = clk.summary()
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    stage_ms = {}
+    for si, name in enumerate(moe.binding.TRACE_STAGES):
+        stage_ms[name] = statistics.mean(evs[i][si].elapsed_time(evs[i][si + 1]) for i in range(args.steps))
+    ids_h = ids.cpu().numpy()
+    nbytes, U = layer_bytes(ids_h, T)
+    gu_bytes = gateup_bytes(U, T)
+    ms_step = elapsed_ms / args.steps
+    value = world * T * args.steps / (elapsed_ms / 1e3)
+    gu_ms = stage_ms["gate_up"]
+    roof = {"bound": "hbm", "kernel": "k_gateup_fp8", "achieved": gu_bytes / (gu_ms * 1e-3) / 1e9,
+            "peak": hbm_peak, "unit": "GB/s", "peak_kind": peak_kind,
+            "frac": gu_bytes / (gu_ms * 1e-3) / 1e9 / hbm_peak, "traffic": None,
+            "algorithmic_bytes_per_launch": gu_bytes, "launch_ms": gu_ms}
+    layer_frac = nbytes / (ms_step * 1e-3) / 1e9 / hbm_peak
+
+    # end to end through the public call: pinned host x -> device, forward, y -> pinned host
+    x_pin = torch.from_numpy(x_host.view(np.int16).copy()).pin_memory()
+    y_pin = torch.empty((T, D), dtype=torch.int16).pin_memory()
+    xd = torch.empty((T, D), dtype=torch.int16, device="cuda")
+    for i in range(args.warmup):
+        xd.copy_(x_pin, non_blocking=True)
+        moe.forward(xd.view(torch.bfloat16), layers[i % len(layers)], ws, out=y, ids=ids, w=wt)
+        y_pin.copy_(y.view(torch.int16), non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        xd.copy_(x_pin, non_blocking=True)
+        moe.forward(xd.view(torch.bfloat16), layers[i % len(layers)], ws, out=y, ids=ids, w=wt)
+        y_pin.copy_(y.view(torch.int16), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2}
+
+    extra = {"layer_hbm_frac": layer_frac, "layer_bytes_per_step": nbytes, "unique_experts": U,
+             "stage_ms": stage_ms}
+    if not args.no_extra:
+        for Tx in (1, 8):
+            extra[f"decode_T{Tx}"] = small_batch(moe, g, layers, Tx, args, hbm_peak)
+
+    status = moe.get_status(ws)
+    out = {
+        "metric": "MoE-layer tokens/s (decode, batch 64); % of HBM roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 weights, bf16 activations, fp32 accumulate (W8A8)", "data": "synthetic (seeded)",
+        "config": {"workload": f"kolibri moe layer decode T={T} (d=2048, ffn=640, 384 experts top-6 + 1 shared, "
+                               f"E4M3 weights, bias N(0,0.5))", "tokens": T, "layers": 1,
+                   "l2": f"inputs larger than L2: {len(layers)} weight copies rotated across steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": args.steps * KERNELS_PER_FORWARD, "device_status": status, "extra": extra,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, x_host)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def small_batch(moe, g, layers, T, args, hbm_peak):
+    """Batch-T decode of the same layer, captured in a CUDA graph (launch overhead excluded)."""
+    import torch
+    x_host = g.make_x(g.SEED_DECODE, T, D, bf16=True)
+    x = torch.from_numpy(x_host.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    ws = moe.workspace(layers[0], T)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    n = len(layers)
+    for i in range(n):
+        moe.forward(x, layers[i], ws, out=y, ids=ids, w=wt)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(n):
+                moe.forward(x, layers[i], ws, out=y, ids=ids, w=wt)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // n)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * n)
+    nbytes, U = layer_bytes(ids.cpu().numpy(), T)
+    return {"tokens_per_s": T / (ms * 1e-3), "ms_per_layer": ms, "unique_experts": U, "bytes": nbytes,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "timing": f"CUDA graph over {n} layer copies"}
+
+
+# ---------------------------------------------------------------------------- oracle ------
+
+def cpu_baseline(w, x_host, budget_s=10.0):
+    """The CPU oracle as it stands, token-sharded over all host cores, on repeats of the same
+    64-token batch until about budget_s seconds have passed."""
+    from oracle import oracle as o
+    cores = os.cpu_count() or 1
+    L = o.Layer(w)
+    T = x_host.shape[0]
+    n = 0
+    t0 = time.time()
+    while time.time() - t0 < budget_s:
+        o.layer_forward(L, x_host, nthreads=cores)
+        n += 1
+    dt = time.time() - t0
+    return {"value": n * T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} x the {T}-token decode batch ({n * T} token-layers), {dt:.1f} s wall"}
+
+
+def run_reference(args):
+    world, rank, local = dist_setup(args)
+    if rank != 0:
+        return
+    from gen import moegen as g
+    from oracle import oracle as o
+    o.build()
+    w = g.kolibri_layer(g.SEED_DECODE)
+    T = args.tokens
+    x_host = g.make_x(g.SEED_DECODE, T, D, bf16=True)
+    cores = os.cpu_count() or 1
+    L = o.Layer(w)
+    for _ in range(args.warmup):
+        o.layer_forward(L, x_host, nthreads=cores)
+    t0 = time.time()
+    for _ in range(args.steps):
+        o.layer_forward(L, x_host, nthreads=cores)
+    dt = time.time() - t0
+    value = T * args.steps / dt
+    out = {"metric": "MoE-layer tokens/s (decode, batch 64); % of HBM roofline", "value": value,
+           "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "e4m3 weights, bf16 activations, fp32 accumulate (W8A8)", "data": "synthetic (seeded)",
+           "config": {"workload": f"kolibri moe layer decode T={T} (d=2048, ffn=640, 384 experts top-6 + 1 shared, "
+                                  f"E4M3 weights, bias N(0,0.5))", "tokens": T, "layers": 1,
+                      "parallelism": "host cores"},
+           "impl": "reference",
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{args.steps} timed steps of the {T}-token batch"},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -27,7 +27,7 @@
  *  - T == 0 is a no-op returning MOE_OK.
  *  - Alignment: x, y, weights, scales and the workspace 16-byte aligned.
  *  - Shapes: top_k == 6 (else MOE_ERR_UNSUPPORTED), n_experts <= 1024, T <= 2^20,
- *    d_model % 256 == 0 and ffn % 64 == 0 for E4M3 weights; d_model % 32 == 0 and
+ *    d_model % 256 == 0 and ffn % 64 == 0 for E4M3 weights; d_model % 128 == 0 and
  *    ffn % 32 == 0 for fp32 weights.
  *  - Layout: row-major, last index contiguous.
  */
@@ -41,8 +41,9 @@
 extern "C" {
 #endif
 
-/* A cudaStream_t (0 = the legacy default stream). */
+/* A cudaStream_t (0 = the legacy default stream) and a cudaEvent_t. */
 typedef struct CUstream_st* moe_stream_t;
+typedef struct CUevent_st* moe_event_t;
 
 typedef enum {
   MOE_OK = 0,
@@ -133,6 +134,22 @@ moe_status moe_forward(const void* x, moe_dtype x_dtype, int T, const moe_layer*
  * ws must hold moe_workspace_bytes() of the largest layer; layers share it in turn. */
 moe_status moe_forward_stack(const moe_layer* layers, int L, void* residual, int T, int32_t* ids_out,
                              unsigned flags, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Stage boundaries recorded by the *_traced calls: before the router, then after the router,
+ * selection, dispatch, activation quantisation, gate/up, h quantisation, down, combine. */
+#define MOE_TRACE_POINTS 9
+
+/* moe_forward, recording `events` (MOE_TRACE_POINTS caller-created CUDA events, or NULL) on
+ * `stream` at the stage boundaries, so the caller can time each kernel stage. */
+moe_status moe_forward_traced(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer,
+                              const int32_t* forced_ids, const float* forced_w, int32_t* ids_out, float* w_out,
+                              void* y, moe_dtype y_dtype, unsigned flags, void* ws, size_t ws_bytes,
+                              moe_stream_t stream, moe_event_t* events);
+
+/* moe_forward_stack with events [L][MOE_TRACE_POINTS] (or NULL) recorded per layer. */
+moe_status moe_forward_stack_traced(const moe_layer* layers, int L, void* residual, int T, int32_t* ids_out,
+                                    unsigned flags, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                    moe_event_t* events);
 
 /* Synchronises `stream`, returns the first device-side error recorded in the workspace
  * since the last call (MOE_OK if none) and clears the record. */

@@ -22,7 +22,10 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 
 # every entry point include/libmoe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward",
-           "moe_forward_stack", "moe_get_status", "moe_status_string", "moe_e4m3_encode")
+           "moe_forward_stack", "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status",
+           "moe_status_string", "moe_e4m3_encode")
+TRACE_POINTS = 9
+TRACE_STAGES = ("router", "select", "dispatch", "act_quant", "gate_up", "h_quant", "down", "combine")
 
 
 class MoeError(RuntimeError):
@@ -59,12 +62,14 @@ def lib():
         L.moe_dispatch.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.moe_forward.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, u32, vp, sz, vp]
         L.moe_forward_stack.argtypes = [vp, i32, vp, i32, vp, u32, vp, sz, vp]
+        L.moe_forward_traced.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, u32, vp, sz, vp, vp]
+        L.moe_forward_stack_traced.argtypes = [vp, i32, vp, i32, vp, u32, vp, sz, vp, vp]
         L.moe_get_status.argtypes = [vp, vp]
         L.moe_status_string.argtypes = [i32]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_e4m3_encode.argtypes = [vp, vp, i64, vp]
         for f in ("moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward", "moe_forward_stack",
-                  "moe_get_status", "moe_e4m3_encode"):
+                  "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status", "moe_e4m3_encode"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -170,16 +175,33 @@ def dispatch(ids: torch.Tensor, n_experts: int, ws: torch.Tensor):
     return dict(counts=counts, offsets=offsets, perm=perm, pos=pos)
 
 
+def event_array(events):
+    """ctypes array of raw cudaEvent_t handles from torch.cuda.Event objects (or None)."""
+    if events is None:
+        return None
+    handles = [e.cuda_event for e in events]
+    if not all(handles):
+        raise ValueError("timing events must exist on the device: torch creates them at their first record()")
+    return (ctypes.c_void_p * len(events))(*handles)
+
+
 def forward(x: torch.Tensor, layer: Layer, ws: torch.Tensor, forced_ids=None, forced_w=None,
-            y_dtype=torch.float32, flags: int = PATH_AUTO, out=None):
-    """The layer.  Returns (y [T,d], ids [T,k], w [T,k])."""
+            y_dtype=torch.float32, flags: int = PATH_AUTO, out=None, ids=None, w=None, events=None):
+    """The layer.  Returns (y [T,d], ids [T,k], w [T,k]).  `events`: TRACE_POINTS
+    torch.cuda.Event(enable_timing=True) recorded at the stage boundaries (moe_forward_traced)."""
     T = x.shape[0]
-    ids = torch.empty((T, layer.k), dtype=torch.int32, device=x.device)
-    w = torch.empty((T, layer.k), dtype=torch.float32, device=x.device)
+    ids = ids if ids is not None else torch.empty((T, layer.k), dtype=torch.int32, device=x.device)
+    w = w if w is not None else torch.empty((T, layer.k), dtype=torch.float32, device=x.device)
     y = out if out is not None else torch.empty((T, layer.d), dtype=y_dtype, device=x.device)
-    _check(lib().moe_forward(_ptr(x), _dtype_code(x), T, layer.ref, _ptr(forced_ids), _ptr(forced_w), _ptr(ids),
-                             _ptr(w), _ptr(y), _dtype_code(y), flags, _ptr(ws), ws.numel(), _stream()),
-           "moe_forward")
+    if events is None:
+        rc = lib().moe_forward(_ptr(x), _dtype_code(x), T, layer.ref, _ptr(forced_ids), _ptr(forced_w), _ptr(ids),
+                               _ptr(w), _ptr(y), _dtype_code(y), flags, _ptr(ws), ws.numel(), _stream())
+    else:
+        assert len(events) == TRACE_POINTS
+        rc = lib().moe_forward_traced(_ptr(x), _dtype_code(x), T, layer.ref, _ptr(forced_ids), _ptr(forced_w),
+                                      _ptr(ids), _ptr(w), _ptr(y), _dtype_code(y), flags, _ptr(ws), ws.numel(),
+                                      _stream(), event_array(events))
+    _check(rc, "moe_forward")
     return y, ids, w
 
 
@@ -189,12 +211,20 @@ def layer_array(layers: Sequence[Layer]):
 
 
 def forward_stack(layers: Sequence[Layer], residual: torch.Tensor, ws: torch.Tensor, ids_out=None,
-                  flags: int = PATH_AUTO, layer_arr=None):
-    """residual [T, d] bf16, updated in place.  ids_out [L, T, k] int32 or None."""
+                  flags: int = PATH_AUTO, layer_arr=None, events=None):
+    """residual [T, d] bf16, updated in place.  ids_out [L, T, k] int32 or None.  `events`:
+    L * TRACE_POINTS timing events (moe_forward_stack_traced) or None."""
     arr = layer_arr if layer_arr is not None else layer_array(layers)
+    n = len(arr)
     T = residual.shape[0]
-    _check(lib().moe_forward_stack(arr, len(layers), _ptr(residual), T, _ptr(ids_out), flags, _ptr(ws), ws.numel(),
-                                   _stream()), "moe_forward_stack")
+    if events is None:
+        rc = lib().moe_forward_stack(arr, n, _ptr(residual), T, _ptr(ids_out), flags, _ptr(ws), ws.numel(),
+                                     _stream())
+    else:
+        assert len(events) == n * TRACE_POINTS
+        rc = lib().moe_forward_stack_traced(arr, n, _ptr(residual), T, _ptr(ids_out), flags, _ptr(ws), ws.numel(),
+                                            _stream(), event_array(events))
+    _check(rc, "moe_forward_stack")
     return residual
 
 

@@ -63,7 +63,8 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 // One layer on device buffers.  `residual_add`: y is the bf16 residual, updated in place.
 moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* Lh, const int32_t* forced_ids,
                      const float* forced_w, int32_t* ids_out, float* w_out, void* y, moe_dtype y_dtype,
-                     bool residual_add, unsigned flags, void* ws, size_t ws_bytes, cudaStream_t s) {
+                     bool residual_add, unsigned flags, void* ws, size_t ws_bytes, cudaStream_t s,
+                     moe_event_t* ev) {
   const LayerDev L = to_dev(Lh);
   const WsLayout lay = ws_layout(*Lh, T);
   if (ws_bytes < lay.total) return MOE_ERR_WORKSPACE;
@@ -78,12 +79,27 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   int32_t* pos = reinterpret_cast<int32_t*>(base + lay.pos);
   const bool x_bf16 = x_dtype == MOE_BF16;
   (void)flags;
+  // ev (optional): MOE_TRACE_POINTS events, recorded before the first stage and after each
+  auto mark = [&](int i) -> cudaError_t {
+    return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
+  };
+  MOE_TRY(mark(0));
   if (!(forced_ids && forced_w)) MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
+  MOE_TRY(mark(1));
   MOE_TRY(launch_select(logits, forced_ids, forced_w, T, L, ids, w, st, s));
+  MOE_TRY(mark(2));
   MOE_TRY(launch_dispatch(ids, T, L.E, L.k, kStreamRows, lay, base, counts, offsets, perm, pos, s));
+  MOE_TRY(mark(3));
   MOE_TRY(launch_act_quant(x, x_bf16, T, L, pos, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
-  MOE_TRY(launch_experts_stream(L, T, lay, base, s));
+  MOE_TRY(mark(4));
+  MOE_TRY(launch_gateup_stream(L, T, lay, base, s));
+  MOE_TRY(mark(5));
+  MOE_TRY(launch_hquant(L, T, lay, base, s));
+  MOE_TRY(mark(6));
+  MOE_TRY(launch_down_stream(L, T, lay, base, s));
+  MOE_TRY(mark(7));
   MOE_TRY(launch_combine(reinterpret_cast<const float*>(base + lay.y_rows), pos, w, T, L, y, y_dtype, residual_add, s));
+  MOE_TRY(mark(8));
   return MOE_OK;
 }
 
@@ -139,9 +155,10 @@ moe_status moe_dispatch(const int32_t* ids, int T, int n_experts, int k, int32_t
                                      perm, pos, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_forward(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, const int32_t* forced_ids,
-                       const float* forced_w, int32_t* ids_out, float* w_out, void* y, moe_dtype y_dtype,
-                       unsigned flags, void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status moe_forward_traced(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer,
+                              const int32_t* forced_ids, const float* forced_w, int32_t* ids_out, float* w_out,
+                              void* y, moe_dtype y_dtype, unsigned flags, void* ws, size_t ws_bytes,
+                              moe_stream_t stream, moe_event_t* events) {
   moe_status rc = check_layer(layer);
   if (rc != MOE_OK) return rc;
   if (T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
@@ -153,11 +170,19 @@ moe_status moe_forward(const void* x, moe_dtype x_dtype, int T, const moe_layer*
   if (flags & ~(MOE_PATH_STREAM | MOE_PATH_TC)) return MOE_ERR_INVALID_ARG;
   if (flags & MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;
   return run_layer(x, x_dtype, T, layer, forced_ids, forced_w, ids_out, w_out, y, y_dtype, false, flags, ws, ws_bytes,
-                   reinterpret_cast<cudaStream_t>(stream));
+                   reinterpret_cast<cudaStream_t>(stream), events);
 }
 
-moe_status moe_forward_stack(const moe_layer* layers, int L, void* residual, int T, int32_t* ids_out, unsigned flags,
-                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status moe_forward(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, const int32_t* forced_ids,
+                       const float* forced_w, int32_t* ids_out, float* w_out, void* y, moe_dtype y_dtype,
+                       unsigned flags, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return moe_forward_traced(x, x_dtype, T, layer, forced_ids, forced_w, ids_out, w_out, y, y_dtype, flags, ws,
+                            ws_bytes, stream, nullptr);
+}
+
+moe_status moe_forward_stack_traced(const moe_layer* layers, int L, void* residual, int T, int32_t* ids_out,
+                                    unsigned flags, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                    moe_event_t* events) {
   if (!layers || L <= 0) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
   for (int l = 0; l < L; ++l) {
@@ -176,10 +201,15 @@ moe_status moe_forward_stack(const moe_layer* layers, int L, void* residual, int
   for (int l = 0; l < L; ++l) {
     moe_status rc = run_layer(residual, MOE_BF16, T, &layers[l], nullptr, nullptr,
                               ids_out ? ids_out + size_t(l) * per_layer_ids : nullptr, nullptr, residual, MOE_BF16,
-                              true, flags, ws, ws_bytes, s);
+                              true, flags, ws, ws_bytes, s, events ? events + size_t(l) * MOE_TRACE_POINTS : nullptr);
     if (rc != MOE_OK) return rc;
   }
   return MOE_OK;
+}
+
+moe_status moe_forward_stack(const moe_layer* layers, int L, void* residual, int T, int32_t* ids_out, unsigned flags,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return moe_forward_stack_traced(layers, L, residual, T, ids_out, flags, ws, ws_bytes, stream, nullptr);
 }
 
 moe_status moe_get_status(void* ws, moe_stream_t stream) {

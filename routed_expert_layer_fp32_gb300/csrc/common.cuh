@@ -145,7 +145,9 @@ cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_pe
                             cudaStream_t s);
 cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
                              float* sx, cudaStream_t s);
-cudaError_t launch_experts_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
+cudaError_t launch_gateup_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
+cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
+cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_combine(const float* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L,
                            void* y, moe_dtype y_dtype, bool residual_add, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);

@@ -225,17 +225,20 @@ cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_pe
   o.n_tiles = reinterpret_cast<int32_t*>(base + ws.n_tiles);
   const size_t smem = size_t(kWarps) * E * sizeof(int);
   const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
-  cudaError_t err;
+  // opt in once per process to the largest per-warp counter table (E <= kMaxExperts); later
+  // calls (also inside a stream capture) only launch
+  static cudaError_t attr = [] {
+    const int most = int(size_t(kWarps) * kMaxExperts * sizeof(int));
+    cudaError_t e1 = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaError_t e2 = cudaFuncSetAttribute(k_dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaError_t e3 = cudaFuncSetAttribute(k_dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    return e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+  }();
+  if (attr != cudaSuccess) return attr;
   if (n_chunks == 1) {
-    err = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (err != cudaSuccess) return err;
     k_dispatch_small<<<1, 1024, smem, s>>>(ids, T, E, k, rows_per_tile, o);
     return cudaGetLastError();
   }
-  err = cudaFuncSetAttribute(k_dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(k_dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (err != cudaSuccess) return err;
   k_dispatch_count<<<n_chunks, 1024, smem, s>>>(ids, T, E, k, o);
   k_dispatch_scan<<<1, 1024, 0, s>>>(T, E, k, n_chunks, rows_per_tile, o);
   k_dispatch_scatter<<<n_chunks, 1024, smem, s>>>(ids, T, E, k, o);

@@ -436,7 +436,8 @@ cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& 
   return cudaGetLastError();
 }
 
-cudaError_t launch_experts_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+namespace {
+ExpertArgs expert_args(const LayerDev& L, const WsLayout& ws, char* base) {
   ExpertArgs a;
   a.d = L.d;
   a.F = L.F;
@@ -457,23 +458,47 @@ cudaError_t launch_experts_stream(const LayerDev& L, int T, const WsLayout& ws, 
   a.qh = reinterpret_cast<uint8_t*>(base + ws.qh);
   a.sh = reinterpret_cast<float*>(base + ws.sh);
   a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
-  // upper bound of the tile count: one partial tile per non-empty group plus full tiles
+  return a;
+}
+
+// Upper bound of the tile count: one partial tile per non-empty group plus full tiles.
+long long max_stream_tiles(const LayerDev& L, int T) {
   const long long R = (long long)T * (L.k + 1);
-  const long long max_tiles = std::min<long long>(R, L.E + 1) + R / kStreamRows;
+  return std::min<long long>(R, L.E + 1) + R / kStreamRows;
+}
+}  // namespace
+
+cudaError_t launch_gateup_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  const ExpertArgs a = expert_args(L, ws, base);
+  const long long tiles = max_stream_tiles(L, T);
   const int sms = num_sms();
   if (L.fp8) {
-    long long items = max_tiles * (L.F / 16);
-    int grid = int(std::min<long long>(items, (long long)sms * 16));
-    k_gateup_fp8<<<grid, 128, 0, s>>>(a);
-    long long hitems = max_tiles * kStreamRows / 8;
-    k_hquant<<<int(std::min<long long>(hitems, (long long)sms * 8)), 256, 0, s>>>(a, kStreamRows);
-    items = max_tiles * (L.d / 64);
-    grid = int(std::min<long long>(items, (long long)sms * 16));
-    k_down_fp8<<<grid, 128, 0, s>>>(a);
+    const long long items = tiles * (L.F / 16);
+    k_gateup_fp8<<<int(std::min<long long>(items, (long long)sms * 16)), 128, 0, s>>>(a);
   } else {
-    long long items = max_tiles * L.F / 8;
+    const long long items = tiles * L.F / 8;
     k_gateup_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
-    items = max_tiles * L.d / 8;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  if (!L.fp8) return cudaSuccess;
+  const ExpertArgs a = expert_args(L, ws, base);
+  const long long items = max_stream_tiles(L, T) * kStreamRows / 8;
+  k_hquant<<<int(std::min<long long>(items, (long long)num_sms() * 8)), 256, 0, s>>>(a, kStreamRows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  const ExpertArgs a = expert_args(L, ws, base);
+  const long long tiles = max_stream_tiles(L, T);
+  const int sms = num_sms();
+  if (L.fp8) {
+    const long long items = tiles * (L.d / 64);
+    k_down_fp8<<<int(std::min<long long>(items, (long long)sms * 16)), 128, 0, s>>>(a);
+  } else {
+    const long long items = tiles * L.d / 8;
     k_down_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
   }
   return cudaGetLastError();
