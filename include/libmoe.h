@@ -155,6 +155,20 @@ moe_status moe_forward_stack_traced(const moe_layer* layers, int L, void* residu
  * since the last call (MOE_OK if none) and clears the record. */
 moe_status moe_get_status(void* ws, moe_stream_t stream);
 
+/* moe_route without a workspace, for callers that cannot allocate device memory (a host
+ * runtime that owns all device memory through its own pool and forbids side allocations, or a
+ * serving loop where an allocation, which may synchronise the device, is not allowed).  The
+ * pages have no counterpart: this is a deployment variant of the router and selection.
+ *   Same arguments and results as moe_route, minus logits_out and the workspace.
+ *   Scratch: a fixed 4 MiB + 256 B array inside the library, resident on every GPU that loads
+ *   it until the process exits; T * n_experts must be <= 1,048,576, else MOE_ERR_WORKSPACE.
+ *   The first call on a device looks up the array's device address (once per device, with
+ *   that device current); make that first call before any stream capture.
+ *   All calls on a device share the array: calls that overlap on the GPU race; serialise them.
+ *   Allocates nothing (no cudaMalloc, no cudaFree). */
+moe_status moe_route_noalloc(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, int k,
+                             int32_t* ids_out, float* w_out, moe_stream_t stream);
+
 /* Static description of a status code. */
 const char* moe_status_string(moe_status status);
 

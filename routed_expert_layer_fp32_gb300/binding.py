@@ -23,7 +23,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 # every entry point include/libmoe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward",
            "moe_forward_stack", "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status",
-           "moe_status_string", "moe_e4m3_encode")
+           "moe_status_string", "moe_e4m3_encode", "moe_route_noalloc")
 TRACE_POINTS = 9
 TRACE_STAGES = ("router", "select", "dispatch", "act_quant", "gate_up", "h_quant", "down", "combine")
 
@@ -68,8 +68,10 @@ def lib():
         L.moe_status_string.argtypes = [i32]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_e4m3_encode.argtypes = [vp, vp, i64, vp]
+        L.moe_route_noalloc.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         for f in ("moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward", "moe_forward_stack",
-                  "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status", "moe_e4m3_encode"):
+                  "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status", "moe_e4m3_encode",
+                  "moe_route_noalloc"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -161,6 +163,19 @@ def route(x: torch.Tensor, layer: Layer, ws: torch.Tensor, logits: bool = False)
     _check(lib().moe_route(_ptr(x), _dtype_code(x), T, layer.ref, layer.k, _ptr(ids), _ptr(w), _ptr(lg), _ptr(ws),
                            ws.numel(), _stream()), "moe_route")
     return ids, w, lg
+
+
+def route_noalloc(x: torch.Tensor, layer: Layer):
+    """Free routing without a workspace (moe_route_noalloc): for callers that cannot allocate
+    device memory.  Returns (ids [T,k] int32, w [T,k] fp32); the caller still owns the
+    outputs.  Calls that overlap on the GPU share the library's scratch and must not run
+    concurrently."""
+    T = x.shape[0]
+    ids = torch.empty((T, layer.k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, layer.k), dtype=torch.float32, device=x.device)
+    _check(lib().moe_route_noalloc(_ptr(x), _dtype_code(x), T, layer.ref, layer.k, _ptr(ids), _ptr(w), _stream()),
+           "moe_route_noalloc")
+    return ids, w
 
 
 def dispatch(ids: torch.Tensor, n_experts: int, ws: torch.Tensor):
