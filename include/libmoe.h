@@ -27,7 +27,8 @@
  *  - T == 0 is a no-op returning MOE_OK.
  *  - Alignment: x, y, weights, scales and the workspace 16-byte aligned.
  *  - Shapes: top_k == 6 (else MOE_ERR_UNSUPPORTED), n_experts <= 1024, T <= 2^20,
- *    d_model % 256 == 0 and ffn % 64 == 0 for E4M3 weights; d_model % 128 == 0 and
+ *    d_model % 256 == 0, d_model <= 2048, ffn % 64 == 0, ffn <= 640 for E4M3 weights;
+ *    d_model % 128 == 0 and
  *    ffn % 32 == 0 for fp32 weights.
  *  - Layout: row-major, last index contiguous.
  */

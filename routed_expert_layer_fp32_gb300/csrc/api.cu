@@ -2,6 +2,7 @@
 // The call names and the problem statement follow the pages' description of the layer
 // ("We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.", sections "The gate",
 // 1 and 3): route (router + top-k), the forced variant, and a stack of layers on a residual.
+#include <cstddef>
 #include <cstring>
 
 #include "common.cuh"
@@ -11,6 +12,12 @@ using namespace moe;
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shapes the weight-streaming kernels handle (their stages hold whole weight rows).
+bool stream_ok(const moe_layer& L) {
+  return L.w_dtype == MOE_F32 ||
+         (L.d_model % 256 == 0 && L.d_model <= 2048 && L.ffn % 64 == 0 && L.ffn <= 640);
+}
 
 moe_status check_layer(const moe_layer* L) {
   if (!L) return MOE_ERR_INVALID_ARG;
@@ -23,7 +30,7 @@ moe_status check_layer(const moe_layer* L) {
     return MOE_ERR_INVALID_ARG;
   if (L->w_dtype == MOE_E4M3) {
     if (!L->s_gate_up || !L->s_down || !L->sh_s_gate_up || !L->sh_s_down) return MOE_ERR_INVALID_ARG;
-    if (L->d_model % 256 != 0 || L->ffn % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!stream_ok(*L) && !(L->d_model % 128 == 0 && L->ffn % 128 == 0)) return MOE_ERR_UNSUPPORTED;
   } else if (L->w_dtype == MOE_F32) {
     if (L->d_model % 128 != 0 || L->ffn % 32 != 0) return MOE_ERR_UNSUPPORTED;
   } else {
@@ -78,25 +85,34 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   int32_t* perm = reinterpret_cast<int32_t*>(base + lay.perm);
   int32_t* pos = reinterpret_cast<int32_t*>(base + lay.pos);
   const bool x_bf16 = x_dtype == MOE_BF16;
-  (void)flags;
+  // expert path: tcgen05 grouped GEMM where it applies (unless the stream path is asked for)
+  bool use_tc = L.fp8 && !(flags & MOE_PATH_STREAM) && tc_supported(L);
+  if ((flags & MOE_PATH_TC) && !use_tc) return MOE_ERR_UNSUPPORTED;
+  if (!use_tc && !stream_ok(*Lh)) return MOE_ERR_UNSUPPORTED;
+  const int rows_per_tile = use_tc ? tc_rows_per_tile(T) : kStreamRows;
   // ev (optional): MOE_TRACE_POINTS events, recorded before the first stage and after each
   auto mark = [&](int i) -> cudaError_t {
     return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
   MOE_TRY(mark(0));
-  if (!(forced_ids && forced_w)) MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
+  float* part = reinterpret_cast<float*>(base + lay.router_part);
+  if (!(forced_ids && forced_w)) {
+    if (T <= kRouterSplitMaxT && L.d <= 2048) MOE_TRY(launch_router_split(x, x_bf16, T, L, part, logits, st, s));
+    else MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
+  }
   MOE_TRY(mark(1));
   MOE_TRY(launch_select(logits, forced_ids, forced_w, T, L, ids, w, st, s));
   MOE_TRY(mark(2));
-  MOE_TRY(launch_dispatch(ids, T, L.E, L.k, kStreamRows, lay, base, counts, offsets, perm, pos, s));
+  MOE_TRY(launch_dispatch(ids, T, L.E, L.k, rows_per_tile, lay, base, counts, offsets, perm, pos, s));
   MOE_TRY(mark(3));
-  MOE_TRY(launch_act_quant(x, x_bf16, T, L, pos, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
+  MOE_TRY(launch_act_quant(x, x_bf16, T, L, pos, base + lay.xq, reinterpret_cast<float*>(base + lay.sx),
+                           reinterpret_cast<float*>(base + lay.hmax), s));
   MOE_TRY(mark(4));
-  MOE_TRY(launch_gateup_stream(L, T, lay, base, s));
+  MOE_TRY(use_tc ? launch_gateup_tc(L, T, lay, base, s) : launch_gateup_stream(L, T, lay, base, s));
   MOE_TRY(mark(5));
-  MOE_TRY(launch_hquant(L, T, lay, base, s));
+  MOE_TRY(launch_hquant(L, T, lay, base, rows_per_tile, s));
   MOE_TRY(mark(6));
-  MOE_TRY(launch_down_stream(L, T, lay, base, s));
+  MOE_TRY(use_tc ? launch_down_tc(L, T, lay, base, s) : launch_down_stream(L, T, lay, base, s));
   MOE_TRY(mark(7));
   MOE_TRY(launch_combine(reinterpret_cast<const float*>(base + lay.y_rows), pos, w, T, L, y, y_dtype, residual_add, s));
   MOE_TRY(mark(8));
@@ -132,8 +148,13 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const LayerDev L = to_dev(layer);
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + lay.logits);
-  MOE_TRY(launch_router_logits(x, x_dtype == MOE_BF16, T, L, logits, s));
-  MOE_TRY(launch_select(logits, nullptr, nullptr, T, L, ids_out, w_out, reinterpret_cast<DevStatus*>(base + lay.status), s));
+  DevStatus* st = reinterpret_cast<DevStatus*>(base + lay.status);
+  if (T <= kRouterSplitMaxT && L.d <= 2048)
+    MOE_TRY(launch_router_split(x, x_dtype == MOE_BF16, T, L, reinterpret_cast<float*>(base + lay.router_part), logits,
+                                st, s));
+  else
+    MOE_TRY(launch_router_logits(x, x_dtype == MOE_BF16, T, L, logits, s));
+  MOE_TRY(launch_select(logits, nullptr, nullptr, T, L, ids_out, w_out, st, s));
   return MOE_OK;
 }
 
@@ -167,8 +188,7 @@ moe_status moe_forward_traced(const void* x, moe_dtype x_dtype, int T, const moe
   if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (y_dtype != MOE_F32 && y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (forced_w && !forced_ids) return MOE_ERR_INVALID_ARG;
-  if (flags & ~(MOE_PATH_STREAM | MOE_PATH_TC)) return MOE_ERR_INVALID_ARG;
-  if (flags & MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;
+  if (flags & ~(MOE_PATH_STREAM | MOE_PATH_TC) || flags == (MOE_PATH_STREAM | MOE_PATH_TC)) return MOE_ERR_INVALID_ARG;
   return run_layer(x, x_dtype, T, layer, forced_ids, forced_w, ids_out, w_out, y, y_dtype, false, flags, ws, ws_bytes,
                    reinterpret_cast<cudaStream_t>(stream), events);
 }
@@ -192,8 +212,7 @@ moe_status moe_forward_stack_traced(const moe_layer* layers, int L, void* residu
   }
   if (T == 0) return MOE_OK;
   if (!residual || !ws || !aligned16(residual) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
-  if (flags & ~(MOE_PATH_STREAM | MOE_PATH_TC)) return MOE_ERR_INVALID_ARG;
-  if (flags & MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;
+  if (flags & ~(MOE_PATH_STREAM | MOE_PATH_TC) || flags == (MOE_PATH_STREAM | MOE_PATH_TC)) return MOE_ERR_INVALID_ARG;
   for (int l = 0; l < L; ++l)
     if (ws_bytes < ws_layout(layers[l], T).total) return MOE_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -218,7 +237,8 @@ moe_status moe_get_status(void* ws, moe_stream_t stream) {
   DevStatus h;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemset(ws, 0, sizeof(DevStatus)) != cudaSuccess) return MOE_ERR_CUDA;
+  // clear the error fields only (the router's completion counters are already back at 0)
+  if (cudaMemset(ws, 0, offsetof(DevStatus, pad)) != cudaSuccess) return MOE_ERR_CUDA;
   if (h.flags & kFlagBadForced) return MOE_ERR_BAD_FORCED_ID;
   if (h.flags & kFlagTimeout) return MOE_ERR_TIMEOUT;
   return MOE_OK;

@@ -19,7 +19,8 @@ struct DevStatus {
   int flags;        // bit 0: bad forced id, bit 1: timeout
   int bad_forced;   // number of rejected forced slots
   int timeout_site; // where a bounded wait gave up (0 = none)
-  int pad[61];
+  int pad[29];
+  unsigned router_done[32];  // per expert block: k-slices finished (back to 0 after each use)
 };
 constexpr int kFlagBadForced = 1;
 constexpr int kFlagTimeout = 2;
@@ -32,13 +33,16 @@ struct Tile {
 
 // Where each buffer lives inside the caller's workspace, for T tokens.
 struct WsLayout {
-  size_t status, logits, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h, qh, sh, y_rows;
+  size_t status, logits, router_part, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h, hmax,
+      qh, sh, y_rows;
   size_t total;
-  int T, R, n_chunks, max_tiles;
+  int T, R, R_alloc, n_chunks, max_tiles;
 };
 
 constexpr int kDispatchChunk = 1024;  // tokens per dispatch CTA
-constexpr int kStreamRows = 32;        // rows per tile on the streaming path
+constexpr int kRouterSplitMaxT = 128;  // up to this many tokens the router splits k (decode)
+constexpr int kRouterSplitK = 128;     // k-slice of the split router
+constexpr int kStreamRows = 16;        // rows per tile on the streaming path
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -49,12 +53,14 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   const bool f32w = (L.w_dtype == MOE_F32);
   w.T = T;
   w.R = int(R);
+  w.R_alloc = int(R) + 256;  // row padding: tensor-map boxes of up to 256 rows stay inside the buffers
   w.n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
   w.max_tiles = int(R / 8 + 2 * (E + 1) + 8);  // tiles of >= 8 rows or a group's tail
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   w.status = take(sizeof(DevStatus));
   w.logits = take(size_t(T) * E * 4);
+  w.router_part = take(T <= kRouterSplitMaxT ? size_t(d / kRouterSplitK) * T * E * 4 : 0);
   w.ids = take(size_t(T) * k * 4);
   w.w = take(size_t(T) * k * 4);
   w.counts = take(size_t(E + 1) * 4);
@@ -64,10 +70,11 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   w.pos = take(size_t(T) * k * 4);
   w.n_tiles = take(16);
   w.tiles = take(size_t(w.max_tiles) * sizeof(Tile));
-  w.xq = take(R * d * (f32w ? 4 : 1));
+  w.xq = take(size_t(w.R_alloc) * d * (f32w ? 4 : 1));
   w.sx = take(R * 4);
   w.h = take(R * F * 4);
-  w.qh = take(R * F);
+  w.hmax = take(R * 4);
+  w.qh = take(size_t(w.R_alloc) * F);
   w.sh = take(R * 4);
   w.y_rows = take(R * d * 4);
   w.total = o;
@@ -95,6 +102,31 @@ __device__ __forceinline__ uint16_t e4m3_code2(float a, float b) {
   return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
+// 16-byte asynchronous global->shared copy (L1 bypassed); src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes = 16) {
+  const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(gmem), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Wait until at most n groups are pending (n folds to a constant in unrolled loops).
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    case 8: cp_async_wait<8>(); break;
+    case 9: cp_async_wait<9>(); break;
+    default: cp_async_wait<0>(); break;
+  }
+}
+
 // 128-bit load of streamed weights: read once, do not keep in L1.
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   uint4 r;
@@ -118,6 +150,12 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ void set_status(DevStatus* st, int flag) { atomicOr(&st->flags, flag); }
 
+// Record a device-side timeout: flags |= kFlagTimeout, and the first site that gave up.
+__device__ __forceinline__ void report_timeout_flag(int* status_flags, int site) {
+  atomicOr(status_flags, kFlagTimeout);
+  atomicCAS(status_flags + 2, 0, site);
+}
+
 }  // namespace moe
 
 // Kernel launchers (defined in the .cu files, called by api.cu).
@@ -140,13 +178,23 @@ struct LayerDev {
 cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
 cudaError_t launch_select(const float* logits, const int32_t* forced_ids, const float* forced_w, int T,
                           const LayerDev& L, int32_t* ids, float* w, DevStatus* st, cudaStream_t s);
+// Decode router (T <= kRouterSplitMaxT): d/kRouterSplitK partial slices [n][T][E] in `part`,
+// summed in slice order (plus bias) into logits [T][E] by the last CTA of each expert block.
+cudaError_t launch_router_split(const void* x, bool x_bf16, int T, const LayerDev& L, float* part, float* logits,
+                                DevStatus* st, cudaStream_t s);
+
 cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_per_tile, const WsLayout& ws,
                             char* base, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
                             cudaStream_t s);
 cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
-                             float* sx, cudaStream_t s);
+                             float* sx, float* hmax, cudaStream_t s);
 cudaError_t launch_gateup_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
-cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
+cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, int rows_per_tile, cudaStream_t s);
+// tcgen05 grouped GEMMs (prefill and decode): E4M3 weights with d % 128 == 0, ffn % 128 == 0.
+bool tc_supported(const LayerDev& L);
+int tc_rows_per_tile(int T);
+cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
+cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_combine(const float* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L,
                            void* y, moe_dtype y_dtype, bool residual_add, cudaStream_t s);

@@ -80,9 +80,16 @@ struct DispatchOut {
 };
 
 // Phase 1 (per CTA): per-warp counts of the chunk -> chunk totals [chunk][e].
+// Warps of this CTA that own tokens (the rest skip every per-warp loop).
+__device__ __forceinline__ int active_warps(int T) {
+  const int n = min(T - int(blockIdx.x) * kDispatchChunk, kDispatchChunk);
+  return min(kWarps, (n + kTokensPerWarp - 1) / kTokensPerWarp);
+}
+
 __device__ void count_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, int32_t* chunk_row) {
   const int warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i] = 0;
+  const int nw = active_warps(T);
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   const int t0 = blockIdx.x * kDispatchChunk + warp * kTokensPerWarp;
   const int t1 = min(T, t0 + kTokensPerWarp);
@@ -90,7 +97,7 @@ __device__ void count_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, 
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
-    for (int w = 0; w < kWarps; ++w) s += wcnt[w * E + e];
+    for (int w = 0; w < nw; ++w) s += wcnt[w * E + e];
     chunk_row[e] = s;
   }
 }
@@ -146,7 +153,8 @@ __device__ void scan_and_tiles(int T, int E, int k, int n_chunks, int rows_per_t
 // experts; writes perm and pos, plus the shared expert's rows.
 __device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, const DispatchOut& o) {
   const int warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i] = 0;
+  const int nw = active_warps(T);
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   const int t0 = blockIdx.x * kDispatchChunk + warp * kTokensPerWarp;
   const int t1 = min(T, t0 + kTokensPerWarp);
@@ -154,7 +162,7 @@ __device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = o.offsets[e] + o.chunk_base[size_t(blockIdx.x) * E + e];
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       int v = wcnt[w * E + e];
       wcnt[w * E + e] = run;
       run += v;

@@ -13,6 +13,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace moe {
 namespace {
@@ -43,7 +44,7 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
 template <typename XT, bool kFp8>
 __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, int k,
                                                    const int32_t* __restrict__ pos, void* __restrict__ xq,
-                                                   float* __restrict__ sx) {
+                                                   float* __restrict__ sx, float* __restrict__ hmax) {
   __shared__ float red[8];
   const int t = blockIdx.x;
   const XT* xr = x + size_t(t) * d;
@@ -93,7 +94,10 @@ __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int
     }
   }
   if (threadIdx.x == 0)
-    for (int j = 0; j < nr; ++j) sx[rows[j]] = s;
+    for (int j = 0; j < nr; ++j) {
+      sx[rows[j]] = s;
+      hmax[rows[j]] = 0.0f;  // row maxima of h are accumulated by the gate/up kernel
+    }
 }
 
 // ------------------------------------------------------------ gate/up, FP8 -----------------
@@ -112,92 +116,162 @@ struct ExpertArgs {
   const uint8_t* xq;  // [R, d] E4M3 (or fp32 for the fp32 path)
   const float* sx;    // [R]
   float* h;           // [R, F]
+  float* hmax;        // [R]  max |h| of each row
   uint8_t* qh;        // [R, F]
   float* sh;          // [R]
   float* y_rows;      // [R, d]
 };
 
-constexpr int kKSplit = 4;  // warps per gate/up CTA, each one quarter of d
+constexpr int kTG = kStreamRows / 8;     // token groups of 8 rows per tile
 
-// CTA = (tile of <= 32 rows, 16 output columns n of gate and of up); warp w covers
-// k in [w*d/4, (w+1)*d/4).  The four partial sums meet in shared memory.
-__global__ void __launch_bounds__(128) k_gateup_fp8(ExpertArgs a) {
-  __shared__ float red[kKSplit][4][2][4][32];
+// Bulk-copy (TMA) pipeline shared by the two streaming kernels: one producer warp copies
+// whole weight rows and activation rows of a work item into a shared-memory stage with
+// cp.async.bulk (completion counted on the stage's "full" mbarrier); four MMA warps wait on
+// it, compute, and release the stage on its "empty" mbarrier.  Rows are stored with a
+// 16-byte pad so the fragment loads of 8 consecutive rows hit distinct banks.  Every wait is
+// bounded (tma.cuh); on a timeout the CTA records MOE_ERR_TIMEOUT, the producer stops, the
+// MMA warps leave at the same stage wait, and the producer waits for its copies in flight
+// before the CTA exits.
+constexpr int kConsumerWarps = 4;
+constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRowPad = 16;
+
+struct PipeCtl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  int abort;
+};
+
+__device__ __forceinline__ void pipe_init(PipeCtl* ctl, int stages) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], kConsumerWarps);
+    }
+    ctl->abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void report_timeout(int* status_flags, int site) { report_timeout_flag(status_flags, site); }
+
+// Producer epilogue: wait (bounded, ignoring the abort flag) until the last copies issued
+// into every stage have landed, so no bulk copy targets this CTA's shared memory after exit.
+__device__ __forceinline__ void pipe_drain(PipeCtl* ctl, int stages, int issued) {
+  for (int s = 0; s < stages && s < issued; ++s) {
+    const int last_use = (issued - 1 - s) / stages;  // uses of stage s: j = s, s + stages, ...
+    int zero = 0;
+    mbar_wait(&ctl->full[s], last_use & 1, &zero);
+  }
+}
+
+// ------------------------------------------------------------ gate/up, FP8 -----------------
+// Work item = (tile of <= kStreamRows rows, 16 output columns n of gate and of up).  The
+// stage holds the 16 gate rows, the 16 up rows and the tile's activation rows (E4M3), all of
+// length d.  MMA warp w covers k in [w*d/4, (w+1)*d/4); the four partial sums meet in shared
+// memory; the epilogue forms h = silu(g) u and folds |h| into the row maxima (atomicMax on
+// the bit pattern, valid for non-negative floats).
+constexpr int kGuStages = 2;
+
+__global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int* status_flags) {
+  extern __shared__ __align__(128) uint8_t gu_smem[];
+  const int rs = a.d + kRowPad;
+  const size_t stage_bytes = size_t(48) * rs;
+  float (*red)[kTG][2][4][32] =
+      reinterpret_cast<float (*)[kTG][2][4][32]>(gu_smem + kGuStages * stage_bytes);
+  PipeCtl* ctl = reinterpret_cast<PipeCtl*>(gu_smem + kGuStages * stage_bytes + sizeof(float) * kConsumerWarps * kTG * 2 * 4 * 32);
+  pipe_init(ctl, kGuStages);
   const int n_tiles = *a.n_tiles;
   const int nblk = a.F / 16;
+  const int total = n_tiles * nblk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == kConsumerWarps) {  // ---------------- producer
+    const uint64_t pol = policy_evict_first();
+    int j = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+      const int s = j % kGuStages, use = j / kGuStages;
+      if (!mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort)) {
+        if (lane == 0) report_timeout(status_flags, 1);
+        break;
+      }
+      const Tile tl = a.tiles[item / nblk];
+      const int n0 = (item % nblk) * 16;
+      const uint8_t* Wg = tl.group == a.E ? a.sh_wgu : a.wgu + size_t(tl.group) * 2 * a.F * a.d;
+      uint8_t* st = gu_smem + s * stage_bytes;
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->full[s], uint32_t((32 + tl.nrows) * a.d));
+      __syncwarp();
+      // lanes 0..15: gate rows n0 + lane; lanes 16..31: up rows n0 + lane - 16
+      const uint8_t* src = Wg + (lane < 16 ? size_t(n0 + lane) : size_t(a.F + n0 + lane - 16)) * a.d;
+      bulk_g2s_stream(st + lane * rs, src, a.d, &ctl->full[s], pol);
+      if (lane < tl.nrows) bulk_g2s(st + (32 + lane) * rs, a.xq + size_t(tl.row0 + lane) * a.d, a.d, &ctl->full[s]);
+    }
+    pipe_drain(ctl, kGuStages, j);
+    return;
+  }
+
+  // ---------------- MMA warps
   const int gq = lane >> 2, tig = lane & 3;
-  const int kq = a.d / kKSplit;
-  for (int item = blockIdx.x; item < n_tiles * nblk; item += gridDim.x) {
+  const int kq = a.d / kConsumerWarps;
+  int j = 0;
+  for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+    const int s = j % kGuStages, use = j / kGuStages;
+    if (!mbar_wait(&ctl->full[s], use & 1, &ctl->abort)) {
+      if (lane == 0) report_timeout(status_flags, 2);
+      break;
+    }
     const Tile tl = a.tiles[item / nblk];
     const int n0 = (item % nblk) * 16;
-    const bool shared = tl.group == a.E;
-    const uint8_t* Wg = shared ? a.sh_wgu : a.wgu + size_t(tl.group) * 2 * a.F * a.d;
-    const uint8_t* Wu = Wg + size_t(a.F) * a.d;
-    const size_t koff = size_t(warp) * kq + tig * 16;
-    const uint8_t* pg0 = Wg + size_t(n0 + gq) * a.d + koff;
-    const uint8_t* pg1 = pg0 + size_t(8) * a.d;
-    const uint8_t* pu0 = Wu + size_t(n0 + gq) * a.d + koff;
-    const uint8_t* pu1 = pu0 + size_t(8) * a.d;
     const int ntg = (tl.nrows + 7) >> 3;
-    const uint8_t* px[4];
-    bool vx[4];
+    const uint8_t* st = gu_smem + s * stage_bytes;
+    const int koff = warp * kq + tig * 16;
+    float acc[kTG][2][4];
 #pragma unroll
-    for (int tg = 0; tg < 4; ++tg) {
-      const int r = tg * 8 + gq;
-      vx[tg] = r < tl.nrows;
-      px[tg] = a.xq + size_t(tl.row0 + (vx[tg] ? r : 0)) * a.d + koff;
-    }
-    float acc[4][2][4];
+    for (int tg = 0; tg < kTG; ++tg)
 #pragma unroll
-    for (int tg = 0; tg < 4; ++tg)
+      for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+        for (int c = 0; c < 4; ++c) acc[tg][jj][c] = 0.0f;
+    for (int ks = 0; ks < kq; ks += 64) {
+      const uint4 g0 = *reinterpret_cast<const uint4*>(st + gq * rs + koff + ks);
+      const uint4 g1 = *reinterpret_cast<const uint4*>(st + (gq + 8) * rs + koff + ks);
+      const uint4 u0 = *reinterpret_cast<const uint4*>(st + (16 + gq) * rs + koff + ks);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(st + (24 + gq) * rs + koff + ks);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[tg][j][c] = 0.0f;
-    for (int ks = 0; ks < kq; ks += 4 * 64) {
-      uint4 wg0[4], wg1[4], wu0[4], wu1[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (ks + j * 64 < kq) {
-          wg0[j] = ld_stream_u4(pg0 + ks + j * 64);
-          wg1[j] = ld_stream_u4(pg1 + ks + j * 64);
-          wu0[j] = ld_stream_u4(pu0 + ks + j * 64);
-          wu1[j] = ld_stream_u4(pu1 + ks + j * 64);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (ks + j * 64 >= kq) break;
-#pragma unroll
-        for (int tg = 0; tg < 4; ++tg) {
-          if (tg < ntg) {
-            const uint4 xa = vx[tg] ? __ldg(reinterpret_cast<const uint4*>(px[tg] + ks + j * 64)) : make_uint4(0, 0, 0, 0);
-            mma_e4m3_16x8x32(acc[tg][0], wg0[j].x, wg1[j].x, wg0[j].y, wg1[j].y, xa.x, xa.y);
-            mma_e4m3_16x8x32(acc[tg][0], wg0[j].z, wg1[j].z, wg0[j].w, wg1[j].w, xa.z, xa.w);
-            mma_e4m3_16x8x32(acc[tg][1], wu0[j].x, wu1[j].x, wu0[j].y, wu1[j].y, xa.x, xa.y);
-            mma_e4m3_16x8x32(acc[tg][1], wu0[j].z, wu1[j].z, wu0[j].w, wu1[j].w, xa.z, xa.w);
-          }
+      for (int tg = 0; tg < kTG; ++tg) {
+        if (tg < ntg) {
+          const int r = tg * 8 + gq;
+          const uint4 xa = r < tl.nrows ? *reinterpret_cast<const uint4*>(st + (32 + r) * rs + koff + ks)
+                                        : make_uint4(0, 0, 0, 0);
+          mma_e4m3_16x8x32(acc[tg][0], g0.x, g1.x, g0.y, g1.y, xa.x, xa.y);
+          mma_e4m3_16x8x32(acc[tg][0], g0.z, g1.z, g0.w, g1.w, xa.z, xa.w);
+          mma_e4m3_16x8x32(acc[tg][1], u0.x, u1.x, u0.y, u1.y, xa.x, xa.y);
+          mma_e4m3_16x8x32(acc[tg][1], u0.z, u1.z, u0.w, u1.w, xa.z, xa.w);
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->empty[s]);
 #pragma unroll
-    for (int tg = 0; tg < 4; ++tg)
+    for (int tg = 0; tg < kTG; ++tg)
       if (tg < ntg)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) red[warp][tg][j][c][lane] = acc[tg][j][c];
-    __syncthreads();
+          for (int c = 0; c < 4; ++c) red[warp][tg][jj][c][lane] = acc[tg][jj][c];
+    named_bar_sync(1, kConsumerWarps * 32);
     const int tg = warp;
     if (tg < ntg) {
+      const bool shared = tl.group == a.E;
       const float* sg = shared ? a.sh_sgu : a.sgu + size_t(tl.group) * 2 * a.F;
       const float* su = sg + a.F;
+      float rmax[2] = {0.0f, 0.0f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float gsum = 0.0f, usum = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kKSplit; ++w) {
+        for (int w = 0; w < kConsumerWarps; ++w) {
           gsum += red[w][tg][0][c][lane];
           usum += red[w][tg][1][c][lane];
         }
@@ -205,99 +279,133 @@ __global__ void __launch_bounds__(128) k_gateup_fp8(ExpertArgs a) {
         const int n = n0 + gq + ((c & 2) ? 8 : 0);
         if (r < tl.nrows) {
           const int row = tl.row0 + r;
-          const float s = a.sx[row];
-          const float gv = gsum * s * sg[n];
-          const float uv = usum * s * su[n];
-          a.h[size_t(row) * a.F + n] = silu(gv) * uv;
+          const float sx = a.sx[row];
+          const float gv = gsum * sx * sg[n];
+          const float uv = usum * sx * su[n];
+          const float hv = silu(gv) * uv;
+          a.h[size_t(row) * a.F + n] = hv;
+          rmax[c & 1] = fmaxf(rmax[c & 1], fabsf(hv));
+        }
+      }
+      // max over the 8 lanes that share tig (the 16 columns of this item), then one atomic
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        rmax[0] = fmaxf(rmax[0], __shfl_xor_sync(0xffffffffu, rmax[0], o));
+        rmax[1] = fmaxf(rmax[1], __shfl_xor_sync(0xffffffffu, rmax[1], o));
+      }
+      if (gq == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = tg * 8 + tig * 2 + i;
+          if (r < tl.nrows)
+            atomicMax(reinterpret_cast<unsigned*>(a.hmax) + tl.row0 + r, __float_as_uint(rmax[i]));
         }
       }
     }
-    __syncthreads();
+    named_bar_sync(1, kConsumerWarps * 32);
   }
 }
 
 // ------------------------------------------------------------ h quantisation ---------------
-// One warp per row of a tile: sh = max|h| / 448 (1 if zero), qh = E4M3(h / sh).
+// Elementwise over the tiles' rows: sh = max|h| / 448 (1 if zero; the maxima come from the
+// gate/up epilogue), qh = E4M3(h / sh).
 __global__ void __launch_bounds__(256) k_hquant(ExpertArgs a, int rows_per_tile) {
   const int n_tiles = *a.n_tiles;
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (int item = warp; item < n_tiles * rows_per_tile; item += nwarps) {
-    const Tile tl = a.tiles[item / rows_per_tile];
-    const int r = item % rows_per_tile;
+  const int per_row = a.F / 4;
+  const long long total = (long long)n_tiles * rows_per_tile * per_row;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const int tile = int(i / ((long long)rows_per_tile * per_row));
+    const int r = int(i / per_row % rows_per_tile);
+    const int n = int(i % per_row) * 4;
+    const Tile tl = a.tiles[tile];
     if (r >= tl.nrows) continue;
     const int row = tl.row0 + r;
-    const float* hr = a.h + size_t(row) * a.F;
-    float amax = 0.0f;
-    for (int n = lane * 4; n < a.F; n += 128) {
-      float4 v = *reinterpret_cast<const float4*>(hr + n);
-      amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fmaxf(fabsf(v.z), fabsf(v.w)), amax));
-    }
-    amax = warp_max(amax);
-    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    for (int n = lane * 4; n < a.F; n += 128) {
-      float4 v = *reinterpret_cast<const float4*>(hr + n);
-      uint32_t q = uint32_t(e4m3_code2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))) |
-                   (uint32_t(e4m3_code2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s))) << 16);
-      *reinterpret_cast<uint32_t*>(a.qh + size_t(row) * a.F + n) = q;
-    }
-    if (lane == 0) a.sh[row] = s;
+    const float mx = a.hmax[row];
+    const float s = mx > 0.0f ? __fdiv_rn(mx, 448.0f) : 1.0f;
+    const float4 v = *reinterpret_cast<const float4*>(a.h + size_t(row) * a.F + n);
+    const uint32_t q = uint32_t(e4m3_code2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))) |
+                       (uint32_t(e4m3_code2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s))) << 16);
+    *reinterpret_cast<uint32_t*>(a.qh + size_t(row) * a.F + n) = q;
+    if (n == 0) a.sh[row] = s;
   }
 }
 
 // ------------------------------------------------------------ down, FP8 --------------------
-// CTA = (tile of <= 32 rows, 64 output columns m); warp w owns 16 of the m columns and the
-// whole k = ffn range.
-__global__ void __launch_bounds__(128) k_down_fp8(ExpertArgs a) {
+// Work item = (tile of <= kStreamRows rows, 64 output columns m).  The stage holds the 64
+// weight rows (length ffn) and the tile's quantised h rows; MMA warp w owns 16 of the m
+// columns and the whole k = ffn range, so no cross-warp reduction is needed.
+constexpr int kDnStages = 4;
+
+__global__ void __launch_bounds__(kStreamThreads) k_down_fp8(ExpertArgs a, int* status_flags) {
+  extern __shared__ __align__(128) uint8_t dn_smem[];
+  const int rs = a.F + kRowPad;
+  const size_t stage_bytes = size_t(64 + kStreamRows) * rs;
+  PipeCtl* ctl = reinterpret_cast<PipeCtl*>(dn_smem + kDnStages * stage_bytes);
+  pipe_init(ctl, kDnStages);
   const int n_tiles = *a.n_tiles;
   const int nblk = a.d / 64;
+  const int total = n_tiles * nblk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tig = lane & 3;
-  for (int item = blockIdx.x; item < n_tiles * nblk; item += gridDim.x) {
-    const Tile tl = a.tiles[item / nblk];
-    const int m0 = (item % nblk) * 64 + warp * 16;
-    const bool shared = tl.group == a.E;
-    const uint8_t* W = shared ? a.sh_wd : a.wd + size_t(tl.group) * a.d * a.F;
-    const float* sdn = shared ? a.sh_sd : a.sd + size_t(tl.group) * a.d;
-    const uint8_t* p0 = W + size_t(m0 + gq) * a.F + tig * 16;
-    const uint8_t* p1 = p0 + size_t(8) * a.F;
-    const int ntg = (tl.nrows + 7) >> 3;
-    const uint8_t* px[4];
-    bool vx[4];
-#pragma unroll
-    for (int tg = 0; tg < 4; ++tg) {
-      const int r = tg * 8 + gq;
-      vx[tg] = r < tl.nrows;
-      px[tg] = a.qh + size_t(tl.row0 + (vx[tg] ? r : 0)) * a.F + tig * 16;
+
+  if (warp == kConsumerWarps) {  // ---------------- producer
+    const uint64_t pol = policy_evict_first();
+    int j = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+      const int s = j % kDnStages, use = j / kDnStages;
+      if (!mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort)) {
+        if (lane == 0) report_timeout(status_flags, 3);
+        break;
+      }
+      const Tile tl = a.tiles[item / nblk];
+      const int m0 = (item % nblk) * 64;
+      const uint8_t* W = tl.group == a.E ? a.sh_wd : a.wd + size_t(tl.group) * a.d * a.F;
+      uint8_t* st = dn_smem + s * stage_bytes;
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->full[s], uint32_t((64 + tl.nrows) * a.F));
+      __syncwarp();
+      bulk_g2s_stream(st + lane * rs, W + size_t(m0 + lane) * a.F, a.F, &ctl->full[s], pol);
+      bulk_g2s_stream(st + (32 + lane) * rs, W + size_t(m0 + 32 + lane) * a.F, a.F, &ctl->full[s], pol);
+      if (lane < tl.nrows) bulk_g2s(st + (64 + lane) * rs, a.qh + size_t(tl.row0 + lane) * a.F, a.F, &ctl->full[s]);
     }
-    float acc[4][4];
+    pipe_drain(ctl, kDnStages, j);
+    return;
+  }
+
+  const int gq = lane >> 2, tig = lane & 3;
+  int j = 0;
+  for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+    const int s = j % kDnStages, use = j / kDnStages;
+    if (!mbar_wait(&ctl->full[s], use & 1, &ctl->abort)) {
+      if (lane == 0) report_timeout(status_flags, 4);
+      break;
+    }
+    const Tile tl = a.tiles[item / nblk];
+    const int mw = warp * 16;  // this warp's columns within the item
+    const int m0 = (item % nblk) * 64 + mw;
+    const int ntg = (tl.nrows + 7) >> 3;
+    const uint8_t* st = dn_smem + s * stage_bytes;
+    float acc[kTG][4];
 #pragma unroll
-    for (int tg = 0; tg < 4; ++tg)
+    for (int tg = 0; tg < kTG; ++tg)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[tg][c] = 0.0f;
-    for (int ks = 0; ks < a.F; ks += 5 * 64) {
-      uint4 w0[5], w1[5];
+    for (int ks = tig * 16; ks < a.F; ks += 64) {
+      const uint4 w0 = *reinterpret_cast<const uint4*>(st + (mw + gq) * rs + ks);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(st + (mw + gq + 8) * rs + ks);
 #pragma unroll
-      for (int j = 0; j < 5; ++j)
-        if (ks + j * 64 < a.F) {
-          w0[j] = ld_stream_u4(p0 + ks + j * 64);
-          w1[j] = ld_stream_u4(p1 + ks + j * 64);
-        }
-#pragma unroll
-      for (int j = 0; j < 5; ++j) {
-        if (ks + j * 64 >= a.F) break;
-#pragma unroll
-        for (int tg = 0; tg < 4; ++tg) {
-          if (tg < ntg) {
-            const uint4 xa = vx[tg] ? __ldg(reinterpret_cast<const uint4*>(px[tg] + ks + j * 64)) : make_uint4(0, 0, 0, 0);
-            mma_e4m3_16x8x32(acc[tg], w0[j].x, w1[j].x, w0[j].y, w1[j].y, xa.x, xa.y);
-            mma_e4m3_16x8x32(acc[tg], w0[j].z, w1[j].z, w0[j].w, w1[j].w, xa.z, xa.w);
-          }
+      for (int tg = 0; tg < kTG; ++tg) {
+        if (tg < ntg) {
+          const int r = tg * 8 + gq;
+          const uint4 xa = r < tl.nrows ? *reinterpret_cast<const uint4*>(st + (64 + r) * rs + ks) : make_uint4(0, 0, 0, 0);
+          mma_e4m3_16x8x32(acc[tg], w0.x, w1.x, w0.y, w1.y, xa.x, xa.y);
+          mma_e4m3_16x8x32(acc[tg], w0.z, w1.z, w0.w, w1.w, xa.z, xa.w);
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->empty[s]);
+    const float* sdn = tl.group == a.E ? a.sh_sd : a.sd + size_t(tl.group) * a.d;
 #pragma unroll
-    for (int tg = 0; tg < 4; ++tg) {
+    for (int tg = 0; tg < kTG; ++tg) {
       if (tg >= ntg) continue;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -425,13 +533,13 @@ int num_sms() {
 }  // namespace
 
 cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
-                             float* sx, cudaStream_t s) {
+                             float* sx, float* hmax, cudaStream_t s) {
   if (x_bf16) {
-    if (L.fp8) k_act_quant<__nv_bfloat16, true><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
-    else k_act_quant<__nv_bfloat16, false><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
+    if (L.fp8) k_act_quant<__nv_bfloat16, true><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx, hmax);
+    else k_act_quant<__nv_bfloat16, false><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx, hmax);
   } else {
-    if (L.fp8) k_act_quant<float, true><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
-    else k_act_quant<float, false><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
+    if (L.fp8) k_act_quant<float, true><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx, hmax);
+    else k_act_quant<float, false><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx, hmax);
   }
   return cudaGetLastError();
 }
@@ -455,6 +563,7 @@ ExpertArgs expert_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.xq = reinterpret_cast<const uint8_t*>(base + ws.xq);
   a.sx = reinterpret_cast<const float*>(base + ws.sx);
   a.h = reinterpret_cast<float*>(base + ws.h);
+  a.hmax = reinterpret_cast<float*>(base + ws.hmax);
   a.qh = reinterpret_cast<uint8_t*>(base + ws.qh);
   a.sh = reinterpret_cast<float*>(base + ws.sh);
   a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
@@ -468,25 +577,37 @@ long long max_stream_tiles(const LayerDev& L, int T) {
 }
 }  // namespace
 
+size_t gateup_smem(int d) {
+  return size_t(kGuStages) * 48 * (d + kRowPad) + sizeof(float) * kConsumerWarps * kTG * 2 * 4 * 32 + sizeof(PipeCtl);
+}
+size_t down_smem(int F) { return size_t(kDnStages) * (64 + kStreamRows) * (F + kRowPad) + sizeof(PipeCtl); }
+
 cudaError_t launch_gateup_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
   const ExpertArgs a = expert_args(L, ws, base);
   const long long tiles = max_stream_tiles(L, T);
   const int sms = num_sms();
   if (L.fp8) {
+    const size_t smem = gateup_smem(L.d);
+    static cudaError_t attr = cudaFuncSetAttribute(k_gateup_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(gateup_smem(2048)));
+    if (attr != cudaSuccess) return attr;
     const long long items = tiles * (L.F / 16);
-    k_gateup_fp8<<<int(std::min<long long>(items, (long long)sms * 16)), 128, 0, s>>>(a);
-  } else {
-    const long long items = tiles * L.F / 8;
-    k_gateup_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
+    int* flags = reinterpret_cast<int*>(base + ws.status);
+    k_gateup_fp8<<<int(std::min<long long>(items, sms)), kStreamThreads, smem, s>>>(a, flags);
+    return cudaGetLastError();
   }
+  const long long items = tiles * L.F / 8;
+  k_gateup_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, int rows_per_tile, cudaStream_t s) {
   if (!L.fp8) return cudaSuccess;
   const ExpertArgs a = expert_args(L, ws, base);
-  const long long items = max_stream_tiles(L, T) * kStreamRows / 8;
-  k_hquant<<<int(std::min<long long>(items, (long long)num_sms() * 8)), 256, 0, s>>>(a, kStreamRows);
+  const long long R = (long long)T * (L.k + 1);
+  const long long tiles = std::min<long long>(R, L.E + 1) + R / rows_per_tile;
+  const long long total = tiles * rows_per_tile * (L.F / 4);
+  k_hquant<<<int(std::min<long long>((total + 255) / 256, (long long)num_sms() * 8)), 256, 0, s>>>(a, rows_per_tile);
   return cudaGetLastError();
 }
 
@@ -495,12 +616,17 @@ cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, cha
   const long long tiles = max_stream_tiles(L, T);
   const int sms = num_sms();
   if (L.fp8) {
+    const size_t smem = down_smem(L.F);
+    static cudaError_t attr = cudaFuncSetAttribute(k_down_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(down_smem(640)));
+    if (attr != cudaSuccess) return attr;
     const long long items = tiles * (L.d / 64);
-    k_down_fp8<<<int(std::min<long long>(items, (long long)sms * 16)), 128, 0, s>>>(a);
-  } else {
-    const long long items = tiles * L.d / 8;
-    k_down_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
+    int* flags = reinterpret_cast<int*>(base + ws.status);
+    k_down_fp8<<<int(std::min<long long>(items, sms)), kStreamThreads, smem, s>>>(a, flags);
+    return cudaGetLastError();
   }
+  const long long items = tiles * L.d / 8;
+  k_down_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,463 @@
+// Grouped FP8 expert GEMMs on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// The experts are SwitchGLU FFNs with E4M3 weights and one fp32 scale per output row
+// ("We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.", section 3, and the
+// E4M3 checkpoint of the vllm.cpp Kolibri-1 CPU FP8 pull request); activations enter each
+// contraction as per-row E4M3 codes (W8A8).
+//
+// One kernel shape serves decode and prefill ("swap-AB"): the A operand (M = 128) is a block
+// of 128 weight rows, the B operand (N = kN) is a tile of up to kN token rows of one expert
+// group, D[weight row][token] accumulates in TMEM in fp32.  Gate/up issues two MMAs per
+// k-step (gate and up rows of the same 128 outputs) into two accumulators, so the epilogue
+// sees g and u side by side and writes h = silu(g) u directly.  Down produces
+// y_e[token][m] for 128 output columns m.
+//
+// Warp roles (192 threads): warp 0 lane 0 issues TMA loads into a ring of shared-memory
+// stages (128-byte swizzle, the layout the MMA descriptors name); warp 1 owns the TMEM
+// allocation and its lane 0 issues tcgen05.mma and tcgen05.commit (the commit frees a stage
+// when its MMAs have read it, and marks an accumulator ready after the last k-step); warps
+// 2-5 (one per TMEM lane quarter) read the accumulators with tcgen05.ld and write the
+// outputs.  Accumulators are double-buffered when TMEM has room, so an item's epilogue
+// overlaps the next item's MMAs.  Every wait is bounded (tma.cuh): on a timeout the CTA
+// records MOE_ERR_TIMEOUT, all roles leave their loops, the producer waits for its loads in
+// flight, the MMA issuer waits for its MMAs, and TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "tma.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kTileM = 128;       // weight rows per item (MMA M)
+constexpr int kKTile = 128;       // bytes (= E4M3 elements) of k per stage: one 128-byte swizzle atom
+constexpr int kATileBytes = kTileM * kKTile;
+constexpr size_t kTcSmemBudget = 200 * 1024;
+
+// ---------------------------------------------------------------- PTX wrappers ------------
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], "
+      "[%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, E4M3 x E4M3 -> fp32, shape from idesc.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// This warp's 32 TMEM lanes x 16 consecutive 32-bit columns starting at taddr.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored with the 128-byte swizzle (rows
+// of 128 bytes, groups of 8 rows 1024 bytes apart, tile base 1024-byte aligned):
+// start address >> 4 in bits 0-13, stride byte offset 1024 >> 4 in bits 32-45, descriptor
+// version 1 in bits 46-47, layout SWIZZLE_128B (2) in bits 61-63.  The leading byte offset
+// is not used by swizzled K-major layouts.  Stepping k by 32 bytes inside the atom adds 2
+// to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(const void* smem_tile) {
+  const uint32_t addr = smem_u32(smem_tile);
+  uint64_t d = uint64_t((addr >> 4) & 0x3FFFu);
+  d |= uint64_t(1) << 16;
+  d |= uint64_t(1024 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f8f6f4: fp32 accumulator (bits 4-5 = 1), A and B E4M3
+// (format 0 in bits 7-9 and 10-12), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+struct TcArgs {
+  int d, F, E;
+  const Tile* tiles;
+  const int* n_tiles;
+  const float* sx;      // [R] activation scales (gate/up)
+  const float* sgu;     // [E, 2, F]
+  const float* sh_sgu;  // [2, F]
+  const float* sd;      // [E, d]
+  const float* sh_sd;   // [d]
+  float* h;             // [R, F]
+  float* hmax;          // [R]
+  const float* sh;      // [R] h scales (down)
+  float* y_rows;        // [R, d]
+  int* status_flags;
+};
+
+template <int kN, bool kGateUp>
+struct TcCfg {
+  static constexpr int kA = kGateUp ? 2 : 1;                         // A tiles per stage
+  static constexpr int kStageBytes = kA * kATileBytes + kN * kKTile;
+  static constexpr int kStages = int(std::min<size_t>(8, kTcSmemBudget / kStageBytes));
+  static constexpr int kColsPerAcc = kA * kN;
+  static constexpr int kBufs = (2 * kColsPerAcc <= 512) ? 2 : 1;
+  static constexpr int kTmemCols = (kBufs * kColsPerAcc <= 32)    ? 32
+                                   : (kBufs * kColsPerAcc <= 64)  ? 64
+                                   : (kBufs * kColsPerAcc <= 128) ? 128
+                                   : (kBufs * kColsPerAcc <= 256) ? 256
+                                                                  : 512;
+  static constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 /* alignment slack */ + 256 /* control */;
+};
+
+struct TcCtl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int kN, bool kGateUp>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_expert_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_wsh,
+                const __grid_constant__ CUtensorMap map_x, TcArgs a) {
+  using C = TcCfg<kN, kGateUp>;
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  TcCtl* ctl = reinterpret_cast<TcCtl*>(smem + size_t(C::kStages) * C::kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->acc_full[b], 1);
+      mbar_init(&ctl->acc_empty[b], 4);
+    }
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  const int n_tiles = *a.n_tiles;
+  const int nblk = (kGateUp ? a.F : a.d) / kTileM;   // weight-row blocks per group
+  const int KT = (kGateUp ? a.d : a.F) / kKTile;      // k-steps per item
+  const int total = n_tiles * nblk;
+  auto stage_a = [&](int s, int i) { return smem + size_t(s) * C::kStageBytes + i * kATileBytes; };
+  auto stage_b = [&](int s) { return smem + size_t(s) * C::kStageBytes + C::kA * kATileBytes; };
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------------ TMA producer
+      const uint64_t pol = policy_evict_first();
+      int it = 0;
+      bool stop = false;
+      for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+        const Tile tl = a.tiles[item / nblk];
+        const int nb = item % nblk;
+        const bool shared = tl.group == a.E;
+        const CUtensorMap* mw = shared ? &map_wsh : &map_w;
+        const int wrow = (shared ? 0 : tl.group * (kGateUp ? 2 * a.F : a.d)) + nb * kTileM;
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int s = it % C::kStages, use = it / C::kStages;
+          if (!mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort)) {
+            report_timeout_flag(a.status_flags, 11);
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctl->full[s], C::kStageBytes);
+          tma_load_2d_hint(stage_a(s, 0), mw, kt * kKTile, wrow, &ctl->full[s], pol);
+          if (kGateUp) tma_load_2d_hint(stage_a(s, 1), mw, kt * kKTile, wrow + a.F, &ctl->full[s], pol);
+          tma_load_2d(stage_b(s), &map_x, kt * kKTile, tl.row0, &ctl->full[s]);
+        }
+      }
+      // wait for the loads still in flight (bounded, regardless of abort)
+      for (int s = 0; s < C::kStages && s < it; ++s) {
+        const int last_use = (it - 1 - s) / C::kStages;
+        int zero = 0;
+        mbar_wait(&ctl->full[s], last_use & 1, &zero);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_e4m3(kTileM, kN);
+      int it = 0, jt = 0;
+      bool stop = false;
+      for (int item = blockIdx.x; item < total && !stop; item += gridDim.x, ++jt) {
+        const int b = jt % C::kBufs, ub = jt / C::kBufs;
+        if (!mbar_wait(&ctl->acc_empty[b], (ub & 1) ^ 1, &ctl->abort)) {
+          report_timeout_flag(a.status_flags, 12);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem + uint32_t(b * C::kColsPerAcc);
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int s = it % C::kStages, use = it / C::kStages;
+          if (!mbar_wait(&ctl->full[s], use & 1, &ctl->abort)) {
+            report_timeout_flag(a.status_flags, 13);
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da0 = sw128_desc(stage_a(s, 0));
+          const uint64_t da1 = kGateUp ? sw128_desc(stage_a(s, 1)) : 0;
+          const uint64_t db = sw128_desc(stage_b(s));
+#pragma unroll
+          for (int kk = 0; kk < kKTile / 32; ++kk) {
+            const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+            tc_mma_f8(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            if (kGateUp) tc_mma_f8(d0 + kN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+          }
+          tc_commit(&ctl->empty[s]);
+        }
+        if (!stop) tc_commit(&ctl->acc_full[b]);
+      }
+      // every MMA issued has completed before TMEM is released
+      tc_commit(&ctl->mma_done);
+      int zero = 0;
+      mbar_wait(&ctl->mma_done, 0, &zero);
+    }
+  } else {  // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int rloc = q * 32 + lane;
+    int jt = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++jt) {
+      const int b = jt % C::kBufs, ub = jt / C::kBufs;
+      if (!mbar_wait(&ctl->acc_full[b], ub & 1, &ctl->abort)) {
+        if (lane == 0) report_timeout_flag(a.status_flags, 14);
+        break;
+      }
+      tc_fence_after();
+      const Tile tl = a.tiles[item / nblk];
+      const int nb = item % nblk;
+      const bool shared = tl.group == a.E;
+      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(b * C::kColsPerAcc);
+      if (kGateUp) {
+        const int n = nb * kTileM + rloc;
+        const float* sgp = shared ? a.sh_sgu : a.sgu + size_t(tl.group) * 2 * a.F;
+        const float sg = sgp[n], su = sgp[a.F + n];
+        for (int c0 = 0; c0 < kN && c0 < tl.nrows; c0 += 16) {
+          float gv[16], uv[16];
+          tmem_ld16(taddr + c0, gv);
+          tmem_ld16(taddr + kN + c0, uv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int t = c0 + i;
+            if (t < tl.nrows) {  // uniform across the warp
+              const int row = tl.row0 + t;
+              const float sx = a.sx[row];
+              const float gq = gv[i] * sx * sg;
+              const float uq = uv[i] * sx * su;
+              const float hv = silu(gq) * uq;
+              a.h[size_t(row) * a.F + n] = hv;
+              const float m = warp_max(fabsf(hv));
+              if (lane == 0) atomicMax(reinterpret_cast<unsigned*>(a.hmax) + row, __float_as_uint(m));
+            }
+          }
+        }
+      } else {
+        const int m = nb * kTileM + rloc;
+        const float sdm = shared ? a.sh_sd[m] : a.sd[size_t(tl.group) * a.d + m];
+        for (int c0 = 0; c0 < kN && c0 < tl.nrows; c0 += 16) {
+          float yv[16];
+          tmem_ld16(taddr + c0, yv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int t = c0 + i;
+            if (t < tl.nrows) {
+              const int row = tl.row0 + t;
+              a.y_rows[size_t(row) * a.d + m] = yv[i] * a.sh[row] * sdm;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->acc_empty[b]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side --------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] uint8 tensor, boxes of box_rows x 128 bytes, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {uint32_t(kKTile), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
+template <int kN, bool kGateUp>
+cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mwsh, const CUtensorMap& mx, const TcArgs& a,
+                      long long max_items, cudaStream_t s) {
+  using C = TcCfg<kN, kGateUp>;
+  static cudaError_t attr =
+      cudaFuncSetAttribute(k_expert_tc<kN, kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
+  if (attr != cudaSuccess) return attr;
+  const int grid = int(std::max<long long>(1, std::min<long long>(max_items, sm_count())));
+  k_expert_tc<kN, kGateUp><<<grid, kTcThreads, C::kSmemBytes, s>>>(mw, mwsh, mx, a);
+  return cudaGetLastError();
+}
+
+template <bool kGateUp>
+cudaError_t launch_tc_n(int kN, const CUtensorMap& mw, const CUtensorMap& mwsh, const CUtensorMap& mx,
+                        const TcArgs& a, long long max_items, cudaStream_t s) {
+  switch (kN) {
+    case 16: return launch_tc<16, kGateUp>(mw, mwsh, mx, a, max_items, s);
+    case 32: return launch_tc<32, kGateUp>(mw, mwsh, mx, a, max_items, s);
+    case 64: return launch_tc<64, kGateUp>(mw, mwsh, mx, a, max_items, s);
+    case 128: return launch_tc<128, kGateUp>(mw, mwsh, mx, a, max_items, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+TcArgs tc_args(const LayerDev& L, const WsLayout& ws, char* base) {
+  TcArgs a;
+  a.d = L.d;
+  a.F = L.F;
+  a.E = L.E;
+  a.tiles = reinterpret_cast<const Tile*>(base + ws.tiles);
+  a.n_tiles = reinterpret_cast<const int*>(base + ws.n_tiles);
+  a.sx = reinterpret_cast<const float*>(base + ws.sx);
+  a.sgu = L.sgu;
+  a.sh_sgu = L.sh_sgu;
+  a.sd = L.sd;
+  a.sh_sd = L.sh_sd;
+  a.h = reinterpret_cast<float*>(base + ws.h);
+  a.hmax = reinterpret_cast<float*>(base + ws.hmax);
+  a.sh = reinterpret_cast<const float*>(base + ws.sh);
+  a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
+  a.status_flags = reinterpret_cast<int*>(base + ws.status);
+  return a;
+}
+
+long long max_tc_tiles(const LayerDev& L, int T, int kN) {
+  const long long R = (long long)T * (L.k + 1);
+  return std::min<long long>(R, L.E + 1) + R / kN;
+}
+
+}  // namespace
+
+bool tc_supported(const LayerDev& L) { return L.fp8 && L.d % 128 == 0 && L.F % 128 == 0 && encode_fn() != nullptr; }
+
+int tc_rows_per_tile(int T) {
+  if (T <= 64) return 16;
+  if (T <= 256) return 32;
+  if (T <= 1024) return 64;
+  return 128;
+}
+
+cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  const int kN = tc_rows_per_tile(T);
+  CUtensorMap mw, mwsh, mx;
+  if (!make_map(&mw, L.wgu, uint64_t(L.E) * 2 * L.F, L.d, kTileM) ||
+      !make_map(&mwsh, L.sh_wgu, uint64_t(2) * L.F, L.d, kTileM) ||
+      !make_map(&mx, base + ws.xq, uint64_t(ws.R_alloc), L.d, kN))
+    return cudaErrorInvalidValue;
+  const long long items = max_tc_tiles(L, T, kN) * (L.F / kTileM);
+  return launch_tc_n<true>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, s);
+}
+
+cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  const int kN = tc_rows_per_tile(T);
+  CUtensorMap mw, mwsh, mx;
+  if (!make_map(&mw, L.wd, uint64_t(L.E) * L.d, L.F, kTileM) ||
+      !make_map(&mwsh, L.sh_wd, uint64_t(L.d), L.F, kTileM) ||
+      !make_map(&mx, base + ws.qh, uint64_t(ws.R_alloc), L.F, kN))
+    return cudaErrorInvalidValue;
+  const long long items = max_tc_tiles(L, T, kN) * (L.d / kTileM);
+  return launch_tc_n<false>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, s);
+}
+
+}  // namespace moe

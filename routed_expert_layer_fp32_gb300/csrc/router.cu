@@ -59,6 +59,87 @@ __global__ void __launch_bounds__(256) k_router_warp(const XT* __restrict__ x, i
   }
 }
 
+// Decode-sized router (T <= kRouterSplitMaxT): split over k so that every SM gets work.
+// CTA (expert block of 32, k-slice of 128) stages Wr[32][128] and x[T][128] in shared
+// memory and writes partial sums part[slice][t][e].  The last CTA of an expert block to
+// finish (a counter in the status record, reset after use) adds the slices in slice order
+// plus the bias, so the logits do not depend on which CTA finished last.
+constexpr int kRsE = 32, kRsK = kRouterSplitK;
+constexpr int kMaxRouterSlices = 2048 / kRouterSplitK;  // d <= 2048 on the split path
+template <typename XT>
+__global__ void __launch_bounds__(256) k_router_split(const XT* __restrict__ x, int T, int d, int E,
+                                                      const float* __restrict__ Wr, const float* __restrict__ bias,
+                                                      float* __restrict__ part, float* __restrict__ logits,
+                                                      DevStatus* st) {
+  __shared__ unsigned s_last;
+  extern __shared__ __align__(16) float rs_smem[];
+  float (*ws)[kRsK + 4] = reinterpret_cast<float (*)[kRsK + 4]>(rs_smem);
+  float (*xs)[kRsK + 4] = reinterpret_cast<float (*)[kRsK + 4]>(rs_smem + kRsE * (kRsK + 4));
+  const int e0 = blockIdx.x * kRsE, k0 = blockIdx.y * kRsK;
+  const int tid = threadIdx.x;
+  // Wr slice: 32 rows x 128 floats, float4 per thread per pass
+  for (int i = tid; i < kRsE * kRsK / 4; i += blockDim.x) {
+    const int r = i / (kRsK / 4), c = (i % (kRsK / 4)) * 4;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (e0 + r < E) load4(Wr + size_t(e0 + r) * d + k0 + c, v);
+    *reinterpret_cast<float4*>(&ws[r][c]) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  for (int i = tid; i < T * kRsK / 4; i += blockDim.x) {
+    const int t = i / (kRsK / 4), c = (i % (kRsK / 4)) * 4;
+    float v[4];
+    load4(x + size_t(t) * d + k0 + c, v);
+    *reinterpret_cast<float4*>(&xs[t][c]) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  __syncthreads();
+  const int e = tid & 31, tg = tid >> 5;  // lane = expert, warp = token group (t = tg + 8j)
+  constexpr int kMaxJ = kRouterSplitMaxT / 8;
+  float acc[kMaxJ];
+#pragma unroll
+  for (int j = 0; j < kMaxJ; ++j) acc[j] = 0.0f;
+#pragma unroll 4
+  for (int c = 0; c < kRsK; c += 4) {
+    const float4 wv = *reinterpret_cast<const float4*>(&ws[e][c]);
+#pragma unroll
+    for (int j = 0; j < kMaxJ; ++j) {
+      const int t = tg + 8 * j;
+      if (t < T) {
+        const float4 xv = *reinterpret_cast<const float4*>(&xs[t][c]);
+        acc[j] = fmaf(xv.x, wv.x, acc[j]);
+        acc[j] = fmaf(xv.y, wv.y, acc[j]);
+        acc[j] = fmaf(xv.z, wv.z, acc[j]);
+        acc[j] = fmaf(xv.w, wv.w, acc[j]);
+      }
+    }
+  }
+  if (e0 + e < E) {
+#pragma unroll
+    for (int j = 0; j < kMaxJ; ++j) {
+      const int t = tg + 8 * j;
+      if (t < T) part[(size_t(blockIdx.y) * T + t) * E + e0 + e] = acc[j];
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&st->router_done[blockIdx.x], 1u) == gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int n_part = gridDim.y;  // <= kMaxRouterSlices
+  for (int i = tid; i < T * kRsE; i += blockDim.x) {
+    const int t = i / kRsE, ee = e0 + i % kRsE;
+    if (ee >= E) continue;
+    float v[kMaxRouterSlices];
+#pragma unroll
+    for (int p = 0; p < kMaxRouterSlices; ++p) v[p] = p < n_part ? __ldcg(part + (size_t(p) * T + t) * E + ee) : 0.0f;
+    float sum = v[0];
+#pragma unroll
+    for (int p = 1; p < kMaxRouterSlices; ++p)
+      if (p < n_part) sum += v[p];
+    logits[size_t(t) * E + ee] = sum + (bias ? bias[ee] : 0.0f);
+  }
+  if (tid == 0) st->router_done[blockIdx.x] = 0;
+}
+
 // Prefill-sized router: SIMT tiled GEMM, 64 tokens x 64 experts per CTA, 4x4 per thread.
 template <typename XT>
 __global__ void __launch_bounds__(256) k_router_gemm(const XT* __restrict__ x, int T, int d, int E,
@@ -118,12 +199,23 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 // expert (softmax is monotone in the logit, so selecting on logits selects on
 // probabilities); forced routing validates the given ids.  Weights: softmax over the k
 // selected logits, or forced_w as given.
-__global__ void __launch_bounds__(256) k_select(const float* __restrict__ logits, const int32_t* __restrict__ forced_ids,
+__global__ void __launch_bounds__(256) k_select(const float* __restrict__ logits,
+                                                const int32_t* __restrict__ forced_ids,
                                                 const float* __restrict__ forced_w, int T, int E, int k,
                                                 int32_t* __restrict__ ids, float* __restrict__ w, DevStatus* st) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
+  // lane-local logits of experts lane + 32 j
+  constexpr int kPer = kMaxExperts / 32;
+  float v[kPer];
+  if (!(forced_ids && forced_w)) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = e < E ? logits[size_t(t) * E + e] : -INFINITY;
+    }
+  }
   int sel = -1;     // lane i < k holds slot i's expert
   float lsel = 0.f; // and its logit
   if (forced_ids) {
@@ -147,14 +239,20 @@ __global__ void __launch_bounds__(256) k_select(const float* __restrict__ logits
       }
       return;
     }
-    if (sel >= 0) lsel = logits[size_t(t) * E + sel];
-  } else {
-    const float* lg = logits + size_t(t) * E;
-    constexpr int kPer = kMaxExperts / 32;
-    float v[kPer];
-    unsigned taken = 0;
+    // each forced expert's logit, fetched from the lane that holds it
+    for (int i = 0; i < k; ++i) {
+      const int ei = __shfl_sync(0xffffffffu, sel, i);
+      float li = 0.0f;
+      if (ei >= 0) {
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) v[j] = (lane + 32 * j < E) ? lg[lane + 32 * j] : -INFINITY;
+        for (int j = 0; j < kPer; ++j)
+          if (ei == lane + 32 * j) li = v[j];
+        li = __shfl_sync(0xffffffffu, li, ei & 31);
+      }
+      if (lane == i) lsel = li;
+    }
+  } else {
+    unsigned taken = 0;
     for (int r = 0; r < k; ++r) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
@@ -205,6 +303,25 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
     else
       k_router_gemm<float><<<grid, 256, 0, s>>>((const float*)x, T, L.d, L.E, L.Wr, L.bias, logits);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_split(const void* x, bool x_bf16, int T, const LayerDev& L, float* part, float* logits,
+                                DevStatus* st, cudaStream_t s) {
+  constexpr int most = (kRsE + kRouterSplitMaxT) * (kRsK + 4) * int(sizeof(float));
+  static cudaError_t attr = [] {
+    cudaError_t e1 = cudaFuncSetAttribute(k_router_split<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaError_t e2 = cudaFuncSetAttribute(k_router_split<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    return e1 != cudaSuccess ? e1 : e2;
+  }();
+  if (attr != cudaSuccess) return attr;
+  const size_t smem = size_t(kRsE + T) * (kRsK + 4) * sizeof(float);
+  dim3 grid((L.E + kRsE - 1) / kRsE, L.d / kRsK);
+  if (x_bf16)
+    k_router_split<__nv_bfloat16><<<grid, 256, smem, s>>>((const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias, part,
+                                                          logits, st);
+  else
+    k_router_split<float><<<grid, 256, smem, s>>>((const float*)x, T, L.d, L.E, L.Wr, L.bias, part, logits, st);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,9 @@ from tests.gpu_helpers import check_forced_layer, check_free_layer, oracle_route
 
 pytestmark = pytest.mark.gpu
 
+# expert kernels: weight-streaming warp-MMA path, or the tcgen05 grouped GEMM
+PATHS = {"stream": 1, "tc": 2}
+
 
 @pytest.fixture(scope="module")
 def moe():
@@ -144,30 +147,32 @@ def test_tiny_fp32_layer_free_then_forced(moe, tiny):
     assert moe.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("T", [1, 8, 64])
-def test_decode_layer(moe, kolibri, T):
+def test_decode_layer(moe, kolibri, T, path):
     w, L = kolibri
     x = g.make_x(g.SEED_DECODE, T, w.d, bf16=True)
     ws = moe.workspace(L, T)
-    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
-    _, msg, _ = check_free_layer(w, x, y, ids, wt, where=f"decode T={T}")
-    print(f"T={T}: {msg}")
-    y_bf, _, _ = moe.forward(to_dev_x(x), L, ws, y_dtype=torch.bfloat16)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws, flags=PATHS[path])
+    _, msg, _ = check_free_layer(w, x, y, ids, wt, where=f"decode T={T} {path}")
+    print(f"T={T} {path}: {msg}")
+    y_bf, _, _ = moe.forward(to_dev_x(x), L, ws, y_dtype=torch.bfloat16, flags=PATHS[path])
     assert torch.allclose(y_bf.float(), y, rtol=1e-2, atol=1e-2 * y.abs().max().item())
     assert moe.get_status(ws) == 0
 
 
-def test_prefill_2048_free_then_4x512_forced(moe, kolibri):
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_prefill_2048_free_then_4x512_forced(moe, kolibri, path):
     w, L = kolibri
     T = 2048
     x = g.make_x(g.SEED_PREFILL, T, w.d, bf16=True)
     ws = moe.workspace(L, T)
-    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
-    check_free_layer(w, x, y, ids, wt, where="prefill 2048 free")
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws, flags=PATHS[path])
+    check_free_layer(w, x, y, ids, wt, where=f"prefill 2048 free {path}")
     ys = []
     for c in range(4):
         sl = slice(512 * c, 512 * (c + 1))
-        yc, idc, _ = moe.forward(to_dev_x(x[sl]), L, ws, forced_ids=ids[sl].contiguous())
+        yc, idc, _ = moe.forward(to_dev_x(x[sl]), L, ws, forced_ids=ids[sl].contiguous(), flags=PATHS[path])
         assert torch.equal(idc, ids[sl]), "forced ids must be used bit-exactly"
         ys.append(yc)
     ych = torch.cat(ys)
@@ -176,7 +181,8 @@ def test_prefill_2048_free_then_4x512_forced(moe, kolibri):
     check_forced_layer(w, x, ids.cpu().numpy(), None, ych, ids, where="prefill 4x512 forced")
 
 
-def test_batched_decode_zipf_forced(moe, kolibri):
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_batched_decode_zipf_forced(moe, kolibri, path):
     w, L = kolibri
     T = 128
     x = g.make_x(g.SEED_ZIPF, T, w.d, bf16=True)
@@ -184,18 +190,19 @@ def test_batched_decode_zipf_forced(moe, kolibri):
     fw = g.dirichlet_w(g.SEED_ZIPF, 0, T, 6)
     ws = moe.workspace(L, T)
     y, ids, wt = moe.forward(to_dev_x(x), L, ws, forced_ids=torch.from_numpy(fid).cuda(),
-                             forced_w=torch.from_numpy(fw).cuda())
+                             forced_w=torch.from_numpy(fw).cuda(), flags=PATHS[path])
     assert np.array_equal(wt.cpu().numpy(), fw)
     _, msg = check_forced_layer(w, x, fid, fw, y, ids, where="zipf T=128")
     print(msg)
 
 
-@pytest.mark.parametrize("T", [0, 37, 333])
-def test_ragged_token_counts(moe, kolibri, T):
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("T", [0, 37, 333, 1500])
+def test_ragged_token_counts(moe, kolibri, T, path):
     w, L = kolibri
     x = g.make_x(77, max(T, 1), w.d, bf16=True)[:T]
     ws = moe.workspace(L, max(T, 1))
-    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws, flags=PATHS[path])
     if T == 0:
         assert y.shape == (0, w.d)
         return
