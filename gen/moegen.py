@@ -150,10 +150,13 @@ class LayerWeights:
 
 
 def make_layer(seed: int, d: int, ffn: int, E: int, fp8: bool, bias_var: Optional[float],
-               layer: int = 0, nthreads: Optional[int] = None, out: Optional[dict] = None) -> LayerWeights:
+               layer: int = 0, nthreads: Optional[int] = None, out: Optional[dict] = None,
+               down_var: Optional[float] = None) -> LayerWeights:
     """One layer's weights from the recipe above.  `out` may supply preallocated arrays
-    (e.g. pinned host buffers) keyed like the LayerWeights fields."""
+    (e.g. pinned host buffers) keyed like the LayerWeights fields.  `down_var` replaces the
+    down-projection variance 1/ffn (used by the stack, see stack_layer)."""
     nt = nthreads or default_threads()
+    dv = down_var if down_var is not None else 1.0 / ffn
     o = out or {}
     Wr = normal_f32(seed, layer, T_WR, (E, d), 1.0 / d, out=o.get("Wr"), nthreads=nt)
     bias = normal_f32(seed, layer, T_BIAS, (E,), bias_var, out=o.get("bias"), nthreads=nt) if bias_var else None
@@ -164,7 +167,7 @@ def make_layer(seed: int, d: int, ffn: int, E: int, fp8: bool, bias_var: Optiona
                          Wgu.reshape(E * 2 * ffn, d), sgu.reshape(-1), nthreads=nt)
         Wd = o.get("Wd", np.empty((E, d, ffn), np.uint8))
         sd = o.get("sd", np.empty((E, d), np.float32))
-        normal_e4m3_rows(seed, layer, T_WD, 0, E * d, ffn, 1.0 / ffn, Wd.reshape(E * d, ffn), sd.reshape(-1),
+        normal_e4m3_rows(seed, layer, T_WD, 0, E * d, ffn, dv, Wd.reshape(E * d, ffn), sd.reshape(-1),
                          nthreads=nt)
         sh_Wgu = o.get("sh_Wgu", np.empty((2, ffn, d), np.uint8))
         sh_sgu = o.get("sh_sgu", np.empty((2, ffn), np.float32))
@@ -172,12 +175,12 @@ def make_layer(seed: int, d: int, ffn: int, E: int, fp8: bool, bias_var: Optiona
                          sh_sgu.reshape(-1), nthreads=nt)
         sh_Wd = o.get("sh_Wd", np.empty((d, ffn), np.uint8))
         sh_sd = o.get("sh_sd", np.empty((d,), np.float32))
-        normal_e4m3_rows(seed, layer, T_SH_WD, 0, d, ffn, 1.0 / ffn, sh_Wd, sh_sd, nthreads=nt)
+        normal_e4m3_rows(seed, layer, T_SH_WD, 0, d, ffn, dv, sh_Wd, sh_sd, nthreads=nt)
         return LayerWeights(d, ffn, E, True, Wr, bias, Wgu, Wd, sh_Wgu, sh_Wd, sgu, sd, sh_sgu, sh_sd)
     Wgu = normal_f32(seed, layer, T_WGU, (E, 2, ffn, d), 1.0 / d, nthreads=nt)
-    Wd = normal_f32(seed, layer, T_WD, (E, d, ffn), 1.0 / ffn, nthreads=nt)
+    Wd = normal_f32(seed, layer, T_WD, (E, d, ffn), dv, nthreads=nt)
     sh_Wgu = normal_f32(seed, layer, T_SH_WGU, (2, ffn, d), 1.0 / d, nthreads=nt)
-    sh_Wd = normal_f32(seed, layer, T_SH_WD, (d, ffn), 1.0 / ffn, nthreads=nt)
+    sh_Wd = normal_f32(seed, layer, T_SH_WD, (d, ffn), dv, nthreads=nt)
     return LayerWeights(d, ffn, E, False, Wr, bias, Wgu, Wd, sh_Wgu, sh_Wd)
 
 
@@ -208,10 +211,53 @@ def tiny_layer():
     return make_layer(SEED_TINY, TINY["d"], TINY["ffn"], TINY["E"], fp8=False, bias_var=None)
 
 
-def kolibri_layer(seed: int, layer: int = 0, out=None, nthreads=None):
+def kolibri_layer(seed: int, layer: int = 0, out=None, nthreads=None, down_var=None):
     return make_layer(seed, KOLIBRI["d"], KOLIBRI["ffn"], KOLIBRI["E"], fp8=True, bias_var=0.5,
-                      layer=layer, out=out, nthreads=nthreads)
+                      layer=layer, out=out, nthreads=nthreads, down_var=down_var)
+
+
+# The 50-layer stack applies r <- r + moe(r) with no normalisation; with the single-layer
+# recipe (down projection ~ N(0, 1/ffn)) the residual grows doubly exponentially (the SwiGLU
+# is quadratic in x for large x) and overflows fp32 after 8 layers.  The stack therefore
+# scales every residual-branch output projection (routed and shared down weights) by
+# 1/sqrt(L), the initialisation Radford et al. use for deep residual stacks (GPT-2, 2019,
+# section 2.3): down ~ N(0, 1/(ffn * L)).
+STACK_LAYERS = 50
+STACK_DOWN_VAR = 1.0 / (KOLIBRI["ffn"] * STACK_LAYERS)
 
 
 def stack_layer(l: int, out=None, nthreads=None):
-    return kolibri_layer(STACK_LAYER_SEED0 + l, out=out, nthreads=nthreads)
+    return kolibri_layer(STACK_LAYER_SEED0 + l, out=out, nthreads=nthreads, down_var=STACK_DOWN_VAR)
+
+
+def sparse_layer(seed: int, experts, d: int = 2048, ffn: int = 640, E: int = 384, bias_var: float = 0.5,
+                 layer: int = 0, nthreads=None, down_var: Optional[float] = None) -> LayerWeights:
+    """The same layer as kolibri_layer(seed), but only the listed routed experts (plus the
+    router and the shared expert) are generated; the other experts' weight arrays are left
+    unwritten (allocated lazily, never read by a forced-route evaluation that avoids them).
+    Every stream is counter-based, so each generated row equals the full layer's row."""
+    nt = nthreads or default_threads()
+    dv = down_var if down_var is not None else 1.0 / ffn
+    Wr = normal_f32(seed, layer, T_WR, (E, d), 1.0 / d, nthreads=nt)
+    bias = normal_f32(seed, layer, T_BIAS, (E,), bias_var, nthreads=nt) if bias_var else None
+    Wgu = np.empty((E, 2, ffn, d), np.uint8)
+    sgu = np.zeros((E, 2, ffn), np.float32)
+    Wd = np.empty((E, d, ffn), np.uint8)
+    sd = np.zeros((E, d), np.float32)
+    for e in sorted(set(int(v) for v in experts)):
+        normal_e4m3_rows(seed, layer, T_WGU, e * 2 * ffn, 2 * ffn, d, 1.0 / d, Wgu[e].reshape(2 * ffn, d),
+                         sgu[e].reshape(-1), nthreads=nt)
+        normal_e4m3_rows(seed, layer, T_WD, e * d, d, ffn, dv, Wd[e], sd[e], nthreads=nt)
+    sh_Wgu = np.empty((2, ffn, d), np.uint8)
+    sh_sgu = np.empty((2, ffn), np.float32)
+    normal_e4m3_rows(seed, layer, T_SH_WGU, 0, 2 * ffn, d, 1.0 / d, sh_Wgu.reshape(2 * ffn, d), sh_sgu.reshape(-1),
+                     nthreads=nt)
+    sh_Wd = np.empty((d, ffn), np.uint8)
+    sh_sd = np.empty((d,), np.float32)
+    normal_e4m3_rows(seed, layer, T_SH_WD, 0, d, ffn, dv, sh_Wd, sh_sd, nthreads=nt)
+    return LayerWeights(d, ffn, E, True, Wr, bias, Wgu, Wd, sh_Wgu, sh_Wd, sgu, sd, sh_sgu, sh_sd)
+
+
+def stack_x(T: int, start_token: int = 0):
+    """Residual stream input of the 50-layer stack: bf16 N(0,1), seed 5."""
+    return make_x(SEED_STACK_X, T, KOLIBRI["d"], bf16=True, start_token=start_token)
