@@ -97,8 +97,12 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   MOE_TRY(mark(0));
   float* part = reinterpret_cast<float*>(base + lay.router_part);
   if (!(forced_ids && forced_w)) {
-    if (T <= kRouterSplitMaxT && L.d <= 2048) MOE_TRY(launch_router_split(x, x_bf16, T, L, part, logits, st, s));
-    else MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
+    if (T <= kRouterSplitMaxT && L.d <= 2048)
+      MOE_TRY(launch_router_split(x, x_bf16, T, L, part, logits, st, s));
+    else if (T > kRouterSplitMaxT && router_tc_supported(L, x_bf16))
+      MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits, st, s));
+    else
+      MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
   }
   MOE_TRY(mark(1));
   MOE_TRY(launch_select(logits, forced_ids, forced_w, T, L, ids, w, st, s));
@@ -152,6 +156,8 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
   if (T <= kRouterSplitMaxT && L.d <= 2048)
     MOE_TRY(launch_router_split(x, x_dtype == MOE_BF16, T, L, reinterpret_cast<float*>(base + lay.router_part), logits,
                                 st, s));
+  else if (T > kRouterSplitMaxT && router_tc_supported(L, x_dtype == MOE_BF16))
+    MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits, st, s));
   else
     MOE_TRY(launch_router_logits(x, x_dtype == MOE_BF16, T, L, logits, s));
   MOE_TRY(launch_select(logits, nullptr, nullptr, T, L, ids_out, w_out, st, s));

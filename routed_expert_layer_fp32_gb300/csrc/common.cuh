@@ -33,7 +33,7 @@ struct Tile {
 
 // Where each buffer lives inside the caller's workspace, for T tokens.
 struct WsLayout {
-  size_t status, logits, router_part, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h, hmax,
+  size_t status, logits, router_part, router_w3, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h, hmax,
       qh, sh, y_rows;
   size_t total;
   int T, R, R_alloc, n_chunks, max_tiles;
@@ -61,6 +61,7 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   w.status = take(sizeof(DevStatus));
   w.logits = take(size_t(T) * E * 4);
   w.router_part = take(T <= kRouterSplitMaxT ? size_t(d / kRouterSplitK) * T * E * 4 : 0);
+  w.router_w3 = take(T > kRouterSplitMaxT ? size_t(3) * E * d * 2 : 0);  // bf16 split of Wr
   w.ids = take(size_t(T) * k * 4);
   w.w = take(size_t(T) * k * 4);
   w.counts = take(size_t(E + 1) * 4);
@@ -178,6 +179,10 @@ struct LayerDev {
 cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
 cudaError_t launch_select(const float* logits, const int32_t* forced_ids, const float* forced_w, int T,
                           const LayerDev& L, int32_t* ids, float* w, DevStatus* st, cudaStream_t s);
+// Prefill router on tensor cores (bf16 x, Wr split into three bf16 terms in w3 [3, E, d]).
+bool router_tc_supported(const LayerDev& L, bool x_bf16);
+cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, DevStatus* st,
+                             cudaStream_t s);
 // Decode router (T <= kRouterSplitMaxT): d/kRouterSplitK partial slices [n][T][E] in `part`,
 // summed in slice order (plus bias) into logits [T][E] by the last CTA of each expert block.
 cudaError_t launch_router_split(const void* x, bool x_bf16, int T, const LayerDev& L, float* part, float* logits,

@@ -1,0 +1,218 @@
+// Prefill router on the tensor cores with fp32 accuracy.
+//
+// The router is float32 ("We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said
+// No.", section "The gate": a bf16 router is one of the planted bugs).  Activations arrive in
+// bf16, so x is exact in bf16; the fp32 router weights are split per call into three bf16
+// terms, w = hi + mid + lo (+ a remainder below 2^-24 |w|): hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid), where both differences are exact in fp32.  Every product of bf16
+// values is exact in fp32, so three accumulating bf16 MMAs with an fp32 accumulator give
+// x . w to fp32 accuracy.
+//
+// Tile: 128 tokens (M) x all experts, the experts split into two MMAs of n_half columns
+// (E = 384: 2 x 192) so one TMEM accumulator row holds a token's full logit row.  Stage =
+// one 64-element (128-byte) k-slice of x and of one weight term; warp roles as in the expert
+// GEMMs (TMA producer, single-thread MMA issuer, four epilogue warps); bounded waits.
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRtThreads = 192;
+constexpr int kRtM = 128;
+constexpr int kRtATile = kRtM * 128;
+constexpr size_t kRtSmemBudget = 200 * 1024;
+
+__global__ void k_router_split_w(const float* __restrict__ Wr, long long n, __nv_bfloat16* __restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float w = Wr[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    out[i] = hi;
+    out[n + i] = mid;
+    out[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+struct RtCtl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kRtThreads, 1)
+    k_router_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                const float* __restrict__ bias, int T, int d, int E, int n_half, int n_stages, int tmem_cols,
+                float* __restrict__ logits, int* status_flags) {
+  extern __shared__ uint8_t rt_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int b_half_bytes = n_half * 128;
+  const int stage_bytes = kRtATile + 2 * b_half_bytes;
+  RtCtl* ctl = reinterpret_cast<RtCtl*>(smem + size_t(n_stages) * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < n_stages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->acc_empty, 4);
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int n_items = (T + kRtM - 1) / kRtM;
+  const int KT = d / 64;  // 64 bf16 per 128-byte k-slice
+  auto sa = [&](int s) { return smem + size_t(s) * stage_bytes; };
+  auto sb = [&](int s, int h) { return smem + size_t(s) * stage_bytes + kRtATile + h * b_half_bytes; };
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer: stage = (k-slice, weight term)
+      int it = 0;
+      bool stop = false;
+      for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
+        for (int kt = 0; kt < KT && !stop; ++kt) {
+          for (int term = 0; term < 3; ++term, ++it) {
+            const int s = it % n_stages, use = it / n_stages;
+            if (!mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort)) {
+              report_timeout_flag(status_flags, 21);
+              stop = true;
+              break;
+            }
+            mbar_arrive_expect_tx(&ctl->full[s], stage_bytes);
+            tma_load_2d(sa(s), &map_x, kt * 64, item * kRtM, &ctl->full[s]);
+            tma_load_2d(sb(s, 0), &map_w, kt * 64, term * E, &ctl->full[s]);
+            tma_load_2d(sb(s, 1), &map_w, kt * 64, term * E + n_half, &ctl->full[s]);
+          }
+        }
+      }
+      for (int s = 0; s < n_stages && s < it; ++s) {
+        int zero = 0;
+        mbar_wait(&ctl->full[s], ((it - 1 - s) / n_stages) & 1, &zero);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t idesc = idesc_bf16(kRtM, n_half);
+      int it = 0, jt = 0;
+      bool stop = false;
+      for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x, ++jt) {
+        if (!mbar_wait(&ctl->acc_empty, (jt & 1) ^ 1, &ctl->abort)) {
+          report_timeout_flag(status_flags, 22);
+          break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < KT && !stop; ++kt) {
+          for (int term = 0; term < 3; ++term, ++it) {
+            const int s = it % n_stages, use = it / n_stages;
+            if (!mbar_wait(&ctl->full[s], use & 1, &ctl->abort)) {
+              report_timeout_flag(status_flags, 23);
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t da = sw128_desc(sa(s));
+            const uint64_t db0 = sw128_desc(sb(s, 0)), db1 = sw128_desc(sb(s, 1));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {  // 16 bf16 (32 bytes) per MMA
+              const uint32_t acc = (kt > 0 || term > 0 || kk > 0) ? 1u : 0u;
+              tc_mma_f16(tmem, da + 2 * kk, db0 + 2 * kk, idesc, acc);
+              tc_mma_f16(tmem + uint32_t(n_half), da + 2 * kk, db1 + 2 * kk, idesc, acc);
+            }
+            tc_commit(&ctl->empty[s]);
+          }
+        }
+        if (!stop) tc_commit(&ctl->acc_full);
+      }
+      tc_commit(&ctl->mma_done);
+      int zero = 0;
+      mbar_wait(&ctl->mma_done, 0, &zero);
+    }
+  } else {  // epilogue: one token per TMEM lane, logits = acc + bias
+    const int q = warp & 3;
+    int jt = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++jt) {
+      if (!mbar_wait(&ctl->acc_full, jt & 1, &ctl->abort)) {
+        if (lane == 0) report_timeout_flag(status_flags, 24);
+        break;
+      }
+      tc_fence_after();
+      const int t = item * kRtM + q * 32 + lane;
+      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16);
+      for (int c0 = 0; c0 < 2 * n_half && c0 < E; c0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + c0, v);
+        if (t < T) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int e = c0 + i;
+            if (e < E) logits[size_t(t) * E + e] = v[i] + (bias ? bias[e] : 0.0f);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->acc_empty);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+int rt_sm_count() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
+}  // namespace
+
+bool router_tc_supported(const LayerDev& L, bool x_bf16) {
+  return x_bf16 && L.d % 64 == 0 && L.E <= 512 && L.E % 32 == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, DevStatus* st,
+                             cudaStream_t s) {
+  const long long n = (long long)L.E * L.d;
+  k_router_split_w<<<int(std::min<long long>((n + 255) / 256, 4096)), 256, 0, s>>>(L.Wr, n, w3);
+  const int n_half = ((L.E / 2) + 15) / 16 * 16;
+  const int stage_bytes = kRtATile + 2 * n_half * 128;
+  const int n_stages = int(std::min<size_t>(8, kRtSmemBudget / stage_bytes));
+  const int tmem_cols = 2 * n_half <= 256 ? 256 : 512;
+  CUtensorMap mx, mw;
+  if (!make_map_bytes(&mx, x, uint64_t(T), uint64_t(L.d), kRtM, 2) ||
+      !make_map_bytes(&mw, w3, uint64_t(3) * L.E, uint64_t(L.d), uint32_t(n_half), 2))
+    return cudaErrorInvalidValue;
+  const size_t smem = size_t(n_stages) * stage_bytes + 1024 + 256;
+  static cudaError_t attr = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (attr != cudaSuccess) return attr;
+  const int items = (T + kRtM - 1) / kRtM;
+  k_router_tc<<<std::min(items, rt_sm_count()), kRtThreads, smem, s>>>(mx, mw, L.bias, T, L.d, L.E, n_half, n_stages,
+                                                                      tmem_cols, logits, &st->flags);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -62,7 +62,7 @@ def test_device_e4m3_encoder_matches_oracle(moe):
 
 # ------------------------------------------------------------------------ router ---------
 
-@pytest.mark.parametrize("T", [1, 8, 33, 64, 2048])
+@pytest.mark.parametrize("T", [1, 8, 33, 64, 129, 300, 2048])
 def test_router_logits_ids_weights(moe, kolibri, T):
     w, L = kolibri
     x = g.make_x(g.SEED_DECODE, T, w.d, bf16=True)
@@ -70,8 +70,11 @@ def test_router_logits_ids_weights(moe, kolibri, T):
     ids, wt, lg = moe.route(to_dev_x(x), L, ws, logits=True)
     ref = oracle_route(w, x)
     lg = lg.cpu().numpy()
+    # fp32 logits: both sides accumulate in fp32 in different orders (the prefill router sums
+    # three bf16 weight terms on the tensor cores); the bound is far below what moves a
+    # routing decision (near-ties within 1e-4 in probability)
     err = np.max(np.abs(lg - ref["logits"]), axis=1) / np.max(np.abs(ref["logits"]), axis=1)
-    assert err.max() < 1e-5, err.max()
+    assert err.max() < 3e-5, err.max()
     ok, bad, ndiff = parity.ids_ok(ids.cpu().numpy(), ref["ids"], ref["p"], w.E)
     assert ok, bad
     same = np.all(ids.cpu().numpy() == ref["ids"], axis=1)
