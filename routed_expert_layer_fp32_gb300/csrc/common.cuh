@@ -33,7 +33,7 @@ struct Tile {
 
 // Where each buffer lives inside the caller's workspace, for T tokens.
 struct WsLayout {
-  size_t status, logits, router_part, router_w3, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h, hmax,
+  size_t status, logits, router_part, router_w3, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h,
       qh, sh, y_rows;
   size_t total;
   int T, R, R_alloc, n_chunks, max_tiles;
@@ -74,7 +74,6 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   w.xq = take(size_t(w.R_alloc) * d * (f32w ? 4 : 1));
   w.sx = take(R * 4);
   w.h = take(R * F * 4);
-  w.hmax = take(R * 4);
   w.qh = take(size_t(w.R_alloc) * F);
   w.sh = take(R * 4);
   w.y_rows = take(R * d * 4);
@@ -192,7 +191,7 @@ cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_pe
                             char* base, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
                             cudaStream_t s);
 cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
-                             float* sx, float* hmax, cudaStream_t s);
+                             float* sx, cudaStream_t s);
 cudaError_t launch_gateup_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, int rows_per_tile, cudaStream_t s);
 // tcgen05 grouped GEMMs (prefill and decode): E4M3 weights with d % 128 == 0, ffn % 128 == 0.

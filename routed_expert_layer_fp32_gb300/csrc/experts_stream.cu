@@ -44,7 +44,7 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
 template <typename XT, bool kFp8>
 __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, int k,
                                                    const int32_t* __restrict__ pos, void* __restrict__ xq,
-                                                   float* __restrict__ sx, float* __restrict__ hmax) {
+                                                   float* __restrict__ sx) {
   __shared__ float red[8];
   const int t = blockIdx.x;
   const XT* xr = x + size_t(t) * d;
@@ -94,10 +94,7 @@ __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int
     }
   }
   if (threadIdx.x == 0)
-    for (int j = 0; j < nr; ++j) {
-      sx[rows[j]] = s;
-      hmax[rows[j]] = 0.0f;  // row maxima of h are accumulated by the gate/up kernel
-    }
+    for (int j = 0; j < nr; ++j) sx[rows[j]] = s;
 }
 
 // ------------------------------------------------------------ gate/up, FP8 -----------------
@@ -116,7 +113,6 @@ struct ExpertArgs {
   const uint8_t* xq;  // [R, d] E4M3 (or fp32 for the fp32 path)
   const float* sx;    // [R]
   float* h;           // [R, F]
-  float* hmax;        // [R]  max |h| of each row
   uint8_t* qh;        // [R, F]
   float* sh;          // [R]
   float* y_rows;      // [R, d]
@@ -170,8 +166,7 @@ __device__ __forceinline__ void pipe_drain(PipeCtl* ctl, int stages, int issued)
 // Work item = (tile of <= kStreamRows rows, 16 output columns n of gate and of up).  The
 // stage holds the 16 gate rows, the 16 up rows and the tile's activation rows (E4M3), all of
 // length d.  MMA warp w covers k in [w*d/4, (w+1)*d/4); the four partial sums meet in shared
-// memory; the epilogue forms h = silu(g) u and folds |h| into the row maxima (atomicMax on
-// the bit pattern, valid for non-negative floats).
+// memory; the epilogue forms h = silu(g) u.
 constexpr int kGuStages = 2;
 
 __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int* status_flags) {
@@ -266,7 +261,6 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
       const bool shared = tl.group == a.E;
       const float* sg = shared ? a.sh_sgu : a.sgu + size_t(tl.group) * 2 * a.F;
       const float* su = sg + a.F;
-      float rmax[2] = {0.0f, 0.0f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float gsum = 0.0f, usum = 0.0f;
@@ -282,23 +276,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
           const float sx = a.sx[row];
           const float gv = gsum * sx * sg[n];
           const float uv = usum * sx * su[n];
-          const float hv = silu(gv) * uv;
-          a.h[size_t(row) * a.F + n] = hv;
-          rmax[c & 1] = fmaxf(rmax[c & 1], fabsf(hv));
-        }
-      }
-      // max over the 8 lanes that share tig (the 16 columns of this item), then one atomic
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        rmax[0] = fmaxf(rmax[0], __shfl_xor_sync(0xffffffffu, rmax[0], o));
-        rmax[1] = fmaxf(rmax[1], __shfl_xor_sync(0xffffffffu, rmax[1], o));
-      }
-      if (gq == 0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int r = tg * 8 + tig * 2 + i;
-          if (r < tl.nrows)
-            atomicMax(reinterpret_cast<unsigned*>(a.hmax) + tl.row0 + r, __float_as_uint(rmax[i]));
+          a.h[size_t(row) * a.F + n] = silu(gv) * uv;
         }
       }
     }
@@ -307,26 +285,46 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
 }
 
 // ------------------------------------------------------------ h quantisation ---------------
-// Elementwise over the tiles' rows: sh = max|h| / 448 (1 if zero; the maxima come from the
-// gate/up epilogue), qh = E4M3(h / sh).
+// One warp per row of a tile: sh = max|h| / 448 (1 if the row is zero), qh = E4M3(h / sh).
 __global__ void __launch_bounds__(256) k_hquant(ExpertArgs a, int rows_per_tile) {
   const int n_tiles = *a.n_tiles;
-  const int per_row = a.F / 4;
-  const long long total = (long long)n_tiles * rows_per_tile * per_row;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
-    const int tile = int(i / ((long long)rows_per_tile * per_row));
-    const int r = int(i / per_row % rows_per_tile);
-    const int n = int(i % per_row) * 4;
-    const Tile tl = a.tiles[tile];
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long total = (long long)n_tiles * rows_per_tile;
+  for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < total; item += nwarps) {
+    const Tile tl = a.tiles[item / rows_per_tile];
+    const int r = int(item % rows_per_tile);
     if (r >= tl.nrows) continue;
     const int row = tl.row0 + r;
-    const float mx = a.hmax[row];
-    const float s = mx > 0.0f ? __fdiv_rn(mx, 448.0f) : 1.0f;
-    const float4 v = *reinterpret_cast<const float4*>(a.h + size_t(row) * a.F + n);
-    const uint32_t q = uint32_t(e4m3_code2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))) |
-                       (uint32_t(e4m3_code2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s))) << 16);
-    *reinterpret_cast<uint32_t*>(a.qh + size_t(row) * a.F + n) = q;
-    if (n == 0) a.sh[row] = s;
+    const float* hr = a.h + size_t(row) * a.F;
+    float4 v[5];  // ffn <= 640 = 5 x 32 lanes x 4
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+      const int n = (j * 32 + lane) * 4;
+      v[j] = n < a.F ? *reinterpret_cast<const float4*>(hr + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+      amax = fmaxf(fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))), amax);
+    }
+    for (int n = 640 + lane * 4; n < a.F; n += 128) {  // wider ffn: rare, second pass for the max
+      const float4 u = *reinterpret_cast<const float4*>(hr + n);
+      amax = fmaxf(fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))), amax);
+    }
+    amax = warp_max(amax);
+    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    uint8_t* qr = a.qh + size_t(row) * a.F;
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+      const int n = (j * 32 + lane) * 4;
+      if (n < a.F)
+        *reinterpret_cast<uint32_t*>(qr + n) = uint32_t(e4m3_code2(__fdiv_rn(v[j].x, s), __fdiv_rn(v[j].y, s))) |
+                                               (uint32_t(e4m3_code2(__fdiv_rn(v[j].z, s), __fdiv_rn(v[j].w, s))) << 16);
+    }
+    for (int n = 640 + lane * 4; n < a.F; n += 128) {
+      const float4 u = *reinterpret_cast<const float4*>(hr + n);
+      *reinterpret_cast<uint32_t*>(qr + n) = uint32_t(e4m3_code2(__fdiv_rn(u.x, s), __fdiv_rn(u.y, s))) |
+                                             (uint32_t(e4m3_code2(__fdiv_rn(u.z, s), __fdiv_rn(u.w, s))) << 16);
+    }
+    if (lane == 0) a.sh[row] = s;
   }
 }
 
@@ -533,13 +531,13 @@ int num_sms() {
 }  // namespace
 
 cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
-                             float* sx, float* hmax, cudaStream_t s) {
+                             float* sx, cudaStream_t s) {
   if (x_bf16) {
-    if (L.fp8) k_act_quant<__nv_bfloat16, true><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx, hmax);
-    else k_act_quant<__nv_bfloat16, false><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx, hmax);
+    if (L.fp8) k_act_quant<__nv_bfloat16, true><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
+    else k_act_quant<__nv_bfloat16, false><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
   } else {
-    if (L.fp8) k_act_quant<float, true><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx, hmax);
-    else k_act_quant<float, false><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx, hmax);
+    if (L.fp8) k_act_quant<float, true><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
+    else k_act_quant<float, false><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
   }
   return cudaGetLastError();
 }
@@ -563,7 +561,6 @@ ExpertArgs expert_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.xq = reinterpret_cast<const uint8_t*>(base + ws.xq);
   a.sx = reinterpret_cast<const float*>(base + ws.sx);
   a.h = reinterpret_cast<float*>(base + ws.h);
-  a.hmax = reinterpret_cast<float*>(base + ws.hmax);
   a.qh = reinterpret_cast<uint8_t*>(base + ws.qh);
   a.sh = reinterpret_cast<float*>(base + ws.sh);
   a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
@@ -606,8 +603,8 @@ cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* ba
   const ExpertArgs a = expert_args(L, ws, base);
   const long long R = (long long)T * (L.k + 1);
   const long long tiles = std::min<long long>(R, L.E + 1) + R / rows_per_tile;
-  const long long total = tiles * rows_per_tile * (L.F / 4);
-  k_hquant<<<int(std::min<long long>((total + 255) / 256, (long long)num_sms() * 8)), 256, 0, s>>>(a, rows_per_tile);
+  const long long warps = tiles * rows_per_tile;
+  k_hquant<<<int(std::min<long long>((warps + 7) / 8, (long long)num_sms() * 16)), 256, 0, s>>>(a, rows_per_tile);
   return cudaGetLastError();
 }
 

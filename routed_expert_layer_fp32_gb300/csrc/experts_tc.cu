@@ -9,15 +9,16 @@
 // of 128 weight rows, the B operand (N = kN) is a tile of up to kN token rows of one expert
 // group, D[weight row][token] accumulates in TMEM in fp32.  Gate/up issues two MMAs per
 // k-step (gate and up rows of the same 128 outputs) into two accumulators, so the epilogue
-// sees g and u side by side and writes h = silu(g) u directly.  Down produces
+// sees g and u side by side and writes h = silu(g) u directly (the per-row maximum of |h|
+// that scales its quantisation is taken afterwards, by the h-quantisation pass).  Down produces
 // y_e[token][m] for 128 output columns m.
 //
 // Warp roles (192 threads): warp 0 lane 0 issues TMA loads into a ring of shared-memory
 // stages (128-byte swizzle, the layout the MMA descriptors name); warp 1 owns the TMEM
 // allocation and its lane 0 issues tcgen05.mma and tcgen05.commit (the commit frees a stage
 // when its MMAs have read it, and marks an accumulator ready after the last k-step); warps
-// 2-5 (one per TMEM lane quarter) read the accumulators with tcgen05.ld and write the
-// outputs.  Accumulators are double-buffered when TMEM has room, so an item's epilogue
+// 2-9 (two per TMEM lane quarter, each half of the token columns) read the accumulators
+// with tcgen05.ld and write the outputs (h = silu(g) u for gate/up, scaled rows for down).  Accumulators are double-buffered when TMEM has room, so an item's epilogue
 // overlaps the next item's MMAs.  Every wait is bounded (tma.cuh): on a timeout the CTA
 // records MOE_ERR_TIMEOUT, all roles leave their loops, the producer waits for its loads in
 // flight, the MMA issuer waits for its MMAs, and TMEM is freed before the CTA exits.
@@ -30,7 +31,8 @@
 namespace moe {
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter, splitting the columns
+constexpr int kTcThreads = (2 + kEpiWarps) * 32;
 constexpr int kTileM = 128;       // weight rows per item (MMA M)
 constexpr int kKTile = 128;       // bytes (= E4M3 elements) of k per stage: one 128-byte swizzle atom
 constexpr int kATileBytes = kTileM * kKTile;
@@ -46,7 +48,6 @@ struct TcArgs {
   const float* sd;      // [E, d]
   const float* sh_sd;   // [d]
   float* h;             // [R, F]
-  float* hmax;          // [R]
   const float* sh;      // [R] h scales (down)
   float* y_rows;        // [R, d]
   int* status_flags;
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->acc_full[b], 1);
-      mbar_init(&ctl->acc_empty[b], 4);
+      mbar_init(&ctl->acc_empty[b], kEpiWarps);
     }
     mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
@@ -187,8 +188,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait(&ctl->mma_done, 0, &zero);
     }
   } else {  // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // warps 2..9: lane quarter q = warp % 4 (the TMEM lanes this warp may read), column half
+    // ch = (warp - 2) / 4 of the kN token columns
+    const int q = warp & 3, ch = (warp - 2) >> 2;
     const int rloc = q * 32 + lane;
+    constexpr int kHalf = kN / 2 >= 16 ? kN / 2 : 16;
+    const int cbeg = kN / 2 >= 16 ? ch * kHalf : (ch == 0 ? 0 : kN);  // kN = 16: one warp set
+    const int cend = kN / 2 >= 16 ? cbeg + kHalf : (ch == 0 ? kN : kN);
     int jt = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++jt) {
       const int b = jt % C::kBufs, ub = jt / C::kBufs;
@@ -205,37 +211,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int n = nb * kTileM + rloc;
         const float* sgp = shared ? a.sh_sgu : a.sgu + size_t(tl.group) * 2 * a.F;
         const float sg = sgp[n], su = sgp[a.F + n];
-        for (int c0 = 0; c0 < kN && c0 < tl.nrows; c0 += 16) {
+        for (int c0 = cbeg; c0 < cend && c0 < tl.nrows; c0 += 16) {
           float gv[16], uv[16];
           tmem_ld16(taddr + c0, gv);
           tmem_ld16(taddr + kN + c0, uv);
+          // lane i < 16 fetches the scale of token c0 + i; shuffles hand it to every lane
+          const float sx_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sx[tl.row0 + c0 + lane] : 0.0f;
+          float* hp = a.h + size_t(tl.row0 + c0) * a.F + n;
+          if (c0 + 16 <= tl.nrows) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int t = c0 + i;
-            if (t < tl.nrows) {  // uniform across the warp
-              const int row = tl.row0 + t;
-              const float sx = a.sx[row];
+            for (int i = 0; i < 16; ++i) {
+              const float sx = __shfl_sync(0xffffffffu, sx_l, i);
               const float gq = gv[i] * sx * sg;
               const float uq = uv[i] * sx * su;
-              const float hv = silu(gq) * uq;
-              a.h[size_t(row) * a.F + n] = hv;
-              const float m = warp_max(fabsf(hv));
-              if (lane == 0) atomicMax(reinterpret_cast<unsigned*>(a.hmax) + row, __float_as_uint(m));
+              hp[size_t(i) * a.F] = __fdividef(gq, 1.0f + expf(-gq)) * uq;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float sx = __shfl_sync(0xffffffffu, sx_l, i);
+              if (c0 + i < tl.nrows) {
+                const float gq = gv[i] * sx * sg;
+                const float uq = uv[i] * sx * su;
+                hp[size_t(i) * a.F] = __fdividef(gq, 1.0f + expf(-gq)) * uq;
+              }
             }
           }
         }
       } else {
         const int m = nb * kTileM + rloc;
         const float sdm = shared ? a.sh_sd[m] : a.sd[size_t(tl.group) * a.d + m];
-        for (int c0 = 0; c0 < kN && c0 < tl.nrows; c0 += 16) {
+        for (int c0 = cbeg; c0 < cend && c0 < tl.nrows; c0 += 16) {
           float yv[16];
           tmem_ld16(taddr + c0, yv);
+          const float sh_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sh[tl.row0 + c0 + lane] : 0.0f;
+          float* yp = a.y_rows + size_t(tl.row0 + c0) * a.d + m;
+          if (c0 + 16 <= tl.nrows) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int t = c0 + i;
-            if (t < tl.nrows) {
-              const int row = tl.row0 + t;
-              a.y_rows[size_t(row) * a.d + m] = yv[i] * a.sh[row] * sdm;
+            for (int i = 0; i < 16; ++i) yp[size_t(i) * a.d] = yv[i] * __shfl_sync(0xffffffffu, sh_l, i) * sdm;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float shv = __shfl_sync(0xffffffffu, sh_l, i);
+              if (c0 + i < tl.nrows) yp[size_t(i) * a.d] = yv[i] * shv * sdm;
             }
           }
         }
@@ -302,7 +320,6 @@ TcArgs tc_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.sd = L.sd;
   a.sh_sd = L.sh_sd;
   a.h = reinterpret_cast<float*>(base + ws.h);
-  a.hmax = reinterpret_cast<float*>(base + ws.hmax);
   a.sh = reinterpret_cast<const float*>(base + ws.sh);
   a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
   a.status_flags = reinterpret_cast<int*>(base + ws.status);
