@@ -37,7 +37,8 @@ ROUTER_BYTES = E * D * 4 + E * 4                         # fp32 router weights +
 GATEUP_EXPERT_BYTES = 2 * FFN * D + 2 * FFN * 4
 N_COPIES = 8
 HEADLINE_T = 64
-KERNELS_PER_FORWARD = 7  # router (split-k), select, dispatch, act_quant, gate_up, down, combine (FP8, T <= 128)
+KERNELS_PER_FORWARD = 8  # router, select, dispatch, act_quant, gate_up, h_quant, down, combine (T <= 1024)
+PATH_FLAGS = {"auto": 0, "stream": 1, "tc": 2}
 
 
 def parse_args():
@@ -50,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true", help="skip the batch-1/8 extras")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_COPIES, help="weight copies rotated across steps")
+    ap.add_argument("--path", choices=sorted(PATH_FLAGS), default="auto", help="expert kernels")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill extras")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 50-layer stack extras")
     return ap.parse_args()
 
 
@@ -60,6 +64,17 @@ def peaks():
             p = json.load(f)
         return float(p["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def fp8_peak():
+    """Dense FP8 tensor peak: the measured bf16 GEMM peak times the nominal fp8/bf16 ratio
+    (4.5 / 2.25 PFLOP/s = 2); burst figure for a kernel timed alone."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return 2.0 * float(p["bf16_tflops"]), "measured bf16 x 2 (nominal fp8/bf16)"
+    return 2.0 * 1900.0, "fallback bf16 x 2"
 
 
 class ClockSampler:
@@ -166,8 +181,10 @@ def run_ours(args):
     wt = torch.empty((T, K), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    flags = PATH_FLAGS[args.path]
+
     def step(i, ev=None):
-        moe.forward(x, layers[i % len(layers)], ws, out=y, ids=ids, w=wt, events=ev)
+        moe.forward(x, layers[i % len(layers)], ws, out=y, ids=ids, w=wt, events=ev, flags=flags)
 
     for i in range(args.warmup):
         step(i)
@@ -203,7 +220,8 @@ def run_ours(args):
     ms_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms / 1e3)
     gu_ms = stage_ms["gate_up"]
-    roof = {"bound": "hbm", "kernel": "k_gateup_fp8", "achieved": gu_bytes / (gu_ms * 1e-3) / 1e9,
+    gu_kernel = "k_gateup_fp8" if args.path == "stream" else "k_expert_tc<16,gate_up>"
+    roof = {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_bytes / (gu_ms * 1e-3) / 1e9,
             "peak": hbm_peak, "unit": "GB/s", "peak_kind": peak_kind,
             "frac": gu_bytes / (gu_ms * 1e-3) / 1e9 / hbm_peak, "traffic": None,
             "algorithmic_bytes_per_launch": gu_bytes, "launch_ms": gu_ms}
@@ -215,14 +233,14 @@ def run_ours(args):
     xd = torch.empty((T, D), dtype=torch.int16, device="cuda")
     for i in range(args.warmup):
         xd.copy_(x_pin, non_blocking=True)
-        moe.forward(xd.view(torch.bfloat16), layers[i % len(layers)], ws, out=y, ids=ids, w=wt)
+        moe.forward(xd.view(torch.bfloat16), layers[i % len(layers)], ws, out=y, ids=ids, w=wt, flags=flags)
         y_pin.copy_(y.view(torch.int16), non_blocking=True)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
         xd.copy_(x_pin, non_blocking=True)
-        moe.forward(xd.view(torch.bfloat16), layers[i % len(layers)], ws, out=y, ids=ids, w=wt)
+        moe.forward(xd.view(torch.bfloat16), layers[i % len(layers)], ws, out=y, ids=ids, w=wt, flags=flags)
         y_pin.copy_(y.view(torch.int16), non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -238,7 +256,14 @@ def run_ours(args):
              "stage_ms": stage_ms}
     if not args.no_extra:
         for Tx in (1, 8):
-            extra[f"decode_T{Tx}"] = small_batch(moe, g, layers, Tx, args, hbm_peak)
+            extra[f"decode_T{Tx}"] = small_batch(moe, g, layers, Tx, args, hbm_peak, flags)
+    if not args.no_prefill:
+        for Tx in (2048, 16384):
+            extra[f"prefill_T{Tx}"] = prefill(moe, g, layers[0], Tx, flags)
+    if not args.no_stack:
+        del layers[1:]
+        torch.cuda.empty_cache()
+        extra.update(stack_bench(moe, g, hbm_peak, flags))
 
     status = moe.get_status(ws)
     out = {
@@ -261,7 +286,86 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def small_batch(moe, g, layers, T, args, hbm_peak):
+def prefill(moe, g, layer, T, flags, warmup=3, iters=10):
+    """One prefill-sized layer call (free routing), eager launches, per-stage events.  The
+    expert FLOPs are 7T x 3 x 2 x d x ffn (six routed rows and one shared row per token)."""
+    import torch
+    peak, kind = fp8_peak()
+    x = torch.from_numpy(g.make_x(g.SEED_PREFILL, T, D, bf16=True).view(np.int16).copy()).cuda().view(torch.bfloat16)
+    ws = moe.workspace(layer, T)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    for _ in range(warmup):
+        moe.forward(x, layer, ws, out=y, flags=flags)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.binding.TRACE_POINTS)] for _ in range(iters)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for i in range(iters):
+        moe.forward(x, layer, ws, out=y, flags=flags, events=evs[i])
+    torch.cuda.synchronize()
+    total = statistics.mean(evs[i][0].elapsed_time(evs[i][-1]) for i in range(iters))
+    stage = {n: statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(iters))
+             for k, n in enumerate(moe.binding.TRACE_STAGES)}
+    flops = 7 * T * 3 * 2 * D * FFN
+    gemm_ms = stage["gate_up"] + stage["down"]
+    return {"tokens_per_s": T / (total * 1e-3), "ms_per_layer": total, "expert_tflops": flops / (total * 1e-3) / 1e12,
+            "fp8_frac": flops / (total * 1e-3) / 1e12 / peak, "gemm_fp8_frac": flops / (gemm_ms * 1e-3) / 1e12 / peak,
+            "fp8_peak_tflops": peak, "peak_kind": kind, "stage_ms": stage}
+
+
+def stack_bench(moe, g, hbm_peak, flags):
+    """The 50-layer stack (r <- bf16(r + moe(r)), free routing, ~76 GB of E4M3 weights
+    resident): decode with 32 tokens and a 16,384-token prefill, each one moe_forward_stack
+    call per step, timed with CUDA events (the residual is reset from the input every step)."""
+    import torch
+    t0 = time.time()
+    layers = [moe.Layer.from_host(g.stack_layer(l)) for l in range(g.STACK_LAYERS)]
+    gen_s = time.time() - t0
+    arr = moe.binding.layer_array(layers)
+    peak8, kind8 = fp8_peak()
+    out = {}
+    for T, iters in ((32, 20), (16384, 3)):
+        x = torch.from_numpy(g.stack_x(T).view(np.int16).copy()).cuda().view(torch.bfloat16)
+        r = x.clone()
+        ws = moe.workspace(layers[0], T)
+        ids = torch.empty((len(layers), T, K), dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            r.copy_(x)
+            moe.forward_stack(layers, r, ws, ids_out=ids, flags=flags, layer_arr=arr)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            r.copy_(x)
+            moe.forward_stack(layers, r, ws, ids_out=ids, flags=flags, layer_arr=arr)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        idh = ids.cpu().numpy()
+        us = [len(np.unique(idh[l])) for l in range(len(layers))]
+        if T == 32:
+            nbytes = sum((u + 1) * EXPERT_BYTES + ROUTER_BYTES + 4 * T * D for u in us)
+            out["stack_decode_T32"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_stack": ms,
+                                       "ms_per_layer": ms / len(layers), "bytes": nbytes,
+                                       "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                                       "unique_experts_mean": float(np.mean(us)), "layers": len(layers)}
+        else:
+            flops = len(layers) * 7 * T * 3 * 2 * D * FFN
+            out["stack_prefill_T16384"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_stack": ms,
+                                           "ms_per_layer": ms / len(layers), "expert_tflops": flops / (ms * 1e-3) / 1e12,
+                                           "fp8_frac": flops / (ms * 1e-3) / 1e12 / peak8, "fp8_peak_tflops": peak8,
+                                           "peak_kind": kind8, "layers": len(layers)}
+        status = moe.get_status(ws)
+        out[f"stack_T{T}_device_status"] = status
+    out["stack_weight_generation_s"] = gen_s
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
+def small_batch(moe, g, layers, T, args, hbm_peak, flags=0):
     """Batch-T decode of the same layer, captured in a CUDA graph (launch overhead excluded)."""
     import torch
     x_host = g.make_x(g.SEED_DECODE, T, D, bf16=True)
@@ -272,14 +376,14 @@ def small_batch(moe, g, layers, T, args, hbm_peak):
     wt = torch.empty((T, K), dtype=torch.float32, device="cuda")
     n = len(layers)
     for i in range(n):
-        moe.forward(x, layers[i], ws, out=y, ids=ids, w=wt)
+        moe.forward(x, layers[i], ws, out=y, ids=ids, w=wt, flags=flags)
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(graph, stream=s):
             for i in range(n):
-                moe.forward(x, layers[i], ws, out=y, ids=ids, w=wt)
+                moe.forward(x, layers[i], ws, out=y, ids=ids, w=wt, flags=flags)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         graph.replay()
