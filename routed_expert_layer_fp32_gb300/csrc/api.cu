@@ -95,11 +95,12 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
     return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
   MOE_TRY(mark(0));
-  float* part = reinterpret_cast<float*>(base + lay.router_part);
   if (!(forced_ids && forced_w)) {
-    if (T <= kRouterSplitMaxT && L.d <= 2048)
-      MOE_TRY(launch_router_split(x, x_bf16, T, L, part, logits, st, s));
-    else if (T > kRouterSplitMaxT && router_tc_supported(L, x_bf16))
+    if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048)
+      MOE_TRY(launch_router_cluster(x, x_bf16, T, L, logits, s));
+    else if (T <= kRouterSmallMaxT && L.d <= 8192)
+      MOE_TRY(launch_router_small(x, x_bf16, T, L, logits, s));
+    else if (T > kRouterSmallMaxT && router_tc_supported(L, x_bf16))
       MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits, st, s));
     else
       MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
@@ -152,10 +153,11 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
   const LayerDev L = to_dev(layer);
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + lay.logits);
   DevStatus* st = reinterpret_cast<DevStatus*>(base + lay.status);
-  if (T <= kRouterSplitMaxT && L.d <= 2048)
-    MOE_TRY(launch_router_split(x, x_dtype == MOE_BF16, T, L, reinterpret_cast<float*>(base + lay.router_part), logits,
-                                st, s));
-  else if (T > kRouterSplitMaxT && router_tc_supported(L, x_dtype == MOE_BF16))
+  if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048)
+    MOE_TRY(launch_router_cluster(x, x_dtype == MOE_BF16, T, L, logits, s));
+  else if (T <= kRouterSmallMaxT && L.d <= 8192)
+    MOE_TRY(launch_router_small(x, x_dtype == MOE_BF16, T, L, logits, s));
+  else if (T > kRouterSmallMaxT && router_tc_supported(L, x_dtype == MOE_BF16))
     MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits, st, s));
   else
     MOE_TRY(launch_router_logits(x, x_dtype == MOE_BF16, T, L, logits, s));
@@ -242,8 +244,7 @@ moe_status moe_get_status(void* ws, moe_stream_t stream) {
   DevStatus h;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  // clear the error fields only (the router's completion counters are already back at 0)
-  if (cudaMemset(ws, 0, offsetof(DevStatus, pad)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(DevStatus)) != cudaSuccess) return MOE_ERR_CUDA;
   if (h.flags & kFlagBadForced) return MOE_ERR_BAD_FORCED_ID;
   if (h.flags & kFlagTimeout) return MOE_ERR_TIMEOUT;
   return MOE_OK;

@@ -19,8 +19,7 @@ struct DevStatus {
   int flags;        // bit 0: bad forced id, bit 1: timeout
   int bad_forced;   // number of rejected forced slots
   int timeout_site; // where a bounded wait gave up (0 = none)
-  int pad[29];
-  unsigned router_done[32];  // per expert block: k-slices finished (back to 0 after each use)
+  int pad[61];
 };
 constexpr int kFlagBadForced = 1;
 constexpr int kFlagTimeout = 2;
@@ -33,15 +32,14 @@ struct Tile {
 
 // Where each buffer lives inside the caller's workspace, for T tokens.
 struct WsLayout {
-  size_t status, logits, router_part, router_w3, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h,
+  size_t status, logits, router_w3, ids, w, counts, offsets, chunk_counts, perm, pos, n_tiles, tiles, xq, sx, h,
       qh, sh, y_rows;
   size_t total;
   int T, R, R_alloc, n_chunks, max_tiles;
 };
 
 constexpr int kDispatchChunk = 1024;  // tokens per dispatch CTA
-constexpr int kRouterSplitMaxT = 128;  // up to this many tokens the router splits k (decode)
-constexpr int kRouterSplitK = 128;     // k-slice of the split router
+constexpr int kRouterSmallMaxT = 128;  // up to this many tokens the decode router runs
 constexpr int kStreamRows = 16;        // rows per tile on the streaming path
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -60,8 +58,7 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   w.status = take(sizeof(DevStatus));
   w.logits = take(size_t(T) * E * 4);
-  w.router_part = take(T <= kRouterSplitMaxT ? size_t(d / kRouterSplitK) * T * E * 4 : 0);
-  w.router_w3 = take(T > kRouterSplitMaxT ? size_t(3) * E * d * 2 : 0);  // bf16 split of Wr
+  w.router_w3 = take(T > kRouterSmallMaxT ? size_t(3) * E * d * 2 : 0);  // bf16 split of Wr
   w.ids = take(size_t(T) * k * 4);
   w.w = take(size_t(T) * k * 4);
   w.counts = take(size_t(E + 1) * 4);
@@ -148,12 +145,38 @@ __device__ __forceinline__ void mma_e4m3_16x8x32(float (&d)[4], uint32_t a0, uin
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Programmatic dependent launch: every kernel of a layer is launched with programmatic
+// stream serialisation, so it may start while its predecessor finishes.  pdl_begin() waits
+// until the predecessor grid has completed (its writes visible) and then lets the next
+// kernel launch; kernels call it before touching global memory.  Without the launch
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(DevStatus* st, int flag) { atomicOr(&st->flags, flag); }
 
 // Record a device-side timeout: flags |= kFlagTimeout, and the first site that gave up.
 __device__ __forceinline__ void report_timeout_flag(int* status_flags, int site) {
   atomicOr(status_flags, kFlagTimeout);
   atomicCAS(status_flags + 2, 0, site);
+}
+
+template <typename... ExpTypes, typename... ActTypes>
+inline cudaError_t launch_pdl(void (*kernel)(ExpTypes...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              ActTypes&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<ActTypes&&>(args)...);
 }
 
 }  // namespace moe
@@ -182,10 +205,12 @@ cudaError_t launch_select(const float* logits, const int32_t* forced_ids, const 
 bool router_tc_supported(const LayerDev& L, bool x_bf16);
 cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, DevStatus* st,
                              cudaStream_t s);
-// Decode router (T <= kRouterSplitMaxT): d/kRouterSplitK partial slices [n][T][E] in `part`,
-// summed in slice order (plus bias) into logits [T][E] by the last CTA of each expert block.
-cudaError_t launch_router_split(const void* x, bool x_bf16, int T, const LayerDev& L, float* part, float* logits,
-                                DevStatus* st, cudaStream_t s);
+// Decode router (T <= kRouterSmallMaxT, d % 256 == 0, d <= 2048): k split over the CTAs of a
+// thread-block cluster, partials summed through distributed shared memory; deterministic.
+cudaError_t launch_router_cluster(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
+// Decode router (T <= kRouterSmallMaxT, d <= 8192): all of k per CTA, deterministic.
+cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
+
 
 cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_per_tile, const WsLayout& ws,
                             char* base, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,

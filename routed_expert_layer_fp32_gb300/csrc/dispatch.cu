@@ -187,12 +187,14 @@ __device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt
 
 __global__ void __launch_bounds__(1024) k_dispatch_count(const int32_t* __restrict__ ids, int T, int E, int k,
                                                          DispatchOut o) {
+  pdl_begin();
   extern __shared__ int smem[];
   count_chunk(ids, T, E, k, smem, o.chunk_base + size_t(blockIdx.x) * E);
 }
 
 __global__ void __launch_bounds__(1024) k_dispatch_scan(int T, int E, int k, int n_chunks, int rows_per_tile,
                                                         DispatchOut o) {
+  pdl_begin();
   __shared__ int sm_a[kMaxExperts + 1];
   __shared__ int warp_tot[33];
   scan_and_tiles(T, E, k, n_chunks, rows_per_tile, o, sm_a, warp_tot);
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(int T, int E, int k, int
 
 __global__ void __launch_bounds__(1024) k_dispatch_scatter(const int32_t* __restrict__ ids, int T, int E, int k,
                                                            DispatchOut o) {
+  pdl_begin();
   extern __shared__ int smem[];
   scatter_chunk(ids, T, E, k, smem, o);
 }
@@ -207,6 +210,7 @@ __global__ void __launch_bounds__(1024) k_dispatch_scatter(const int32_t* __rest
 // T <= one chunk: the three phases in one CTA.
 __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restrict__ ids, int T, int E, int k,
                                                          int rows_per_tile, DispatchOut o) {
+  pdl_begin();
   extern __shared__ int smem[];
   __shared__ int sm_a[kMaxExperts + 1];
   __shared__ int warp_tot[33];
@@ -217,6 +221,85 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
   __threadfence_block();
   __syncthreads();
   scatter_chunk(ids, T, E, k, smem, o);
+}
+
+// T <= kDispatchChunk and E < 512: one CTA of 256 threads, every count in shared memory.
+// Warp w owns the run of tokens [w*tpw, (w+1)*tpw); per-warp counts become per-warp row
+// bases by a prefix over the warps, then over the experts.
+constexpr int kLeanWarps = 8;
+__global__ void __launch_bounds__(kLeanWarps * 32) k_dispatch_lean(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                                  int rows_per_tile, DispatchOut o) {
+  pdl_begin();
+  extern __shared__ int lean_smem[];
+  int* wcnt = lean_smem;             // [kLeanWarps][E]
+  int* tot = lean_smem + kLeanWarps * E;  // [E + 1]
+  __shared__ int warp_tot[33];
+  const int warp = threadIdx.x >> 5;
+  const int tpw = (T + kLeanWarps - 1) / kLeanWarps;
+  const int t0 = min(T, warp * tpw), t1 = min(T, t0 + tpw);
+  for (int i = threadIdx.x; i < kLeanWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kLeanWarps; ++w) {
+      const int v = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += v;
+    }
+    tot[e] = run;
+    o.counts[e] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan(tot, E, warp_tot);  // tot[e] = offset of expert e
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    o.offsets[e] = tot[e];
+    for (int w = 0; w < kLeanWarps; ++w) wcnt[w * E + e] += tot[e];
+  }
+  if (threadIdx.x == 0) {
+    o.counts[E] = T;
+    o.offsets[E] = k * T;
+    o.offsets[E + 1] = (k + 1) * T;
+  }
+  __syncthreads();
+  // tile list, shared expert first: tile counts per group, scanned
+  int* ntile = tot;  // reused: [E + 1] tiles per group (shared expert first)
+  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
+    const int g = q == 0 ? E : q - 1;
+    const int c = g == E ? T : o.counts[g];
+    ntile[q] = (c + rows_per_tile - 1) / rows_per_tile;
+  }
+  __syncthreads();
+  const int total_tiles = block_exclusive_scan(ntile, E + 1, warp_tot);
+  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
+    const int g = q == 0 ? E : q - 1;
+    const int c = g == E ? T : o.counts[g];
+    const int base_row = g == E ? k * T : o.offsets[g];
+    int ti = ntile[q];
+    for (int r = 0; r < c; r += rows_per_tile, ++ti) {
+      Tile tl;
+      tl.group = g;
+      tl.row0 = base_row + r;
+      tl.nrows = min(rows_per_tile, c - r);
+      tl.pad = 0;
+      o.tiles[ti] = tl;
+    }
+  }
+  if (threadIdx.x == 0) *o.n_tiles = total_tiles;
+  // rows: invalid slots get pos = -1; valid ones are placed in token order
+  for (int i = (threadIdx.x & 31); i < (t1 - t0) * k; i += 32) {
+    const int t = t0 + i / k;
+    const int e = ids[size_t(t) * k + (i % k)];
+    if (e < 0 || e >= E) o.pos[size_t(t) * k + (i % k)] = -1;
+  }
+  int32_t* perm = o.perm;
+  int32_t* pos = o.pos;
+  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [&](int t, int s, int row) {
+    perm[row] = t;
+    pos[size_t(t) * k + s] = row;
+  });
+  for (int t = threadIdx.x; t < T; t += blockDim.x) perm[size_t(k) * T + t] = t;
 }
 
 }  // namespace
@@ -243,14 +326,17 @@ cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_pe
     return e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
   }();
   if (attr != cudaSuccess) return attr;
-  if (n_chunks == 1) {
-    k_dispatch_small<<<1, 1024, smem, s>>>(ids, T, E, k, rows_per_tile, o);
-    return cudaGetLastError();
+  if (n_chunks == 1 && E < 512) {
+    const size_t lean = size_t(kLeanWarps * E + E + 1) * sizeof(int);
+    return launch_pdl(k_dispatch_lean, dim3(1), dim3(kLeanWarps * 32), lean, s, ids, T, E, k, rows_per_tile, o);
   }
-  k_dispatch_count<<<n_chunks, 1024, smem, s>>>(ids, T, E, k, o);
-  k_dispatch_scan<<<1, 1024, 0, s>>>(T, E, k, n_chunks, rows_per_tile, o);
-  k_dispatch_scatter<<<n_chunks, 1024, smem, s>>>(ids, T, E, k, o);
-  return cudaGetLastError();
+  if (n_chunks == 1) {
+    return launch_pdl(k_dispatch_small, dim3(1), dim3(1024), smem, s, ids, T, E, k, rows_per_tile, o);
+  }
+  cudaError_t e = launch_pdl(k_dispatch_count, dim3(n_chunks), dim3(1024), smem, s, ids, T, E, k, o);
+  if (e == cudaSuccess) e = launch_pdl(k_dispatch_scan, dim3(1), dim3(1024), 0, s, T, E, k, n_chunks, rows_per_tile, o);
+  if (e == cudaSuccess) e = launch_pdl(k_dispatch_scatter, dim3(n_chunks), dim3(1024), smem, s, ids, T, E, k, o);
+  return e;
 }
 
 }  // namespace moe

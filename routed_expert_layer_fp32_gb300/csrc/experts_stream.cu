@@ -45,6 +45,7 @@ template <typename XT, bool kFp8>
 __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, int k,
                                                    const int32_t* __restrict__ pos, void* __restrict__ xq,
                                                    float* __restrict__ sx) {
+  pdl_begin();
   __shared__ float red[8];
   const int t = blockIdx.x;
   const XT* xr = x + size_t(t) * d;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
       reinterpret_cast<float (*)[kTG][2][4][32]>(gu_smem + kGuStages * stage_bytes);
   PipeCtl* ctl = reinterpret_cast<PipeCtl*>(gu_smem + kGuStages * stage_bytes + sizeof(float) * kConsumerWarps * kTG * 2 * 4 * 32);
   pipe_init(ctl, kGuStages);
+  pdl_begin();
   const int n_tiles = *a.n_tiles;
   const int nblk = a.F / 16;
   const int total = n_tiles * nblk;
@@ -286,16 +288,14 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
 
 // ------------------------------------------------------------ h quantisation ---------------
 // One warp per row of a tile: sh = max|h| / 448 (1 if the row is zero), qh = E4M3(h / sh).
-__global__ void __launch_bounds__(256) k_hquant(ExpertArgs a, int rows_per_tile) {
-  const int n_tiles = *a.n_tiles;
+// Rows are taken in order 0..R-1; rows that no tile covers (slots of rejected forced ids)
+// are quantised too, harmlessly: nothing reads them.
+__global__ void __launch_bounds__(256) k_hquant(ExpertArgs a, int R) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long total = (long long)n_tiles * rows_per_tile;
-  for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < total; item += nwarps) {
-    const Tile tl = a.tiles[item / rows_per_tile];
-    const int r = int(item % rows_per_tile);
-    if (r >= tl.nrows) continue;
-    const int row = tl.row0 + r;
+  for (long long row_l = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row_l < R; row_l += nwarps) {
+    const int row = int(row_l);
     const float* hr = a.h + size_t(row) * a.F;
     float4 v[5];  // ffn <= 640 = 5 x 32 lanes x 4
     float amax = 0.0f;
@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_down_fp8(ExpertArgs a, int* 
   const size_t stage_bytes = size_t(64 + kStreamRows) * rs;
   PipeCtl* ctl = reinterpret_cast<PipeCtl*>(dn_smem + kDnStages * stage_bytes);
   pipe_init(ctl, kDnStages);
+  pdl_begin();
   const int n_tiles = *a.n_tiles;
   const int nblk = a.d / 64;
   const int total = n_tiles * nblk;
@@ -422,6 +423,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_down_fp8(ExpertArgs a, int* 
 // fp32 weights and activations (no quantisation): one warp per (tile, output column),
 // lanes split k, for every row of the tile.
 __global__ void __launch_bounds__(256) k_gateup_f32(ExpertArgs a) {
+  pdl_begin();
   const int n_tiles = *a.n_tiles;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -448,6 +450,7 @@ __global__ void __launch_bounds__(256) k_gateup_f32(ExpertArgs a) {
 }
 
 __global__ void __launch_bounds__(256) k_down_f32(ExpertArgs a) {
+  pdl_begin();
   const int n_tiles = *a.n_tiles;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -473,6 +476,7 @@ __global__ void __launch_bounds__(256) k_down_f32(ExpertArgs a) {
 template <typename OT, bool kResidual>
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_rows, const int32_t* __restrict__ pos,
                                                  const float* __restrict__ w, int T, int d, int k, OT* __restrict__ out) {
+  pdl_begin();
   const int t = blockIdx.x;
   int rows[kTopK];
   float wt[kTopK];
@@ -533,13 +537,15 @@ int num_sms() {
 cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
                              float* sx, cudaStream_t s) {
   if (x_bf16) {
-    if (L.fp8) k_act_quant<__nv_bfloat16, true><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
-    else k_act_quant<__nv_bfloat16, false><<<T, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.k, pos, xq, sx);
-  } else {
-    if (L.fp8) k_act_quant<float, true><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
-    else k_act_quant<float, false><<<T, 256, 0, s>>>((const float*)x, T, L.d, L.k, pos, xq, sx);
+    if (L.fp8)
+      return launch_pdl(k_act_quant<__nv_bfloat16, true>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, L.k,
+                        pos, xq, sx);
+    return launch_pdl(k_act_quant<__nv_bfloat16, false>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, L.k,
+                      pos, xq, sx);
   }
-  return cudaGetLastError();
+  if (L.fp8)
+    return launch_pdl(k_act_quant<float, true>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, L.k, pos, xq, sx);
+  return launch_pdl(k_act_quant<float, false>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, L.k, pos, xq, sx);
 }
 
 namespace {
@@ -590,22 +596,19 @@ cudaError_t launch_gateup_stream(const LayerDev& L, int T, const WsLayout& ws, c
     if (attr != cudaSuccess) return attr;
     const long long items = tiles * (L.F / 16);
     int* flags = reinterpret_cast<int*>(base + ws.status);
-    k_gateup_fp8<<<int(std::min<long long>(items, sms)), kStreamThreads, smem, s>>>(a, flags);
-    return cudaGetLastError();
+    return launch_pdl(k_gateup_fp8, dim3(int(std::min<long long>(items, sms))), dim3(kStreamThreads), smem, s, a, flags);
   }
   const long long items = tiles * L.F / 8;
-  k_gateup_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_gateup_f32, dim3(int(std::min<long long>(items, (long long)sms * 16))), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, int rows_per_tile, cudaStream_t s) {
   if (!L.fp8) return cudaSuccess;
   const ExpertArgs a = expert_args(L, ws, base);
-  const long long R = (long long)T * (L.k + 1);
-  const long long tiles = std::min<long long>(R, L.E + 1) + R / rows_per_tile;
-  const long long warps = tiles * rows_per_tile;
-  k_hquant<<<int(std::min<long long>((warps + 7) / 8, (long long)num_sms() * 16)), 256, 0, s>>>(a, rows_per_tile);
-  return cudaGetLastError();
+  (void)rows_per_tile;
+  const int R = T * (L.k + 1);
+  return launch_pdl(k_hquant, dim3(int(std::min<long long>((R + 7) / 8, (long long)num_sms() * 16))), dim3(256), 0, s,
+                    a, R);
 }
 
 cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
@@ -619,23 +622,21 @@ cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, cha
     if (attr != cudaSuccess) return attr;
     const long long items = tiles * (L.d / 64);
     int* flags = reinterpret_cast<int*>(base + ws.status);
-    k_down_fp8<<<int(std::min<long long>(items, sms)), kStreamThreads, smem, s>>>(a, flags);
-    return cudaGetLastError();
+    return launch_pdl(k_down_fp8, dim3(int(std::min<long long>(items, sms))), dim3(kStreamThreads), smem, s, a, flags);
   }
   const long long items = tiles * L.d / 8;
-  k_down_f32<<<int(std::min<long long>(items, (long long)sms * 16)), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_down_f32, dim3(int(std::min<long long>(items, (long long)sms * 16))), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
                            moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
   if (y_dtype == MOE_F32)
-    k_combine<float, false><<<T, 256, 0, s>>>(y_rows, pos, w, T, L.d, L.k, (float*)y);
-  else if (residual_add)
-    k_combine<__nv_bfloat16, true><<<T, 256, 0, s>>>(y_rows, pos, w, T, L.d, L.k, (__nv_bfloat16*)y);
-  else
-    k_combine<__nv_bfloat16, false><<<T, 256, 0, s>>>(y_rows, pos, w, T, L.d, L.k, (__nv_bfloat16*)y);
-  return cudaGetLastError();
+    return launch_pdl(k_combine<float, false>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k, (float*)y);
+  if (residual_add)
+    return launch_pdl(k_combine<__nv_bfloat16, true>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+                      (__nv_bfloat16*)y);
+  return launch_pdl(k_combine<__nv_bfloat16, false>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+                    (__nv_bfloat16*)y);
 }
 
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s) {

@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_begin();
   const uint32_t tmem = ctl->tmem_base;
 
   const int n_tiles = *a.n_tiles;
@@ -291,8 +292,7 @@ cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mwsh, const CUte
       cudaFuncSetAttribute(k_expert_tc<kN, kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
   if (attr != cudaSuccess) return attr;
   const int grid = int(std::max<long long>(1, std::min<long long>(max_items, sm_count())));
-  k_expert_tc<kN, kGateUp><<<grid, kTcThreads, C::kSmemBytes, s>>>(mw, mwsh, mx, a);
-  return cudaGetLastError();
+  return launch_pdl(k_expert_tc<kN, kGateUp>, dim3(grid), dim3(kTcThreads), C::kSmemBytes, s, mw, mwsh, mx, a);
 }
 
 template <bool kGateUp>

@@ -3,6 +3,8 @@
 // Layer definition: "We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.",
 // section "The gate" (384 experts scored per token in float32, top 6) and section 1
 // (score plus a per-expert bias; forced ids replayed from a free run).
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -59,85 +61,137 @@ __global__ void __launch_bounds__(256) k_router_warp(const XT* __restrict__ x, i
   }
 }
 
-// Decode-sized router (T <= kRouterSplitMaxT): split over k so that every SM gets work.
-// CTA (expert block of 32, k-slice of 128) stages Wr[32][128] and x[T][128] in shared
-// memory and writes partial sums part[slice][t][e].  The last CTA of an expert block to
-// finish (a counter in the status record, reset after use) adds the slices in slice order
-// plus the bias, so the logits do not depend on which CTA finished last.
-constexpr int kRsE = 32, kRsK = kRouterSplitK;
-constexpr int kMaxRouterSlices = 2048 / kRouterSplitK;  // d <= 2048 on the split path
+// Decode router without a k split: CTA = kRsmE experts x all T tokens x all of k.  The CTA
+// keeps its experts' rows of Wr in shared memory; warp w takes tokens 8w..8w+7, lanes split k
+// (lane owns k = 4 lane + 128 j), and warp shuffles sum the lanes in a fixed order, so the
+// logits are deterministic.
+constexpr int kRsmE = 2;
 template <typename XT>
-__global__ void __launch_bounds__(256) k_router_split(const XT* __restrict__ x, int T, int d, int E,
+__global__ void __launch_bounds__(512) k_router_small(const XT* __restrict__ x, int T, int d, int E,
                                                       const float* __restrict__ Wr, const float* __restrict__ bias,
-                                                      float* __restrict__ part, float* __restrict__ logits,
-                                                      DevStatus* st) {
-  __shared__ unsigned s_last;
-  extern __shared__ __align__(16) float rs_smem[];
-  float (*ws)[kRsK + 4] = reinterpret_cast<float (*)[kRsK + 4]>(rs_smem);
-  float (*xs)[kRsK + 4] = reinterpret_cast<float (*)[kRsK + 4]>(rs_smem + kRsE * (kRsK + 4));
-  const int e0 = blockIdx.x * kRsE, k0 = blockIdx.y * kRsK;
-  const int tid = threadIdx.x;
-  // Wr slice: 32 rows x 128 floats, float4 per thread per pass
-  for (int i = tid; i < kRsE * kRsK / 4; i += blockDim.x) {
-    const int r = i / (kRsK / 4), c = (i % (kRsK / 4)) * 4;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (e0 + r < E) load4(Wr + size_t(e0 + r) * d + k0 + c, v);
-    *reinterpret_cast<float4*>(&ws[r][c]) = make_float4(v[0], v[1], v[2], v[3]);
-  }
-  for (int i = tid; i < T * kRsK / 4; i += blockDim.x) {
-    const int t = i / (kRsK / 4), c = (i % (kRsK / 4)) * 4;
-    float v[4];
-    load4(x + size_t(t) * d + k0 + c, v);
-    *reinterpret_cast<float4*>(&xs[t][c]) = make_float4(v[0], v[1], v[2], v[3]);
+                                                      float* __restrict__ logits) {
+  pdl_begin();
+  extern __shared__ __align__(16) float rsm_w[];  // [kRsmE][d]
+  const int e0 = blockIdx.x * kRsmE;
+  for (int i = threadIdx.x * 4; i < kRsmE * d; i += blockDim.x * 4) {
+    const int r = i / d, c = i % d;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e0 + r < E) v = *reinterpret_cast<const float4*>(Wr + size_t(e0 + r) * d + c);
+    *reinterpret_cast<float4*>(rsm_w + i) = v;
   }
   __syncthreads();
-  const int e = tid & 31, tg = tid >> 5;  // lane = expert, warp = token group (t = tg + 8j)
-  constexpr int kMaxJ = kRouterSplitMaxT / 8;
-  float acc[kMaxJ];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = warp * 8;
+  if (t0 >= T) return;
+  const int nt = min(8, T - t0);
+  float acc[8][kRsmE];
 #pragma unroll
-  for (int j = 0; j < kMaxJ; ++j) acc[j] = 0.0f;
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int e = 0; e < kRsmE; ++e) acc[i][e] = 0.0f;
 #pragma unroll 4
-  for (int c = 0; c < kRsK; c += 4) {
-    const float4 wv = *reinterpret_cast<const float4*>(&ws[e][c]);
+  for (int k = lane * 4; k < d; k += 128) {
+    float w[kRsmE][4];
 #pragma unroll
-    for (int j = 0; j < kMaxJ; ++j) {
-      const int t = tg + 8 * j;
-      if (t < T) {
-        const float4 xv = *reinterpret_cast<const float4*>(&xs[t][c]);
-        acc[j] = fmaf(xv.x, wv.x, acc[j]);
-        acc[j] = fmaf(xv.y, wv.y, acc[j]);
-        acc[j] = fmaf(xv.z, wv.z, acc[j]);
-        acc[j] = fmaf(xv.w, wv.w, acc[j]);
+    for (int e = 0; e < kRsmE; ++e) {
+      const float4 wv = *reinterpret_cast<const float4*>(rsm_w + e * d + k);
+      w[e][0] = wv.x; w[e][1] = wv.y; w[e][2] = wv.z; w[e][3] = wv.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < nt) {
+        float xv[4];
+        load4(x + size_t(t0 + i) * d + k, xv);
+#pragma unroll
+        for (int e = 0; e < kRsmE; ++e) {
+          acc[i][e] = fmaf(xv[0], w[e][0], acc[i][e]);
+          acc[i][e] = fmaf(xv[1], w[e][1], acc[i][e]);
+          acc[i][e] = fmaf(xv[2], w[e][2], acc[i][e]);
+          acc[i][e] = fmaf(xv[3], w[e][3], acc[i][e]);
+        }
       }
     }
   }
-  if (e0 + e < E) {
 #pragma unroll
-    for (int j = 0; j < kMaxJ; ++j) {
-      const int t = tg + 8 * j;
-      if (t < T) part[(size_t(blockIdx.y) * T + t) * E + e0 + e] = acc[j];
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int e = 0; e < kRsmE; ++e) {
+      const float sum = warp_sum(acc[i][e]);
+      if (lane == 0 && i < nt && e0 + e < E) logits[size_t(t0 + i) * E + e0 + e] = sum + (bias ? bias[e0 + e] : 0.0f);
+    }
+}
+
+// Decode router, split over k inside thread-block clusters.  CTA (32 experts, 256-wide
+// k-slice) stages its slice of Wr (fp32) and of x in shared memory with all threads loading
+// at once, computes partial logits [T][32] into its own shared memory, and the n_slice CTAs
+// of the cluster (one per k-slice) then sum the partials through distributed shared memory,
+// each CTA for a share of the tokens, adding the slices in rank order (deterministic).
+constexpr int kRcE = 32, kRcK = 256, kRcThreads = 256;
+template <typename XT>
+__global__ void __launch_bounds__(kRcThreads) k_router_cluster(const XT* __restrict__ x, int T, int d, int E,
+                                                               const float* __restrict__ Wr,
+                                                               const float* __restrict__ bias,
+                                                               float* __restrict__ logits) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(16) uint8_t rc_smem[];
+  float* ws = reinterpret_cast<float*>(rc_smem);                      // [kRcE][kRcK + 4]
+  XT* xs = reinterpret_cast<XT*>(ws + kRcE * (kRcK + 4));             // [T][kRcK + 8]
+  float* part = reinterpret_cast<float*>(xs + size_t(T) * (kRcK + 8));  // [T][kRcE]
+  pdl_begin();
+  const int e0 = blockIdx.x * kRcE, k0 = blockIdx.y * kRcK;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kRcE * (kRcK / 4); i += kRcThreads) {
+    const int r = i / (kRcK / 4), c = (i % (kRcK / 4)) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e0 + r < E) v = *reinterpret_cast<const float4*>(Wr + size_t(e0 + r) * d + k0 + c);
+    *reinterpret_cast<float4*>(ws + r * (kRcK + 4) + c) = v;
+  }
+  constexpr int kVec = 16 / sizeof(XT);  // elements per 16-byte load
+  for (int i = tid; i < T * (kRcK / kVec); i += kRcThreads) {
+    const int t = i / (kRcK / kVec), c = (i % (kRcK / kVec)) * kVec;
+    *reinterpret_cast<uint4*>(xs + size_t(t) * (kRcK + 8) + c) =
+        *reinterpret_cast<const uint4*>(x + size_t(t) * d + k0 + c);
+  }
+  __syncthreads();
+  const int e = tid & 31, tg = tid >> 5;  // lane = expert, warp = tokens tg, tg + 8, ...
+  for (int tb = tg; tb < T; tb += 8 * 8) {  // up to 8 tokens per pass
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int c = 0; c < kRcK; c += 4) {
+      const float4 wv = *reinterpret_cast<const float4*>(ws + e * (kRcK + 4) + c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = tb + 8 * j;
+        if (t < T) {
+          float xv[4];
+          load4(xs + size_t(t) * (kRcK + 8) + c, xv);
+          acc[j] = fmaf(xv[0], wv.x, acc[j]);
+          acc[j] = fmaf(xv[1], wv.y, acc[j]);
+          acc[j] = fmaf(xv[2], wv.z, acc[j]);
+          acc[j] = fmaf(xv[3], wv.w, acc[j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = tb + 8 * j;
+      if (t < T) part[t * kRcE + e] = acc[j];
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&st->router_done[blockIdx.x], 1u) == gridDim.y - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int n_part = gridDim.y;  // <= kMaxRouterSlices
-  for (int i = tid; i < T * kRsE; i += blockDim.x) {
-    const int t = i / kRsE, ee = e0 + i % kRsE;
-    if (ee >= E) continue;
-    float v[kMaxRouterSlices];
-#pragma unroll
-    for (int p = 0; p < kMaxRouterSlices; ++p) v[p] = p < n_part ? __ldcg(part + (size_t(p) * T + t) * E + ee) : 0.0f;
-    float sum = v[0];
-#pragma unroll
-    for (int p = 1; p < kMaxRouterSlices; ++p)
-      if (p < n_part) sum += v[p];
-    logits[size_t(t) * E + ee] = sum + (bias ? bias[ee] : 0.0f);
+  cluster.sync();
+  const int n_slice = int(cluster.num_blocks());
+  const int rank = int(cluster.block_rank());
+  const int per = (T + n_slice - 1) / n_slice;
+  const int t_lo = rank * per, t_hi = min(T, t_lo + per);
+  for (int i = tid; i < (t_hi - t_lo) * kRcE; i += kRcThreads) {
+    const int t = t_lo + i / kRcE, ee = i % kRcE;
+    float sum = 0.0f;
+    for (int r = 0; r < n_slice; ++r) sum += cluster.map_shared_rank(part, r)[t * kRcE + ee];
+    if (e0 + ee < E) logits[size_t(t) * E + e0 + ee] = sum + (bias ? bias[e0 + ee] : 0.0f);
   }
-  if (tid == 0) st->router_done[blockIdx.x] = 0;
+  cluster.sync();  // no CTA leaves while another still reads its partials
 }
 
 // Prefill-sized router: SIMT tiled GEMM, 64 tokens x 64 experts per CTA, 4x4 per thread.
@@ -145,6 +199,7 @@ template <typename XT>
 __global__ void __launch_bounds__(256) k_router_gemm(const XT* __restrict__ x, int T, int d, int E,
                                                      const float* __restrict__ Wr, const float* __restrict__ bias,
                                                      float* __restrict__ logits) {
+  pdl_begin();
   constexpr int BM = 64, BN = 64, BK = 16;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
@@ -203,6 +258,7 @@ __global__ void __launch_bounds__(256) k_select(const float* __restrict__ logits
                                                 const int32_t* __restrict__ forced_ids,
                                                 const float* __restrict__ forced_w, int T, int E, int k,
                                                 int32_t* __restrict__ ids, float* __restrict__ w, DevStatus* st) {
+  pdl_begin();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -299,36 +355,65 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
   } else {
     dim3 grid((L.E + 63) / 64, (T + 63) / 64);
     if (x_bf16)
-      k_router_gemm<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias, logits);
-    else
-      k_router_gemm<float><<<grid, 256, 0, s>>>((const float*)x, T, L.d, L.E, L.Wr, L.bias, logits);
+      return launch_pdl(k_router_gemm<__nv_bfloat16>, grid, dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr,
+                        L.bias, logits);
+    return launch_pdl(k_router_gemm<float>, grid, dim3(256), 0, s, (const float*)x, T, L.d, L.E, L.Wr, L.bias, logits);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_split(const void* x, bool x_bf16, int T, const LayerDev& L, float* part, float* logits,
-                                DevStatus* st, cudaStream_t s) {
-  constexpr int most = (kRsE + kRouterSplitMaxT) * (kRsK + 4) * int(sizeof(float));
+cudaError_t launch_router_cluster(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s) {
+  const int n_slice = L.d / kRcK;
+  const size_t xel = x_bf16 ? 2 : 4;
+  const size_t smem = size_t(kRcE) * (kRcK + 4) * 4 + size_t(T) * (kRcK + 8) * xel + size_t(T) * kRcE * 4;
   static cudaError_t attr = [] {
-    cudaError_t e1 = cudaFuncSetAttribute(k_router_split<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    cudaError_t e2 = cudaFuncSetAttribute(k_router_split<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    const int most = 200 * 1024;
+    cudaError_t e1 = cudaFuncSetAttribute(k_router_cluster<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaError_t e2 = cudaFuncSetAttribute(k_router_cluster<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     return e1 != cudaSuccess ? e1 : e2;
   }();
   if (attr != cudaSuccess) return attr;
-  const size_t smem = size_t(kRsE + T) * (kRsK + 4) * sizeof(float);
-  dim3 grid((L.E + kRsE - 1) / kRsE, L.d / kRsK);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((L.E + kRcE - 1) / kRcE, n_slice);
+  cfg.blockDim = dim3(kRcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 1;
+  attrs[0].val.clusterDim.y = n_slice;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
   if (x_bf16)
-    k_router_split<__nv_bfloat16><<<grid, 256, smem, s>>>((const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias, part,
-                                                          logits, st);
-  else
-    k_router_split<float><<<grid, 256, smem, s>>>((const float*)x, T, L.d, L.E, L.Wr, L.bias, part, logits, st);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, k_router_cluster<__nv_bfloat16>, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias,
+                              logits);
+  return cudaLaunchKernelEx(&cfg, k_router_cluster<float>, (const float*)x, T, L.d, L.E, L.Wr, L.bias, logits);
+}
+
+cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s) {
+  const size_t smem = size_t(kRsmE) * L.d * sizeof(float);
+  static cudaError_t attr = [] {
+    const int most = int(kRsmE * 8192 * sizeof(float));
+    cudaError_t e1 = cudaFuncSetAttribute(k_router_small<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaError_t e2 = cudaFuncSetAttribute(k_router_small<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    return e1 != cudaSuccess ? e1 : e2;
+  }();
+  if (attr != cudaSuccess) return attr;
+  const int threads = ((T + 7) / 8) * 32;
+  const dim3 grid((L.E + kRsmE - 1) / kRsmE);
+  if (x_bf16)
+    return launch_pdl(k_router_small<__nv_bfloat16>, grid, dim3(threads), smem, s, (const __nv_bfloat16*)x, T, L.d, L.E,
+                      L.Wr, L.bias, logits);
+  return launch_pdl(k_router_small<float>, grid, dim3(threads), smem, s, (const float*)x, T, L.d, L.E, L.Wr, L.bias,
+                    logits);
 }
 
 cudaError_t launch_select(const float* logits, const int32_t* forced_ids, const float* forced_w, int T,
                           const LayerDev& L, int32_t* ids, float* w, DevStatus* st, cudaStream_t s) {
-  k_select<<<(T + 7) / 8, 256, 0, s>>>(logits, forced_ids, forced_w, T, L.E, L.k, ids, w, st);
-  return cudaGetLastError();
+  return launch_pdl(k_select, dim3((T + 7) / 8), dim3(256), 0, s, logits, forced_ids, forced_w, T, L.E, L.k, ids, w, st);
 }
 
 }  // namespace moe

@@ -24,6 +24,7 @@ constexpr int kRtATile = kRtM * 128;
 constexpr size_t kRtSmemBudget = 200 * 1024;
 
 __global__ void k_router_split_w(const float* __restrict__ Wr, long long n, __nv_bfloat16* __restrict__ out) {
+  pdl_begin();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const float w = Wr[i];
     const __nv_bfloat16 hi = __float2bfloat16_rn(w);
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_begin();
   const uint32_t tmem = ctl->tmem_base;
   const int n_items = (T + kRtM - 1) / kRtM;
   const int KT = d / 64;  // 64 bf16 per 128-byte k-slice
@@ -197,7 +199,9 @@ bool router_tc_supported(const LayerDev& L, bool x_bf16) {
 cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, DevStatus* st,
                              cudaStream_t s) {
   const long long n = (long long)L.E * L.d;
-  k_router_split_w<<<int(std::min<long long>((n + 255) / 256, 4096)), 256, 0, s>>>(L.Wr, n, w3);
+  cudaError_t e = launch_pdl(k_router_split_w, dim3(int(std::min<long long>((n + 255) / 256, 4096))), dim3(256), 0, s,
+                             L.Wr, n, w3);
+  if (e != cudaSuccess) return e;
   const int n_half = ((L.E / 2) + 15) / 16 * 16;
   const int stage_bytes = kRtATile + 2 * n_half * 128;
   const int n_stages = int(std::min<size_t>(8, kRtSmemBudget / stage_bytes));
@@ -210,9 +214,8 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   static cudaError_t attr = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   if (attr != cudaSuccess) return attr;
   const int items = (T + kRtM - 1) / kRtM;
-  k_router_tc<<<std::min(items, rt_sm_count()), kRtThreads, smem, s>>>(mx, mw, L.bias, T, L.d, L.E, n_half, n_stages,
-                                                                      tmem_cols, logits, &st->flags);
-  return cudaGetLastError();
+  return launch_pdl(k_router_tc, dim3(std::min(items, rt_sm_count())), dim3(kRtThreads), smem, s, mx, mw, L.bias, T,
+                    L.d, L.E, n_half, n_stages, tmem_cols, logits, &st->flags);
 }
 
 }  // namespace moe
