@@ -155,6 +155,24 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(value: float) -> float:
+    """The maximum of `value` over the ranks of the default process group (replica timing)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: int, steps: int, world: int, elapsed_ms_max: float) -> float:
+    """Whole-job throughput of `world` independent replicas: every rank's units over the
+    slowest rank's time."""
+    return world * units_per_rank * steps / (elapsed_ms_max / 1e3)
+
+
 def layer_bytes(ids: np.ndarray, T: int):
     """Algorithmic HBM bytes of one forward: the used experts (and the shared one) once, the
     router once, x read and y written in bf16."""
@@ -222,12 +240,8 @@ def run_ours(args):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop))
     clocks = clk.summary()
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
     # per-kernel durations: the same steps again with events at every stage boundary (an
     # event between two kernels makes the second wait for the first to finish, so this pass
     # is only used for the per-stage split, not for the step time)
@@ -248,7 +262,7 @@ def run_ours(args):
     nbytes, U = layer_bytes(ids_h, T)
     gu_bytes = gateup_bytes(U, T)
     ms_step = elapsed_ms / args.steps
-    value = world * T * args.steps / (elapsed_ms / 1e3)
+    value = replica_throughput(T, args.steps, world, elapsed_ms)
     gu_ms = stage_ms["gate_up"]
     gu_kernel = "k_gateup_fp8" if args.path == "stream" else "k_expert_tc<16,gate_up>"
     traffic = profiled_traffic(gu_kernel) if (args.path != "stream" and T == HEADLINE_T) else None
@@ -275,12 +289,8 @@ def run_ours(args):
         y_pin.copy_(y.view(torch.int16), non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e = {"value": replica_throughput(T, args.steps, world, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2}
 
     extra = {"layer_hbm_frac": layer_frac, "layer_bytes_per_step": nbytes, "unique_experts": U,

@@ -170,6 +170,12 @@ moe_status moe_get_status(void* ws, moe_stream_t stream);
 moe_status moe_route_noalloc(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, int k,
                              int32_t* ids_out, float* w_out, moe_stream_t stream);
 
+/* Exercises the device-side timeout path: launches one CTA whose wait on a barrier can never
+ * complete; the wait gives up after timeout_us (<= 1 s) and records MOE_ERR_TIMEOUT in the
+ * workspace's status record, which moe_get_status() then returns.  The GPU context stays
+ * usable.  For failure-detection tests. */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned timeout_us, moe_stream_t stream);
+
 /* Static description of a status code. */
 const char* moe_status_string(moe_status status);
 

@@ -23,7 +23,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 # every entry point include/libmoe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward",
            "moe_forward_stack", "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status",
-           "moe_status_string", "moe_e4m3_encode", "moe_route_noalloc")
+           "moe_status_string", "moe_e4m3_encode", "moe_route_noalloc", "moe_selftest_wait_timeout")
 TRACE_POINTS = 9
 TRACE_STAGES = ("router", "select", "dispatch", "act_quant", "gate_up", "h_quant", "down", "combine")
 
@@ -69,9 +69,10 @@ def lib():
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_e4m3_encode.argtypes = [vp, vp, i64, vp]
         L.moe_route_noalloc.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
+        L.moe_selftest_wait_timeout.argtypes = [vp, sz, u32, vp]
         for f in ("moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward", "moe_forward_stack",
                   "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status", "moe_e4m3_encode",
-                  "moe_route_noalloc"):
+                  "moe_route_noalloc", "moe_selftest_wait_timeout"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -246,6 +247,11 @@ def forward_stack(layers: Sequence[Layer], residual: torch.Tensor, ws: torch.Ten
 def get_status(ws: torch.Tensor) -> int:
     """Synchronises the current stream; returns (and clears) the device-side status code."""
     return int(lib().moe_get_status(_ptr(ws), _stream()))
+
+
+def selftest_wait_timeout(ws: torch.Tensor, timeout_us: int = 10000):
+    """Launch the bounded-wait self-test; moe_get_status(ws) then reports MOE_ERR_TIMEOUT."""
+    _check(lib().moe_selftest_wait_timeout(_ptr(ws), ws.numel(), timeout_us, _stream()), "moe_selftest_wait_timeout")
 
 
 def e4m3_encode(v: torch.Tensor) -> torch.Tensor:

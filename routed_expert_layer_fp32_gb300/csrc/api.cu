@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 using namespace moe;
 
@@ -123,9 +124,40 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   return MOE_OK;
 }
 
+// Self-test of the bounded-wait path: one CTA waits on an mbarrier that expects two arrivals
+// but receives one, so the phase never completes; the wait gives up after limit_ns, records
+// MOE_ERR_TIMEOUT in the status record and the kernel returns normally.
+__global__ void k_selftest_wait_timeout(int* status_flags, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 2);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive(&bar);
+    const unsigned long long t0 = global_timer_ns();
+    bool done = false;
+    while (!done) {
+      done = mbar_try_wait(&bar, 0);
+      if (!done && global_timer_ns() - t0 > limit_ns) break;
+    }
+    if (!done) report_timeout_flag(status_flags, 99);
+  }
+}
+
 }  // namespace
 
 extern "C" {
+
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned timeout_us, moe_stream_t stream) {
+  if (!ws || !aligned16(ws) || ws_bytes < sizeof(DevStatus) || timeout_us == 0 || timeout_us > 1000000)
+    return MOE_ERR_INVALID_ARG;
+  k_selftest_wait_timeout<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<int*>(ws), 1000ull * timeout_us);
+  return cuda_status(cudaGetLastError());
+}
+
 
 size_t moe_workspace_bytes(const moe_layer* layer, int T) {
   if (!layer || T < 0 || check_layer(layer) != MOE_OK) return 0;

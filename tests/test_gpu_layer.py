@@ -236,6 +236,21 @@ def test_bad_forced_ids_are_reported_and_skipped(moe, kolibri):
     assert ok, msg
 
 
+def test_device_wait_timeout_is_reported_and_context_survives(moe, kolibri):
+    """A wait that can never complete gives up after its limit, reports MOE_ERR_TIMEOUT
+    through the status record, and the next forward on the same context is correct."""
+    w, L = kolibri
+    ws = moe.workspace(L, 8)
+    assert moe.get_status(ws) == 0
+    moe.binding.selftest_wait_timeout(ws, 10000)
+    assert moe.get_status(ws) == -5
+    assert moe.get_status(ws) == 0  # cleared
+    x = g.make_x(81, 8, w.d, bf16=True)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    check_free_layer(w, x, y, ids, wt, where="after timeout self-test")
+    assert moe.get_status(ws) == 0
+
+
 def test_rows_do_not_depend_on_other_rows(moe, kolibri):
     """Batch parity: a token's output is the same alone, in a batch, and in a permuted batch
     (the batched expert layer on the pages returned wrong rows depending on the batch)."""
