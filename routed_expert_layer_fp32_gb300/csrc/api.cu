@@ -96,18 +96,22 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
     return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
   MOE_TRY(mark(0));
+  bool selected = false;  // the tensor-core router selects in its epilogue under free routing
   if (!(forced_ids && forced_w)) {
-    if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048)
+    if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
       MOE_TRY(launch_router_cluster(x, x_bf16, T, L, logits, s));
-    else if (T <= kRouterSmallMaxT && L.d <= 8192)
+    } else if (T <= kRouterSmallMaxT && L.d <= 8192) {
       MOE_TRY(launch_router_small(x, x_bf16, T, L, logits, s));
-    else if (T > kRouterSmallMaxT && router_tc_supported(L, x_bf16))
-      MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits, st, s));
-    else
+    } else if (T > kRouterSmallMaxT && router_tc_supported(L, x_bf16)) {
+      selected = !forced_ids;
+      MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3),
+                               selected ? nullptr : logits, selected ? ids : nullptr, selected ? w : nullptr, st, s));
+    } else {
       MOE_TRY(launch_router_logits(x, x_bf16, T, L, logits, s));
+    }
   }
   MOE_TRY(mark(1));
-  MOE_TRY(launch_select(logits, forced_ids, forced_w, T, L, ids, w, st, s));
+  if (!selected) MOE_TRY(launch_select(logits, forced_ids, forced_w, T, L, ids, w, st, s));
   MOE_TRY(mark(2));
   MOE_TRY(launch_dispatch(ids, T, L.E, L.k, rows_per_tile, lay, base, counts, offsets, perm, pos, s));
   MOE_TRY(mark(3));
@@ -189,9 +193,11 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
     MOE_TRY(launch_router_cluster(x, x_dtype == MOE_BF16, T, L, logits, s));
   else if (T <= kRouterSmallMaxT && L.d <= 8192)
     MOE_TRY(launch_router_small(x, x_dtype == MOE_BF16, T, L, logits, s));
-  else if (T > kRouterSmallMaxT && router_tc_supported(L, x_dtype == MOE_BF16))
-    MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits, st, s));
-  else
+  else if (T > kRouterSmallMaxT && router_tc_supported(L, x_dtype == MOE_BF16)) {
+    MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits_out, ids_out, w_out,
+                             st, s));
+    return MOE_OK;
+  } else
     MOE_TRY(launch_router_logits(x, x_dtype == MOE_BF16, T, L, logits, s));
   MOE_TRY(launch_select(logits, nullptr, nullptr, T, L, ids_out, w_out, st, s));
   return MOE_OK;

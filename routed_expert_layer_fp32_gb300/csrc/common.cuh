@@ -202,9 +202,11 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
 cudaError_t launch_select(const float* logits, const int32_t* forced_ids, const float* forced_w, int T,
                           const LayerDev& L, int32_t* ids, float* w, DevStatus* st, cudaStream_t s);
 // Prefill router on tensor cores (bf16 x, Wr split into three bf16 terms in w3 [3, E, d]).
+// logits (or NULL) receive the logits; with ids/wts not NULL the kernel also selects the
+// top-k (free routing) and writes ids and renormalised weights.
 bool router_tc_supported(const LayerDev& L, bool x_bf16);
-cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, DevStatus* st,
-                             cudaStream_t s);
+cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, int32_t* ids,
+                             float* wts, DevStatus* st, cudaStream_t s);
 // Decode router (T <= kRouterSmallMaxT, d % 256 == 0, d <= 2048): k split over the CTAs of a
 // thread-block cluster, partials summed through distributed shared memory; deterministic.
 cudaError_t launch_router_cluster(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);

@@ -50,7 +50,8 @@ struct RtCtl {
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_router_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                 const float* __restrict__ bias, int T, int d, int E, int n_half, int n_stages, int tmem_cols,
-                float* __restrict__ logits, int* status_flags) {
+                float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int k,
+                int* status_flags) {
   extern __shared__ uint8_t rt_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_half_bytes = n_half * 128;
@@ -145,6 +146,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_wait(&ctl->mma_done, 0, &zero);
     }
   } else {  // epilogue: one token per TMEM lane, logits = acc + bias
+    // With ids != nullptr the epilogue also selects: a sorted list of the kTopK best
+    // (larger logit first, lower index first on equal logits; the scan visits experts in
+    // increasing index, so an equal later logit never displaces an earlier one), then the
+    // softmax over the selected logits, summed in slot order.
     const int q = warp & 3;
     int jt = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++jt) {
@@ -155,6 +160,13 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       tc_fence_after();
       const int t = item * kRtM + q * 32 + lane;
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16);
+      float tv[kTopK];
+      int ti[kTopK];
+#pragma unroll
+      for (int i = 0; i < kTopK; ++i) {
+        tv[i] = -INFINITY;
+        ti[i] = 0x7fffffff;
+      }
       for (int c0 = 0; c0 < 2 * n_half && c0 < E; c0 += 16) {
         float v[16];
         tmem_ld16(taddr + c0, v);
@@ -162,7 +174,40 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int e = c0 + i;
-            if (e < E) logits[size_t(t) * E + e] = v[i] + (bias ? bias[e] : 0.0f);
+            if (e < E) {
+              const float lg = v[i] + (bias ? bias[e] : 0.0f);
+              if (logits) logits[size_t(t) * E + e] = lg;
+              if (ids && (lg > tv[kTopK - 1] || (lg == tv[kTopK - 1] && e < ti[kTopK - 1]))) {
+                tv[kTopK - 1] = lg;
+                ti[kTopK - 1] = e;
+#pragma unroll
+                for (int j = kTopK - 1; j > 0; --j) {
+                  if (tv[j] > tv[j - 1] || (tv[j] == tv[j - 1] && ti[j] < ti[j - 1])) {
+                    const float fv = tv[j];
+                    tv[j] = tv[j - 1];
+                    tv[j - 1] = fv;
+                    const int fi = ti[j];
+                    ti[j] = ti[j - 1];
+                    ti[j - 1] = fi;
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      if (ids && t < T) {
+        float ex[kTopK], sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kTopK; ++i) {
+          ex[i] = i < k ? expf(tv[i] - tv[0]) : 0.0f;
+          sum += ex[i];
+        }
+#pragma unroll
+        for (int i = 0; i < kTopK; ++i) {
+          if (i < k) {
+            ids[size_t(t) * k + i] = ti[i];
+            wts[size_t(t) * k + i] = ex[i] / sum;
           }
         }
       }
@@ -196,8 +241,8 @@ bool router_tc_supported(const LayerDev& L, bool x_bf16) {
   return x_bf16 && L.d % 64 == 0 && L.E <= 512 && L.E % 32 == 0 && encode_fn() != nullptr;
 }
 
-cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, DevStatus* st,
-                             cudaStream_t s) {
+cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, int32_t* ids,
+                             float* wts, DevStatus* st, cudaStream_t s) {
   const long long n = (long long)L.E * L.d;
   cudaError_t e = launch_pdl(k_router_split_w, dim3(int(std::min<long long>((n + 255) / 256, 4096))), dim3(256), 0, s,
                              L.Wr, n, w3);
@@ -215,7 +260,7 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   if (attr != cudaSuccess) return attr;
   const int items = (T + kRtM - 1) / kRtM;
   return launch_pdl(k_router_tc, dim3(std::min(items, rt_sm_count())), dim3(kRtThreads), smem, s, mx, mw, L.bias, T,
-                    L.d, L.E, n_half, n_stages, tmem_cols, logits, &st->flags);
+                    L.d, L.E, n_half, n_stages, tmem_cols, logits, ids, wts, L.k, &st->flags);
 }
 
 }  // namespace moe
