@@ -96,10 +96,11 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
     return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
   MOE_TRY(mark(0));
-  bool selected = false;  // the tensor-core router selects in its epilogue under free routing
+  bool selected = false;  // the decode and tensor-core routers select in-kernel under free routing
   if (!(forced_ids && forced_w)) {
     if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
-      MOE_TRY(launch_router_cluster(x, x_bf16, T, L, logits, s));
+      selected = !forced_ids;
+      MOE_TRY(launch_router_decode(x, x_bf16, T, L, logits, selected ? ids : nullptr, selected ? w : nullptr, st, s));
     } else if (T <= kRouterSmallMaxT && L.d <= 8192) {
       MOE_TRY(launch_router_small(x, x_bf16, T, L, logits, s));
     } else if (T > kRouterSmallMaxT && router_tc_supported(L, x_bf16)) {
@@ -189,9 +190,10 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
   const LayerDev L = to_dev(layer);
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + lay.logits);
   DevStatus* st = reinterpret_cast<DevStatus*>(base + lay.status);
-  if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048)
-    MOE_TRY(launch_router_cluster(x, x_dtype == MOE_BF16, T, L, logits, s));
-  else if (T <= kRouterSmallMaxT && L.d <= 8192)
+  if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
+    MOE_TRY(launch_router_decode(x, x_dtype == MOE_BF16, T, L, logits, ids_out, w_out, st, s));
+    return MOE_OK;
+  } else if (T <= kRouterSmallMaxT && L.d <= 8192)
     MOE_TRY(launch_router_small(x, x_dtype == MOE_BF16, T, L, logits, s));
   else if (T > kRouterSmallMaxT && router_tc_supported(L, x_dtype == MOE_BF16)) {
     MOE_TRY(launch_router_tc(x, T, L, reinterpret_cast<__nv_bfloat16*>(base + lay.router_w3), logits_out, ids_out, w_out,

@@ -19,8 +19,11 @@ struct DevStatus {
   int flags;        // bit 0: bad forced id, bit 1: timeout
   int bad_forced;   // number of rejected forced slots
   int timeout_site; // where a bounded wait gave up (0 = none)
-  int pad[61];
+  int pad0;
+  int tickets[16];  // decode router: CTAs done per (token block, token sub-block); 0 between launches
+  int pad[44];
 };
+static_assert(sizeof(DevStatus) == 256, "DevStatus is one 256-byte block");
 constexpr int kFlagBadForced = 1;
 constexpr int kFlagTimeout = 2;
 
@@ -209,7 +212,10 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
                              float* wts, DevStatus* st, cudaStream_t s);
 // Decode router (T <= kRouterSmallMaxT, d % 256 == 0, d <= 2048): k split over the CTAs of a
 // thread-block cluster, partials summed through distributed shared memory; deterministic.
-cudaError_t launch_router_cluster(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
+// Writes logits; with ids/wts not NULL it also selects the top-k (free routing), using the
+// ticket counters in st (zero between launches).
+cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, int32_t* ids,
+                                 float* wts, DevStatus* st, cudaStream_t s);
 // Decode router (T <= kRouterSmallMaxT, d <= 8192): all of k per CTA, deterministic.
 cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
 

@@ -22,6 +22,104 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* x, float (&v)[4]) {
   v[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 
+// Order-preserving 32-bit key of a logit; 0 means "not selectable" (NaN, or taken).  -0 and +0
+// get one key, so they tie as floats do.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t u = v == 0.0f ? 0u : __float_as_uint(v);
+  const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return v != v ? 0u : key;
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// Free selection of one token by one warp, written out with its weights.  Lane l holds the keys
+// of experts l + 32 j (j < kPer).  Each of the kTopK rounds takes the warp's largest key (one
+// warp reduction), then the lowest expert index holding it (a second reduction), and the lane
+// owning that expert drops it: the same experts in the same order as kTopK rounds of "larger
+// logit, or equal logit and lower index" over all E logits (softmax is monotone in the logit,
+// so choosing on logits chooses on probabilities).  Every lane ends with all kTopK choices, so
+// the weights need no further exchange: softmax over the selected logits, the largest (slot
+// 0) subtracted, summed in slot order.  A slot without a selectable expert gets id -1 and
+// weight 0.  The row is read through L2, so logits that other CTAs of the same grid wrote
+// (made visible by a fence and a ticket) are seen.
+template <int kPer>
+__device__ __forceinline__ void select_write_free_t(const float* row, int E, int lane, int32_t* ids_row,
+                                                    float* w_row) {
+  // every load unconditional and in bounds (a clamped index), so all are in flight at once
+  float raw[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) raw[j] = __ldcg(row + min(lane + 32 * j, E - 1));
+  uint32_t key[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) key[j] = lane + 32 * j < E ? logit_key(raw[j]) : 0u;
+  uint32_t best = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) best = max(best, key[j]);
+  int sel[kTopK];
+  float val[kTopK];
+#pragma unroll
+  for (int r = 0; r < kTopK; ++r) {
+    const uint32_t M = __reduce_max_sync(0xffffffffu, best);
+    uint32_t mine = 0xffffffffu;
+#pragma unroll
+    for (int j = kPer - 1; j >= 0; --j)
+      if (key[j] == M) mine = uint32_t(lane + 32 * j);
+    const uint32_t I = __reduce_min_sync(0xffffffffu, mine);
+    if (M != 0u && int(I & 31u) == lane) {
+      best = 0u;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        if (j == int(I >> 5)) key[j] = 0u;
+        best = max(best, key[j]);
+      }
+    }
+    sel[r] = M != 0u ? int(I) : -1;
+    val[r] = M != 0u ? key_logit(M) : 0.0f;
+  }
+  const float m = val[0];
+  float ex[kTopK], s = 0.0f;
+#pragma unroll
+  for (int r = 0; r < kTopK; ++r) {
+    ex[r] = sel[r] >= 0 ? expf(val[r] - m) : 0.0f;
+    s += ex[r];
+  }
+#pragma unroll
+  for (int r = 0; r < kTopK; ++r) {
+    if (lane == r) {
+      ids_row[r] = sel[r];
+      w_row[r] = sel[r] >= 0 ? ex[r] / s : 0.0f;
+    }
+  }
+}
+
+__device__ __forceinline__ void select_write_free(const float* row, int E, int lane, int32_t* ids_row, float* w_row) {
+  if (E <= 128) select_write_free_t<4>(row, E, lane, ids_row, w_row);
+  else if (E <= 256) select_write_free_t<8>(row, E, lane, ids_row, w_row);
+  else if (E <= 384) select_write_free_t<12>(row, E, lane, ids_row, w_row);
+  else if (E <= 512) select_write_free_t<16>(row, E, lane, ids_row, w_row);
+  else select_write_free_t<kMaxExperts / 32>(row, E, lane, ids_row, w_row);
+}
+
+// Weights of a forced selection: softmax over the valid selected logits (max subtracted, summed
+// in slot order); an invalid slot (sel < 0) gets weight 0.
+__device__ __forceinline__ void write_selection(int sel, float lsel, int k, int lane, int32_t* ids_row,
+                                                float* w_row) {
+  float m = -INFINITY;
+  for (int j = 0; j < k; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, sel, j);
+    const float lj = __shfl_sync(0xffffffffu, lsel, j);
+    if (ej >= 0) m = fmaxf(m, lj);
+  }
+  const float ex = (sel >= 0 && lane < k) ? expf(lsel - m) : 0.0f;
+  float s = 0.0f;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    ids_row[lane] = sel;
+    w_row[lane] = sel >= 0 ? ex / s : 0.0f;
+  }
+}
+
 // Decode-sized router: one warp per expert, tokens in groups of 8.  Each lane owns the
 // k-positions {4*lane + 128*j}; the warp sums its lanes at the end.
 template <typename XT>
@@ -121,77 +219,266 @@ __global__ void __launch_bounds__(512) k_router_small(const XT* __restrict__ x, 
     }
 }
 
-// Decode router, split over k inside thread-block clusters.  CTA (32 experts, 256-wide
-// k-slice) stages its slice of Wr (fp32) and of x in shared memory with all threads loading
-// at once, computes partial logits [T][32] into its own shared memory, and the n_slice CTAs
-// of the cluster (one per k-slice) then sum the partials through distributed shared memory,
-// each CTA for a share of the tokens, adding the slices in rank order (deterministic).
-constexpr int kRcE = 32, kRcK = 256, kRcThreads = 256;
-template <typename XT>
-__global__ void __launch_bounds__(kRcThreads) k_router_cluster(const XT* __restrict__ x, int T, int d, int E,
-                                                               const float* __restrict__ Wr,
-                                                               const float* __restrict__ bias,
-                                                               float* __restrict__ logits) {
+// Decode routers with the selection fused in.  Grid (expert groups of 16, k-slices of 256,
+// token blocks of 64); the k-slices of one (expert group, token block) form a thread-block
+// cluster.  Each CTA computes partial logits [64 tokens][16 experts] over its k-slice; then
+// decode_router_tail sums the cluster's partials and selects.
+constexpr int kRdE = 16, kRdK = 256, kRdT = 64, kRdThreads = 256;
+
+// Cluster rank r sums the n_slice partials of token sub-block r through distributed shared
+// memory in rank order (deterministic) and writes logits + bias.  With ids != NULL, the CTAs
+// that wrote token sub-block r of token block z then count themselves on a ticket; the last of
+// them (every expert group's logits for those tokens are written by then) picks top-k and
+// weights for those tokens, a warp per token, as k_select does, and resets the ticket.
+__device__ __forceinline__ void decode_router_tail(const float* part, int Tb, int E, const float* __restrict__ bias,
+                                                   float* logits, int k, int32_t* __restrict__ ids,
+                                                   float* __restrict__ wts, int* tickets, int* last_flag) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ __align__(16) uint8_t rc_smem[];
-  float* ws = reinterpret_cast<float*>(rc_smem);                      // [kRcE][kRcK + 4]
-  XT* xs = reinterpret_cast<XT*>(ws + kRcE * (kRcK + 4));             // [T][kRcK + 8]
-  float* part = reinterpret_cast<float*>(xs + size_t(T) * (kRcK + 8));  // [T][kRcE]
-  pdl_begin();
-  const int e0 = blockIdx.x * kRcE, k0 = blockIdx.y * kRcK;
   const int tid = threadIdx.x;
-  for (int i = tid; i < kRcE * (kRcK / 4); i += kRcThreads) {
-    const int r = i / (kRcK / 4), c = (i % (kRcK / 4)) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (e0 + r < E) v = *reinterpret_cast<const float4*>(Wr + size_t(e0 + r) * d + k0 + c);
-    *reinterpret_cast<float4*>(ws + r * (kRcK + 4) + c) = v;
-  }
-  constexpr int kVec = 16 / sizeof(XT);  // elements per 16-byte load
-  for (int i = tid; i < T * (kRcK / kVec); i += kRcThreads) {
-    const int t = i / (kRcK / kVec), c = (i % (kRcK / kVec)) * kVec;
-    *reinterpret_cast<uint4*>(xs + size_t(t) * (kRcK + 8) + c) =
-        *reinterpret_cast<const uint4*>(x + size_t(t) * d + k0 + c);
-  }
-  __syncthreads();
-  const int e = tid & 31, tg = tid >> 5;  // lane = expert, warp = tokens tg, tg + 8, ...
-  for (int tb = tg; tb < T; tb += 8 * 8) {  // up to 8 tokens per pass
-    float acc[8];
+  const int e0 = blockIdx.x * kRdE, t_base = blockIdx.z * kRdT;
+  cluster.sync();
+  const int n_slice = int(cluster.num_blocks()), rank = int(cluster.block_rank());
+  const int per = (Tb + n_slice - 1) / n_slice;
+  const int t_lo = min(Tb, rank * per), t_hi = min(Tb, t_lo + per);
+  for (int i = tid; i < (t_hi - t_lo) * kRdE; i += kRdThreads) {  // one pass unless the cluster has < 4 slices
+    const int t = t_lo + i / kRdE, e = i % kRdE;
+    float v[8];  // all remote loads in flight at once, then summed in rank order
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int c = 0; c < kRcK; c += 4) {
-      const float4 wv = *reinterpret_cast<const float4*>(ws + e * (kRcK + 4) + c);
+    for (int r = 0; r < 8; ++r) v[r] = cluster.map_shared_rank(part, min(r, n_slice - 1))[t * kRdE + e];
+    float sum = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int t = tb + 8 * j;
-        if (t < T) {
-          float xv[4];
-          load4(xs + size_t(t) * (kRcK + 8) + c, xv);
-          acc[j] = fmaf(xv[0], wv.x, acc[j]);
-          acc[j] = fmaf(xv[1], wv.y, acc[j]);
-          acc[j] = fmaf(xv[2], wv.z, acc[j]);
-          acc[j] = fmaf(xv[3], wv.w, acc[j]);
-        }
+    for (int r = 0; r < 8; ++r)
+      if (r < n_slice) sum += v[r];
+    if (e0 + e < E) logits[size_t(t_base + t) * E + e0 + e] = sum + (bias ? bias[e0 + e] : 0.0f);
+  }
+  // this CTA is done reading its peers' partials; it waits for them to be done with its own
+  // only before it exits
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  if (ids) {
+    __syncthreads();  // the CTA's logits are written ...
+    if (tid == 0) {
+      // ... released device-wide by the ticket, which also acquires what the earlier CTAs released
+      int* ticket = tickets + blockIdx.z * 8 + rank;
+      int old;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
+      const int last = old == int(gridDim.x) - 1;
+      if (last) *ticket = 0;  // every contributor has counted: ready for the next launch
+      *last_flag = last;
+    }
+    __syncthreads();
+    if (*last_flag) {
+      const int warp = tid >> 5, lane = tid & 31;
+      for (int t = t_lo + warp; t < t_hi; t += kRdThreads / 32) {
+        const size_t row = size_t(t_base + t);
+        select_write_free(logits + row * E, E, lane, ids + row * k, wts + row * k);
       }
     }
+  }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fp32 x: SIMT.  The CTA stages its slices of Wr and x in shared memory with every load
+// issued up front; thread = 2 experts x 2 tokens, one sequential fp32 sum over the slice.
+constexpr int kRdLd = kRdK + 4;
+constexpr size_t kRdSmemF32 = size_t(kRdE + kRdT) * kRdLd * 4 + size_t(kRdT) * kRdE * 4 + 16;
+__global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float* __restrict__ x, int T, int d, int E,
+                                                                  const float* __restrict__ Wr,
+                                                                  const float* __restrict__ bias, float* logits,
+                                                                  int k, int32_t* __restrict__ ids,
+                                                                  float* __restrict__ wts, int* tickets) {
+  extern __shared__ __align__(16) uint8_t rd_smem[];
+  float* ws = reinterpret_cast<float*>(rd_smem);  // [kRdE][kRdLd]
+  float* xs = ws + kRdE * kRdLd;                   // [kRdT][kRdLd]
+  float* part = xs + kRdT * kRdLd;                 // [kRdT][kRdE]
+  int* last_flag = reinterpret_cast<int*>(part + kRdT * kRdE);
+  const int tid = threadIdx.x;
+  const int e0 = blockIdx.x * kRdE, k0 = blockIdx.y * kRdK, t_base = blockIdx.z * kRdT;
+  const int Tb = min(kRdT, T - t_base);
+  pdl_begin();
+  {
+    float4 wv[4], xv[16];  // Wr slice: 16 rows x 64 float4; x slice: 64 rows x 64 float4
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = tb + 8 * j;
-      if (t < T) part[t * kRcE + e] = acc[j];
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + kRdThreads * j, r = i >> 6, c = (i & 63) * 4;
+      wv[j] = e0 + r < E ? *reinterpret_cast<const float4*>(Wr + size_t(e0 + r) * d + k0 + c)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int i = tid + kRdThreads * j, t = i >> 6, c = (i & 63) * 4;
+      xv[j] = t < Tb ? *reinterpret_cast<const float4*>(x + size_t(t_base + t) * d + k0 + c)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + kRdThreads * j, r = i >> 6, c = (i & 63) * 4;
+      *reinterpret_cast<float4*>(ws + r * kRdLd + c) = wv[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int i = tid + kRdThreads * j, t = i >> 6, c = (i & 63) * 4;
+      *reinterpret_cast<float4*>(xs + t * kRdLd + c) = xv[j];
     }
   }
-  cluster.sync();
-  const int n_slice = int(cluster.num_blocks());
-  const int rank = int(cluster.block_rank());
-  const int per = (T + n_slice - 1) / n_slice;
-  const int t_lo = rank * per, t_hi = min(T, t_lo + per);
-  for (int i = tid; i < (t_hi - t_lo) * kRcE; i += kRcThreads) {
-    const int t = t_lo + i / kRcE, ee = i % kRcE;
-    float sum = 0.0f;
-    for (int r = 0; r < n_slice; ++r) sum += cluster.map_shared_rank(part, r)[t * kRcE + ee];
-    if (e0 + ee < E) logits[size_t(t) * E + e0 + ee] = sum + (bias ? bias[e0 + ee] : 0.0f);
+  __syncthreads();
+  // thread: experts eg and eg + 8 (rows 4 banks apart: conflict-free), tokens 2 tg and 2 tg + 1
+  const int eg = tid & 7, tg = tid >> 3;
+  if (2 * tg < Tb) {
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    const float* wa = ws + eg * kRdLd;
+    const float* wb = ws + (eg + 8) * kRdLd;
+    const float* xa = xs + (2 * tg) * kRdLd;
+    const float* xb = xa + kRdLd;
+#pragma unroll 4
+    for (int c = 0; c < kRdK; c += 4) {
+      const float4 w0 = *reinterpret_cast<const float4*>(wa + c), w1 = *reinterpret_cast<const float4*>(wb + c);
+      const float4 x0 = *reinterpret_cast<const float4*>(xa + c), x1 = *reinterpret_cast<const float4*>(xb + c);
+      acc[0][0] = fmaf(x0.x, w0.x, acc[0][0]); acc[0][0] = fmaf(x0.y, w0.y, acc[0][0]);
+      acc[0][0] = fmaf(x0.z, w0.z, acc[0][0]); acc[0][0] = fmaf(x0.w, w0.w, acc[0][0]);
+      acc[0][1] = fmaf(x0.x, w1.x, acc[0][1]); acc[0][1] = fmaf(x0.y, w1.y, acc[0][1]);
+      acc[0][1] = fmaf(x0.z, w1.z, acc[0][1]); acc[0][1] = fmaf(x0.w, w1.w, acc[0][1]);
+      acc[1][0] = fmaf(x1.x, w0.x, acc[1][0]); acc[1][0] = fmaf(x1.y, w0.y, acc[1][0]);
+      acc[1][0] = fmaf(x1.z, w0.z, acc[1][0]); acc[1][0] = fmaf(x1.w, w0.w, acc[1][0]);
+      acc[1][1] = fmaf(x1.x, w1.x, acc[1][1]); acc[1][1] = fmaf(x1.y, w1.y, acc[1][1]);
+      acc[1][1] = fmaf(x1.z, w1.z, acc[1][1]); acc[1][1] = fmaf(x1.w, w1.w, acc[1][1]);
+    }
+    part[(2 * tg) * kRdE + eg] = acc[0][0];
+    part[(2 * tg) * kRdE + eg + 8] = acc[0][1];
+    part[(2 * tg + 1) * kRdE + eg] = acc[1][0];
+    part[(2 * tg + 1) * kRdE + eg + 8] = acc[1][1];
   }
-  cluster.sync();  // no CTA leaves while another still reads its partials
+  decode_router_tail(part, Tb, E, bias, logits, k, ids, wts, tickets, last_flag);
+}
+
+// bf16 x: tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).  Wr rows are split on
+// the fly into three bf16 terms hi + mid + lo that together carry its 24 significand bits;
+// with x exact in bf16 every product is exact, so the logit keeps fp32 accuracy, as on the
+// prefill router.  A = 16 experts x 16 k, B = 16 k x 8 tokens.  The CTA stages its slices of Wr
+// (fp32) and x (bf16) in shared memory with 16-byte asynchronous copies, all in flight at
+// once; warp w then takes k-steps 2w and 2w + 1 of the slice for all 8 token tiles (A
+// fragments by 8-byte shared loads, B fragments by ldmatrix), and the 8 warps' accumulators
+// are summed in warp order through shared memory.
+constexpr int kRmLd = 20;          // token-row stride of a warp's partial tile: fragment stores are conflict-free
+constexpr int kRmWLd = kRdK + 8;   // floats per staged Wr row: A-fragment loads are conflict-free
+constexpr int kRmXLd = kRdK + 8;   // bf16 per staged x row: ldmatrix rows are conflict-free
+constexpr size_t kRmOffX = size_t(kRdE) * kRmWLd * 4;
+constexpr size_t kRmOffWpart = kRmOffX + size_t(kRdT) * kRmXLd * 2;
+constexpr size_t kRmOffPart = kRmOffWpart + size_t(kRdThreads / 32) * kRdT * kRmLd * 4;
+constexpr size_t kRdSmemBf16 = kRmOffPart + size_t(kRdT) * kRdE * 4 + 16;
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
+  const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(smem_row));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a)
+               : "memory");
+}
+
+// (a, b) -> three packed bf16 pairs with a = hi.x + mid.x + lo.x (likewise b), low half = a.
+__device__ __forceinline__ void split3(float2 v, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  const float2 r1 = make_float2(v.x - __low2float(h), v.y - __high2float(h));
+  const __nv_bfloat162 m = __floats2bfloat162_rn(r1.x, r1.y);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(r1.x - __low2float(m), r1.y - __high2float(m));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  mid = *reinterpret_cast<const uint32_t*>(&m);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv_bfloat16* __restrict__ x, int T, int d,
+                                                                   int E, const float* __restrict__ Wr,
+                                                                   const float* __restrict__ bias, float* logits,
+                                                                   int k, int32_t* __restrict__ ids,
+                                                                   float* __restrict__ wts, int* tickets) {
+  extern __shared__ __align__(16) uint8_t rd_smem[];
+  float* ws = reinterpret_cast<float*>(rd_smem);                                  // [kRdE][kRmWLd]
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(rd_smem + kRmOffX);        // [kRdT][kRmXLd]
+  float* wpart = reinterpret_cast<float*>(rd_smem + kRmOffWpart);                  // [8 warps][kRdT][kRmLd]
+  float* part = reinterpret_cast<float*>(rd_smem + kRmOffPart);                    // [kRdT][kRdE]
+  int* last_flag = reinterpret_cast<int*>(part + kRdT * kRdE);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int e0 = blockIdx.x * kRdE, k0 = blockIdx.y * kRdK, t_base = blockIdx.z * kRdT;
+  const int Tb = min(kRdT, T - t_base);
+  const int n_tiles = (Tb + 7) >> 3;
+  pdl_begin();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // Wr slice: 16 rows x 64 chunks of 16 bytes
+    const int i = tid + kRdThreads * j, r = i >> 6, c = (i & 63) * 4;
+    const bool ok = e0 + r < E;
+    cp_async16(ws + r * kRmWLd + c, ok ? Wr + size_t(e0 + r) * d + k0 + c : Wr, ok ? 16 : 0);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // x slice: 64 rows x 32 chunks of 16 bytes (rows past the tokens zero-filled)
+    const int i = tid + kRdThreads * j, t = i >> 5, c = (i & 31) * 8;
+    const bool ok = t < Tb;
+    cp_async16(xs + t * kRmXLd + c, ok ? x + size_t(t_base + t) * d + k0 + c : x, ok ? 16 : 0);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  float acc[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+  uint32_t a_hi[2][4], a_mid[2][4], a_lo[2][4];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    // A registers: (row g, cols 2q..), (row g + 8, cols 2q..), (row g, cols 2q + 8..), (row g + 8, cols 2q + 8..)
+    const int kk = warp * 32 + s * 16 + 2 * q;
+    const float* w0 = ws + g * kRmWLd + kk;
+    const float* w1 = w0 + 8 * kRmWLd;
+    split3(*reinterpret_cast<const float2*>(w0), a_hi[s][0], a_mid[s][0], a_lo[s][0]);
+    split3(*reinterpret_cast<const float2*>(w1), a_hi[s][1], a_mid[s][1], a_lo[s][1]);
+    split3(*reinterpret_cast<const float2*>(w0 + 8), a_hi[s][2], a_mid[s][2], a_lo[s][2]);
+    split3(*reinterpret_cast<const float2*>(w1 + 8), a_hi[s][3], a_mid[s][3], a_lo[s][3]);
+  }
+  // ldmatrix x4: matrix m = lane / 8 is (k-step m / 2, k half m % 2) of the token tile; lane
+  // supplies row lane % 8 of it
+  const int mrow = lane & 7, mk = warp * 32 + (lane >> 4) * 16 + ((lane >> 3) & 1) * 8;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < n_tiles) {
+      uint32_t b[4];
+      ldmatrix_x4(b, xs + (8 * j + mrow) * kRmXLd + mk);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        mma_bf16_16816(acc[j], a_lo[s], b[2 * s], b[2 * s + 1]);
+        mma_bf16_16816(acc[j], a_mid[s], b[2 * s], b[2 * s + 1]);
+        mma_bf16_16816(acc[j], a_hi[s], b[2 * s], b[2 * s + 1]);
+      }
+    }
+  }
+  // C registers: (expert g, token 2q), (g, 2q + 1), (g + 8, 2q), (g + 8, 2q + 1) of tile j
+  float* wp = wpart + warp * kRdT * kRmLd;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int t = 8 * j + 2 * q;
+    wp[t * kRmLd + g] = acc[j][0];
+    wp[(t + 1) * kRmLd + g] = acc[j][1];
+    wp[t * kRmLd + g + 8] = acc[j][2];
+    wp[(t + 1) * kRmLd + g + 8] = acc[j][3];
+  }
+  __syncthreads();
+  {
+    const int t = tid >> 2, c = (tid & 3) * 4;  // 64 tokens x 4 groups of 4 experts
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kRdThreads / 32; ++w) {
+      const float4 v = *reinterpret_cast<const float4*>(wpart + (w * kRdT + t) * kRmLd + c);
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    }
+    *reinterpret_cast<float4*>(part + t * kRdE + c) = sum;
+  }
+  decode_router_tail(part, Tb, E, bias, logits, k, ids, wts, tickets, last_flag);
 }
 
 // Prefill-sized router: SIMT tiled GEMM, 64 tokens x 64 experts per CTA, 4x4 per thread.
@@ -245,16 +532,10 @@ __global__ void __launch_bounds__(256) k_router_gemm(const XT* __restrict__ x, i
   }
 }
 
-// "a is preferred over b": larger logit, or equal logit and lower index.
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// Selection: one warp per token.  Free routing picks k rounds of the preferred remaining
-// expert (softmax is monotone in the logit, so selecting on logits selects on
-// probabilities); forced routing validates the given ids.  Weights: softmax over the k
-// selected logits, or forced_w as given.
-__global__ void __launch_bounds__(256) k_select(const float* __restrict__ logits,
+// Selection: one warp per token.  Free routing as select_write_free; forced routing validates
+// the given ids (range and repeats) and takes the router's logits at them, or forced_w as
+// given.
+__global__ void __launch_bounds__(256, 2) k_select(const float* __restrict__ logits,
                                                 const int32_t* __restrict__ forced_ids,
                                                 const float* __restrict__ forced_w, int T, int E, int k,
                                                 int32_t* __restrict__ ids, float* __restrict__ w, DevStatus* st) {
@@ -262,27 +543,21 @@ __global__ void __launch_bounds__(256) k_select(const float* __restrict__ logits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  // lane-local logits of experts lane + 32 j
-  constexpr int kPer = kMaxExperts / 32;
-  float v[kPer];
-  if (!(forced_ids && forced_w)) {
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = e < E ? logits[size_t(t) * E + e] : -INFINITY;
-    }
+  if (!forced_ids) {
+    select_write_free(logits + size_t(t) * E, E, lane, ids + size_t(t) * k, w + size_t(t) * k);
+    return;
   }
-  int sel = -1;     // lane i < k holds slot i's expert
-  float lsel = 0.f; // and its logit
-  if (forced_ids) {
+  int sel = -1;      // lane i < k holds slot i's expert
+  float lsel = 0.f;  // and its logit
+  {
     int e = lane < k ? forced_ids[size_t(t) * k + lane] : -1;
     bool bad = lane < k && (e < 0 || e >= E);
     // a repeat of an earlier slot's id is rejected too
     for (int j = 0; j < k; ++j) {
-      int ej = __shfl_sync(0xffffffffu, e, j);
+      const int ej = __shfl_sync(0xffffffffu, e, j);
       if (lane < k && j < lane && ej == e) bad = true;
     }
-    unsigned badmask = __ballot_sync(0xffffffffu, bad);
+    const unsigned badmask = __ballot_sync(0xffffffffu, bad);
     if (badmask && lane == 0) {
       set_status(st, kFlagBadForced);
       atomicAdd(&st->bad_forced, __popc(badmask));
@@ -295,52 +570,9 @@ __global__ void __launch_bounds__(256) k_select(const float* __restrict__ logits
       }
       return;
     }
-    // each forced expert's logit, fetched from the lane that holds it
-    for (int i = 0; i < k; ++i) {
-      const int ei = __shfl_sync(0xffffffffu, sel, i);
-      float li = 0.0f;
-      if (ei >= 0) {
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-          if (ei == lane + 32 * j) li = v[j];
-        li = __shfl_sync(0xffffffffu, li, ei & 31);
-      }
-      if (lane == i) lsel = li;
-    }
-  } else {
-    unsigned taken = 0;
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !(taken >> j & 1u) && better(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == r) { sel = bi; lsel = bv; }
-    }
+    lsel = sel >= 0 ? logits[size_t(t) * E + sel] : 0.0f;
   }
-  // softmax over the valid selected logits, summed in slot order
-  float m = -INFINITY;
-  for (int j = 0; j < k; ++j) {
-    int ej = __shfl_sync(0xffffffffu, sel, j);
-    float lj = __shfl_sync(0xffffffffu, lsel, j);
-    if (ej >= 0) m = fmaxf(m, lj);
-  }
-  float ex = (sel >= 0 && lane < k) ? expf(lsel - m) : 0.0f;
-  float s = 0.0f;
-  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
-  if (lane < k) {
-    ids[size_t(t) * k + lane] = sel;
-    w[size_t(t) * k + lane] = sel >= 0 ? ex / s : 0.0f;
-  }
+  write_selection(sel, lsel, k, lane, ids + size_t(t) * k, w + size_t(t) * k);
 }
 
 }  // namespace
@@ -362,21 +594,22 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_cluster(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s) {
-  const int n_slice = L.d / kRcK;
-  const size_t xel = x_bf16 ? 2 : 4;
-  const size_t smem = size_t(kRcE) * (kRcK + 4) * 4 + size_t(T) * (kRcK + 8) * xel + size_t(T) * kRcE * 4;
+cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, int32_t* ids,
+                                 float* wts, DevStatus* st, cudaStream_t s) {
+  if (T > kRouterSmallMaxT || L.d % kRdK || L.d / kRdK > 8) return cudaErrorInvalidValue;
+  const int n_slice = L.d / kRdK;
   static cudaError_t attr = [] {
-    const int most = 200 * 1024;
-    cudaError_t e1 = cudaFuncSetAttribute(k_router_cluster<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    cudaError_t e2 = cudaFuncSetAttribute(k_router_cluster<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaError_t e1 = cudaFuncSetAttribute(k_router_decode_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          int(kRdSmemBf16));
+    cudaError_t e2 = cudaFuncSetAttribute(k_router_decode_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          int(kRdSmemF32));
     return e1 != cudaSuccess ? e1 : e2;
   }();
   if (attr != cudaSuccess) return attr;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((L.E + kRcE - 1) / kRcE, n_slice);
-  cfg.blockDim = dim3(kRcThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3((L.E + kRdE - 1) / kRdE, n_slice, (T + kRdT - 1) / kRdT);
+  cfg.blockDim = dim3(kRdThreads);
+  cfg.dynamicSmemBytes = x_bf16 ? kRdSmemBf16 : kRdSmemF32;
   cfg.stream = s;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
@@ -388,9 +621,10 @@ cudaError_t launch_router_cluster(const void* x, bool x_bf16, int T, const Layer
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
   if (x_bf16)
-    return cudaLaunchKernelEx(&cfg, k_router_cluster<__nv_bfloat16>, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias,
-                              logits);
-  return cudaLaunchKernelEx(&cfg, k_router_cluster<float>, (const float*)x, T, L.d, L.E, L.Wr, L.bias, logits);
+    return cudaLaunchKernelEx(&cfg, k_router_decode_bf16, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias, logits,
+                              L.k, ids, wts, st->tickets);
+  return cudaLaunchKernelEx(&cfg, k_router_decode_f32, (const float*)x, T, L.d, L.E, L.Wr, L.bias, logits, L.k, ids,
+                            wts, st->tickets);
 }
 
 cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s) {

@@ -82,6 +82,38 @@ def test_router_logits_ids_weights(moe, kolibri, T):
     assert moe.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("d,E,T,bf16", [(256, 200, 128, True), (512, 200, 65, True), (768, 384, 17, False),
+                                        (1280, 100, 128, True), (2048, 384, 100, False), (512, 512, 64, True),
+                                        (256, 1000, 40, True), (512, 1000, 300, True), (512, 480, 200, True)])
+def test_router_shapes(moe, d, E, T, bf16):
+    """The decode router at every cluster size it takes (d / 256 = 1..8 k-slices), expert counts
+    that leave a ragged expert group or need every lane-register count of the warp selection
+    (E up to 128, 256, 384, 512, 1024), one and two token blocks, bf16 and fp32 x; the prefill
+    routers beside them (tensor-core with fused selection for E <= 512, SIMT + select kernel
+    above); each twice in a row on one workspace, so a selection ticket left behind would show
+    in the second call."""
+    w = g.make_layer(31 + d, d, 64, E, fp8=True, bias_var=0.5)
+    L = moe.Layer.from_host(w)
+    x = g.make_x(32 + d, T, d, bf16=bf16)
+    ws = moe.workspace(L, T)
+    ref = oracle_route(w, x)
+    first = None
+    for _ in range(2):
+        ids, wt, lg = moe.route(to_dev_x(x), L, ws, logits=True)
+        lg = lg.cpu().numpy()
+        err = np.max(np.abs(lg - ref["logits"]), axis=1) / np.max(np.abs(ref["logits"]), axis=1)
+        assert err.max() < 3e-5, err.max()
+        ok, bad, _ = parity.ids_ok(ids.cpu().numpy(), ref["ids"], ref["p"], E)
+        assert ok, bad
+        same = np.all(ids.cpu().numpy() == ref["ids"], axis=1)
+        assert np.max(np.abs(wt.cpu().numpy()[same] - ref["w"][same])) < 1e-5
+        if first is None:
+            first = (ids.clone(), wt.clone())
+        else:
+            assert torch.equal(ids, first[0]) and torch.equal(wt, first[1])
+    assert moe.get_status(ws) == 0
+
+
 def test_router_fp32_tiny(moe, tiny):
     w, L = tiny
     x = g.make_x(g.SEED_TINY, 32, w.d, bf16=False)
