@@ -37,6 +37,9 @@ constexpr int kTileM = 128;       // weight rows per item (MMA M)
 constexpr int kKTile = 128;       // bytes (= E4M3 elements) of k per stage: one 128-byte swizzle atom
 constexpr int kATileBytes = kTileM * kKTile;
 constexpr size_t kTcSmemBudget = 200 * 1024;
+constexpr int kPrefetchBytes = 256 * 1024;  // weights a CTA pulls into L2 before its dependency wait
+constexpr int kMaxStages = 8;
+constexpr int kDownPairMinN = 64;
 
 struct TcArgs {
   int d, F, E;
@@ -53,11 +56,11 @@ struct TcArgs {
   int* status_flags;
 };
 
-template <int kN, bool kGateUp>
+template <int kN, bool kGateUp, int kA_>
 struct TcCfg {
-  static constexpr int kA = kGateUp ? 2 : 1;                         // A tiles per stage
+  static constexpr int kA = kA_;  // A tiles per stage: gate/up 2 (gate and up rows); down 1 or 2 row blocks
   static constexpr int kStageBytes = kA * kATileBytes + kN * kKTile;
-  static constexpr int kStages = int(std::min<size_t>(8, kTcSmemBudget / kStageBytes));
+  static constexpr int kStages = int(std::min<size_t>(kMaxStages, kTcSmemBudget / kStageBytes));
   static constexpr int kColsPerAcc = kA * kN;
   static constexpr int kBufs = (2 * kColsPerAcc <= 512) ? 2 : 1;
   static constexpr int kTmemCols = (kBufs * kColsPerAcc <= 32)    ? 32
@@ -69,8 +72,8 @@ struct TcCfg {
 };
 
 struct TcCtl {
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
@@ -78,11 +81,12 @@ struct TcCtl {
   int abort;
 };
 
-template <int kN, bool kGateUp>
+template <int kN, bool kGateUp, int kA>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_expert_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_wsh,
                 const __grid_constant__ CUtensorMap map_x, TcArgs a) {
-  using C = TcCfg<kN, kGateUp>;
+  using C = TcCfg<kN, kGateUp, kA>;
+  static_assert(!kGateUp || kA == 2, "gate/up stages hold the gate and the up rows");
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   TcCtl* ctl = reinterpret_cast<TcCtl*>(smem + size_t(C::kStages) * C::kStageBytes);
@@ -108,18 +112,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_begin();
   const uint32_t tmem = ctl->tmem_base;
 
+  // the tile list comes from the dispatch kernel, which completed before the kernel this
+  // launch overlaps started: readable before the dependency wait
   const int n_tiles = *a.n_tiles;
-  const int nblk = (kGateUp ? a.F : a.d) / kTileM;   // weight-row blocks per group
-  const int KT = (kGateUp ? a.d : a.F) / kKTile;      // k-steps per item
+  const int nblk = kGateUp ? a.F / kTileM : a.d / (kTileM * kA);  // items per tile
+  const int KT = (kGateUp ? a.d : a.F) / kKTile;                  // k-steps per item
   const int total = n_tiles * nblk;
   auto stage_a = [&](int s, int i) { return smem + size_t(s) * C::kStageBytes + i * kATileBytes; };
   auto stage_b = [&](int s) { return smem + size_t(s) * C::kStageBytes + C::kA * kATileBytes; };
 
+  auto weight_row = [&](const Tile& tl, int nb) {  // first weight row of an item's A tile 0
+    return (tl.group == a.E ? 0 : tl.group * (kGateUp ? 2 * a.F : a.d)) + nb * kTileM * (kGateUp ? 1 : kA);
+  };
+  const int a1_off = kGateUp ? a.F : kTileM;  // rows from A tile 0 to A tile 1: the up rows, or the next block
+
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
+      // Weights need nothing from the kernel this launch overlaps: pull this CTA's first
+      // items into L2 while that kernel runs (up to kPrefetchBytes), then wait for it.
+      int budget = kPrefetchBytes;
+      for (int item = blockIdx.x; item < total && budget > 0; item += gridDim.x) {
+        const Tile tl = a.tiles[item / nblk];
+        const CUtensorMap* mw = tl.group == a.E ? &map_wsh : &map_w;
+        const int wrow = weight_row(tl, item % nblk);
+        for (int kt = 0; kt < KT && budget > 0; ++kt, budget -= kA * kATileBytes) {
+          tma_prefetch_2d(mw, kt * kKTile, wrow);
+          if (kA == 2) tma_prefetch_2d(mw, kt * kKTile, wrow + a1_off);
+        }
+      }
+      pdl_begin();
       const uint64_t pol = policy_evict_first();
       int it = 0;
       bool stop = false;
@@ -128,7 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nb = item % nblk;
         const bool shared = tl.group == a.E;
         const CUtensorMap* mw = shared ? &map_wsh : &map_w;
-        const int wrow = (shared ? 0 : tl.group * (kGateUp ? 2 * a.F : a.d)) + nb * kTileM;
+        const int wrow = weight_row(tl, nb);
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int s = it % C::kStages, use = it / C::kStages;
           if (!mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort)) {
@@ -138,7 +161,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           mbar_arrive_expect_tx(&ctl->full[s], C::kStageBytes);
           tma_load_2d_hint(stage_a(s, 0), mw, kt * kKTile, wrow, &ctl->full[s], pol);
-          if (kGateUp) tma_load_2d_hint(stage_a(s, 1), mw, kt * kKTile, wrow + a.F, &ctl->full[s], pol);
+          if (kA == 2) tma_load_2d_hint(stage_a(s, 1), mw, kt * kKTile, wrow + a1_off, &ctl->full[s], pol);
           tma_load_2d(stage_b(s), &map_x, kt * kKTile, tl.row0, &ctl->full[s]);
         }
       }
@@ -148,8 +171,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int zero = 0;
         mbar_wait(&ctl->full[s], last_use & 1, &zero);
       }
+    } else {
+      pdl_begin();
     }
   } else if (warp == 1) {
+    pdl_begin();
     if (lane == 0) {  // ------------------------------------------------ MMA issuer
       constexpr uint32_t idesc = idesc_e4m3(kTileM, kN);
       int it = 0, jt = 0;
@@ -171,13 +197,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           const uint64_t da0 = sw128_desc(stage_a(s, 0));
-          const uint64_t da1 = kGateUp ? sw128_desc(stage_a(s, 1)) : 0;
+          const uint64_t da1 = kA == 2 ? sw128_desc(stage_a(s, 1)) : 0;
           const uint64_t db = sw128_desc(stage_b(s));
 #pragma unroll
           for (int kk = 0; kk < kKTile / 32; ++kk) {
             const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
             tc_mma_f8(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            if (kGateUp) tc_mma_f8(d0 + kN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            if (kA == 2) tc_mma_f8(d0 + kN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
           tc_commit(&ctl->empty[s]);
         }
@@ -189,6 +215,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait(&ctl->mma_done, 0, &zero);
     }
   } else {  // ------------------------------------------------------------ epilogue
+    pdl_begin();
     // warps 2..9: lane quarter q = warp % 4 (the TMEM lanes this warp may read), column half
     // ch = (warp - 2) / 4 of the kN token columns
     const int q = warp & 3, ch = (warp - 2) >> 2;
@@ -240,11 +267,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       } else {
-        const int m = nb * kTileM + rloc;
+#pragma unroll
+       for (int ai = 0; ai < kA; ++ai) {  // row block ai of the item: accumulator columns ai * kN
+        const int m = (nb * kA + ai) * kTileM + rloc;
         const float sdm = shared ? a.sh_sd[m] : a.sd[size_t(tl.group) * a.d + m];
         for (int c0 = cbeg; c0 < cend && c0 < tl.nrows; c0 += 16) {
           float yv[16];
-          tmem_ld16(taddr + c0, yv);
+          tmem_ld16(taddr + ai * kN + c0, yv);
           const float sh_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sh[tl.row0 + c0 + lane] : 0.0f;
           float* yp = a.y_rows + size_t(tl.row0 + c0) * a.d + m;
           if (c0 + 16 <= tl.nrows) {
@@ -258,6 +287,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
+       }
       }
       tc_fence_before();
       __syncwarp();
@@ -284,25 +314,25 @@ int sm_count() {
   return sms;
 }
 
-template <int kN, bool kGateUp>
+template <int kN, bool kGateUp, int kA>
 cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mwsh, const CUtensorMap& mx, const TcArgs& a,
                       long long max_items, cudaStream_t s) {
-  using C = TcCfg<kN, kGateUp>;
-  static cudaError_t attr =
-      cudaFuncSetAttribute(k_expert_tc<kN, kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
+  using C = TcCfg<kN, kGateUp, kA>;
+  static cudaError_t attr = cudaFuncSetAttribute(k_expert_tc<kN, kGateUp, kA>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
   if (attr != cudaSuccess) return attr;
   const int grid = int(std::max<long long>(1, std::min<long long>(max_items, sm_count())));
-  return launch_pdl(k_expert_tc<kN, kGateUp>, dim3(grid), dim3(kTcThreads), C::kSmemBytes, s, mw, mwsh, mx, a);
+  return launch_pdl(k_expert_tc<kN, kGateUp, kA>, dim3(grid), dim3(kTcThreads), C::kSmemBytes, s, mw, mwsh, mx, a);
 }
 
-template <bool kGateUp>
+template <bool kGateUp, int kA>
 cudaError_t launch_tc_n(int kN, const CUtensorMap& mw, const CUtensorMap& mwsh, const CUtensorMap& mx,
                         const TcArgs& a, long long max_items, cudaStream_t s) {
   switch (kN) {
-    case 16: return launch_tc<16, kGateUp>(mw, mwsh, mx, a, max_items, s);
-    case 32: return launch_tc<32, kGateUp>(mw, mwsh, mx, a, max_items, s);
-    case 64: return launch_tc<64, kGateUp>(mw, mwsh, mx, a, max_items, s);
-    case 128: return launch_tc<128, kGateUp>(mw, mwsh, mx, a, max_items, s);
+    case 16: return launch_tc<16, kGateUp, kA>(mw, mwsh, mx, a, max_items, s);
+    case 32: return launch_tc<32, kGateUp, kA>(mw, mwsh, mx, a, max_items, s);
+    case 64: return launch_tc<64, kGateUp, kA>(mw, mwsh, mx, a, max_items, s);
+    case 128: return launch_tc<128, kGateUp, kA>(mw, mwsh, mx, a, max_items, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -350,7 +380,7 @@ cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char*
       !make_map(&mx, base + ws.xq, uint64_t(ws.R_alloc), L.d, kN))
     return cudaErrorInvalidValue;
   const long long items = max_tc_tiles(L, T, kN) * (L.F / kTileM);
-  return launch_tc_n<true>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, s);
+  return launch_tc_n<true, 2>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, s);
 }
 
 cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
@@ -360,8 +390,14 @@ cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* b
       !make_map(&mwsh, L.sh_wd, uint64_t(L.d), L.F, kTileM) ||
       !make_map(&mx, base + ws.qh, uint64_t(ws.R_alloc), L.F, kN))
     return cudaErrorInvalidValue;
+  // two 128-row blocks per item (two accumulators fed from one activation stage) where d allows
+  // and the tiles are wide enough for the activation traffic to matter
+  if (L.d % (2 * kTileM) == 0 && kN >= kDownPairMinN) {
+    const long long items = max_tc_tiles(L, T, kN) * (L.d / (2 * kTileM));
+    return launch_tc_n<false, 2>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, s);
+  }
   const long long items = max_tc_tiles(L, T, kN) * (L.d / kTileM);
-  return launch_tc_n<false>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, s);
+  return launch_tc_n<false, 1>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, s);
 }
 
 }  // namespace moe
