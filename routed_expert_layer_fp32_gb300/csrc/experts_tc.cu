@@ -26,9 +26,11 @@
 // item: rank 0 runs the first half of the k-steps, rank 1 the second; rank 1's epilogue
 // writes its fp32 partial accumulators into rank 0's shared memory (distributed shared
 // memory, an mbarrier counting the writers), and rank 0 adds them to its own (always in that
-// order, so results do not depend on timing) before the nonlinearity.  Every wait is bounded (tma.cuh): on a timeout the CTA
-// records MOE_ERR_TIMEOUT, all roles leave their loops, the producer waits for its loads in
-// flight, the MMA issuer waits for its MMAs, and TMEM is freed before the CTA exits.
+// order, so results do not depend on timing) before the nonlinearity.
+//
+// Every wait is bounded (tma.cuh): on a timeout the CTA records MOE_ERR_TIMEOUT, all roles
+// leave their loops, the producer waits for its loads in flight, the MMA issuer waits for its
+// MMAs, and TMEM is freed before the CTA exits.
 #include <algorithm>
 
 #include "common.cuh"
