@@ -298,9 +298,11 @@ def run_ours(args):
     if not args.no_extra:
         for Tx in (1, 8):
             extra[f"decode_T{Tx}"] = small_batch(moe, g, layers, Tx, args, hbm_peak, flags)
+        extra["zipf_forced_T128"] = zipf_forced(moe, g, layers, args, hbm_peak, flags)
     if not args.no_prefill:
         for Tx in (2048, 16384):
             extra[f"prefill_T{Tx}"] = prefill(moe, g, layers[0], Tx, flags)
+        extra["prefill_T2048_as_4x512_forced"] = prefill_forced_chunks(moe, g, layers[0], flags)
     if not args.no_stack:
         del layers[1:]
         torch.cuda.empty_cache()
@@ -440,6 +442,78 @@ def small_batch(moe, g, layers, T, args, hbm_peak, flags=0):
     nbytes, U = layer_bytes(ids.cpu().numpy(), T)
     return {"tokens_per_s": T / (ms * 1e-3), "ms_per_layer": ms, "unique_experts": U, "bytes": nbytes,
             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "timing": f"CUDA graph over {n} layer copies"}
+
+
+def zipf_forced(moe, g, layers, args, hbm_peak, flags=0, T=128):
+    """Batched decode of 128 tokens with forced routing: Zipf(1.1) expert ids (six per token,
+    without replacement) and Dirichlet(1) weights, the load-imbalanced grouped GEMM; CUDA graph
+    over the rotated layer copies, as small_batch."""
+    import torch
+    x = torch.from_numpy(g.make_x(g.SEED_ZIPF, T, D, bf16=True).view(np.int16).copy()).cuda().view(torch.bfloat16)
+    fid_h = g.zipf_ids(g.SEED_ZIPF, 0, T, 384, K, 1.1)
+    fid = torch.from_numpy(fid_h).cuda()
+    fw = torch.from_numpy(g.dirichlet_w(g.SEED_ZIPF, 0, T, K)).cuda()
+    ws = moe.workspace(layers[0], T)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    n = len(layers)
+
+    def run():
+        for i in range(n):
+            moe.forward(x, layers[i], ws, forced_ids=fid, forced_w=fw, out=y, ids=ids, w=wt, flags=flags)
+
+    run()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // n)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * n)
+    nbytes, U = layer_bytes(fid_h, T)
+    return {"tokens_per_s": T / (ms * 1e-3), "ms_per_layer": ms, "unique_experts": U, "bytes": nbytes,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "timing": f"CUDA graph over {n} layer copies"}
+
+
+def prefill_forced_chunks(moe, g, layer, flags, T=2048, chunk=512, iters=10):
+    """The 2048-token prefill run free once (recording ids), then replayed as four 512-token
+    calls with routing forced from the recorded ids (weights from each call's own router);
+    tokens/s over the four forced calls, timed with CUDA events."""
+    import torch
+    x = torch.from_numpy(g.make_x(g.SEED_PREFILL, T, D, bf16=True).view(np.int16).copy()).cuda().view(torch.bfloat16)
+    ws = moe.workspace(layer, T)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    _, ids, _ = moe.forward(x, layer, ws, out=y, flags=flags)
+    ids = ids.clone()
+    yc = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+
+    def run():
+        for c in range(0, T, chunk):
+            moe.forward(x[c:c + chunk], layer, ws, forced_ids=ids[c:c + chunk], out=yc[c:c + chunk], flags=flags)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    return {"tokens_per_s": T / (ms * 1e-3), "ms_per_2048_tokens": ms, "calls": T // chunk}
 
 
 # ---------------------------------------------------------------------------- oracle ------
