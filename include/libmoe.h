@@ -26,10 +26,10 @@
  *    recorded in the workspace and reported by moe_get_status().  Nothing traps.
  *  - T == 0 is a no-op returning MOE_OK.
  *  - Alignment: x, y, weights, scales and the workspace 16-byte aligned.
- *  - Shapes: top_k == 6 (else MOE_ERR_UNSUPPORTED), n_experts <= 1024, T <= 2^20,
- *    d_model % 256 == 0, d_model <= 2048, ffn % 64 == 0, ffn <= 640 for E4M3 weights;
- *    d_model % 128 == 0 and
- *    ffn % 32 == 0 for fp32 weights.
+ *  - Shapes: top_k == 6 (else MOE_ERR_UNSUPPORTED), n_experts <= 1024, T <= 2^20;
+ *    E4M3 weights in the tiled layout: d_model % 128 == 0 and ffn % 128 == 0; E4M3 weights
+ *    in the row layout: d_model % 256 == 0, d_model <= 2048, ffn % 64 == 0, ffn <= 640;
+ *    fp32 weights: d_model % 128 == 0 and ffn % 32 == 0.
  *  - Layout: row-major, last index contiguous.
  */
 #ifndef LIBMOE_H
@@ -58,6 +58,23 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
 
+/* Byte order of the E4M3 expert weight tensors (w_gate_up, w_down, sh_gate_up, sh_down).
+ *   MOE_LAYOUT_ROWS   the shapes below, row-major (a checkpoint's order).
+ *   MOE_LAYOUT_TILED  the same bytes regrouped by moe_pack_weights into 16 KB tiles of 128
+ *                     rows x 128 bytes of k, each tile stored in the 128-byte-swizzled order
+ *                     the tensor cores read, and ordered so that the tiles one GEMM step
+ *                     needs are contiguous:
+ *                     gate/up tile (e, n, j, half) at byte ((((e * F/128) + n) * d/128 + j) * 2 + half) * 16384
+ *                       = rows half*F + 128 n .. +127 of expert e's [2F, d] matrix, k = 128 j .. 128 j + 127
+ *                     down tile (e, m, j) at byte (((e * d/128) + m) * F/128 + j) * 16384
+ *                       = rows 128 m .. +127 of expert e's [d, F] matrix, k = 128 j .. +127
+ *                     inside a tile, byte (r, c) sits at r*128 + 16*((c/16) ^ (r%8)) + c%16.
+ *                     The shared expert's tensors are tiled the same way (as expert 0).
+ *                     Requires E4M3, d_model % 128 == 0 and ffn % 128 == 0.
+ * The tensor-core expert kernels read the tiled layout (each pipeline stage is then one
+ * contiguous copy of 32-80 KB); the weight-streaming kernels read the row layout. */
+typedef enum { MOE_LAYOUT_ROWS = 0, MOE_LAYOUT_TILED = 1 } moe_layout;
+
 /* One layer: borrowed device pointers.  Shapes with d = d_model, F = ffn, E = n_experts.
  *   w_router     [E, d]  fp32            router_bias [E] fp32 or NULL
  *   w_gate_up    [E, 2, F, d]            gate rows (index 0) then up rows (index 1)
@@ -79,12 +96,23 @@ typedef struct {
   const float* sh_s_gate_up;
   const void* sh_down;
   const float* sh_s_down;
+  moe_layout w_layout; /* order of the four E4M3 weight tensors (MOE_LAYOUT_ROWS for fp32) */
 } moe_layer;
 
-/* Flags for moe_forward / moe_forward_stack: which expert kernels run.  0 = automatic. */
+/* Flags for moe_forward / moe_forward_stack: which expert kernels run.  0 = automatic: the
+ * tcgen05 grouped GEMMs for tiled E4M3 weights, the weight-streaming kernels otherwise. */
 #define MOE_PATH_AUTO 0u
-#define MOE_PATH_STREAM 1u /* weight-streaming kernels (any T; sized for decode) */
-#define MOE_PATH_TC 2u     /* tcgen05 grouped GEMM (prefill-sized groups) */
+#define MOE_PATH_STREAM 1u /* weight-streaming kernels (row layout; any T) */
+#define MOE_PATH_TC 2u     /* tcgen05 grouped GEMMs (tiled layout; any T) */
+
+/* Writes the tiled layout (MOE_LAYOUT_TILED above) of src's four E4M3 weight tensors, which
+ * must be in the row layout, into gate_up [E*2*F*d], down [E*d*F], sh_gate_up [2*F*d] and
+ * sh_down [d*F] bytes of caller-owned device memory (16-byte aligned, not overlapping the
+ * sources).  The scales and the router are unchanged; a moe_layer with the four pointers
+ * replaced and w_layout = MOE_LAYOUT_TILED then describes the same layer.  Asynchronous on
+ * `stream`.  MOE_ERR_UNSUPPORTED unless E4M3 with d_model % 128 == 0 and ffn % 128 == 0. */
+moe_status moe_pack_weights(const moe_layer* src, void* gate_up, void* down, void* sh_gate_up, void* sh_down,
+                            moe_stream_t stream);
 
 /* Bytes of workspace the calls below need for T tokens of this layer (host only). */
 size_t moe_workspace_bytes(const moe_layer* layer, int T);

@@ -29,10 +29,13 @@ moe_status check_layer(const moe_layer* L) {
   if (!aligned16(L->w_router) || !aligned16(L->w_gate_up) || !aligned16(L->w_down) || !aligned16(L->sh_gate_up) ||
       !aligned16(L->sh_down))
     return MOE_ERR_INVALID_ARG;
+  if (L->w_layout != MOE_LAYOUT_ROWS && L->w_layout != MOE_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
   if (L->w_dtype == MOE_E4M3) {
     if (!L->s_gate_up || !L->s_down || !L->sh_s_gate_up || !L->sh_s_down) return MOE_ERR_INVALID_ARG;
-    if (!stream_ok(*L) && !(L->d_model % 128 == 0 && L->ffn % 128 == 0)) return MOE_ERR_UNSUPPORTED;
+    if (L->w_layout == MOE_LAYOUT_TILED ? !(L->d_model % 128 == 0 && L->ffn % 128 == 0) : !stream_ok(*L))
+      return MOE_ERR_UNSUPPORTED;
   } else if (L->w_dtype == MOE_F32) {
+    if (L->w_layout != MOE_LAYOUT_ROWS) return MOE_ERR_INVALID_ARG;
     if (L->d_model % 128 != 0 || L->ffn % 32 != 0) return MOE_ERR_UNSUPPORTED;
   } else {
     return MOE_ERR_INVALID_ARG;
@@ -47,6 +50,7 @@ LayerDev to_dev(const moe_layer* L) {
   d.E = L->n_experts;
   d.k = L->top_k;
   d.fp8 = L->w_dtype == MOE_E4M3;
+  d.tiled = L->w_layout == MOE_LAYOUT_TILED;
   d.Wr = L->w_router;
   d.bias = L->router_bias;
   d.wgu = static_cast<const uint8_t*>(L->w_gate_up);
@@ -86,10 +90,11 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   int32_t* perm = reinterpret_cast<int32_t*>(base + lay.perm);
   int32_t* pos = reinterpret_cast<int32_t*>(base + lay.pos);
   const bool x_bf16 = x_dtype == MOE_BF16;
-  // expert path: tcgen05 grouped GEMM where it applies (unless the stream path is asked for)
-  bool use_tc = L.fp8 && !(flags & MOE_PATH_STREAM) && tc_supported(L);
+  // expert path: the tcgen05 grouped GEMMs read tiled weights, the streaming kernels rows
+  const bool use_tc = L.tiled && tc_supported(L);
   if ((flags & MOE_PATH_TC) && !use_tc) return MOE_ERR_UNSUPPORTED;
-  if (!use_tc && !stream_ok(*Lh)) return MOE_ERR_UNSUPPORTED;
+  if ((flags & MOE_PATH_STREAM) && use_tc) return MOE_ERR_UNSUPPORTED;
+  if (!use_tc && (L.tiled || !stream_ok(*Lh))) return MOE_ERR_UNSUPPORTED;
   const int rows_per_tile = use_tc ? tc_rows_per_tile(T) : kStreamRows;
   // ev (optional): MOE_TRACE_POINTS events, recorded before the first stage and after each
   auto mark = [&](int i) -> cudaError_t {
@@ -172,6 +177,23 @@ size_t moe_workspace_bytes(const moe_layer* layer, int T) {
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!ws || !aligned16(ws) || ws_bytes < sizeof(DevStatus)) return MOE_ERR_INVALID_ARG;
   return cuda_status(cudaMemsetAsync(ws, 0, sizeof(DevStatus), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_pack_weights(const moe_layer* src, void* gate_up, void* down, void* sh_gate_up, void* sh_down,
+                            moe_stream_t stream) {
+  // only the four weight tensors are read: no check of the shapes the other kernels need
+  if (!src || src->w_dtype != MOE_E4M3 || src->w_layout != MOE_LAYOUT_ROWS) return MOE_ERR_INVALID_ARG;
+  if (src->n_experts < 1 || src->n_experts > kMaxExperts || src->d_model <= 0 || src->ffn <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!src->w_gate_up || !src->w_down || !src->sh_gate_up || !src->sh_down || !aligned16(src->w_gate_up) ||
+      !aligned16(src->w_down) || !aligned16(src->sh_gate_up) || !aligned16(src->sh_down))
+    return MOE_ERR_INVALID_ARG;
+  if (src->d_model % 128 != 0 || src->ffn % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!gate_up || !down || !sh_gate_up || !sh_down || !aligned16(gate_up) || !aligned16(down) ||
+      !aligned16(sh_gate_up) || !aligned16(sh_down))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_weights(to_dev(src), gate_up, down, sh_gate_up, sh_down,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, int k, int32_t* ids_out,

@@ -189,6 +189,7 @@ namespace moe {
 struct LayerDev {
   int d, F, E, k;
   bool fp8;
+  bool tiled;  // E4M3 weights in the tiled layout (MOE_LAYOUT_TILED)
   const float* Wr;
   const float* bias;
   const uint8_t* wgu;
@@ -202,6 +203,9 @@ struct LayerDev {
 };
 
 cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
+// The four E4M3 weight tensors of L (row layout) rewritten in the tiled layout.
+cudaError_t launch_pack_weights(const LayerDev& L, void* gate_up, void* down, void* sh_gate_up, void* sh_down,
+                                cudaStream_t s);
 cudaError_t launch_select(const float* logits, const int32_t* forced_ids, const float* forced_w, int T,
                           const LayerDev& L, int32_t* ids, float* w, DevStatus* st, cudaStream_t s);
 // Prefill router on tensor cores (bf16 x, Wr split into three bf16 terms in w3 [3, E, d]).

@@ -42,10 +42,10 @@ namespace {
 
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter, splitting the columns
 constexpr int kTcThreads = (2 + kEpiWarps) * 32;
-constexpr int kTileM = 128;       // weight rows per item (MMA M)
-constexpr int kKTile = 128;       // bytes (= E4M3 elements) of k per stage: one 128-byte swizzle atom
-constexpr int kATileBytes = kTileM * kKTile;
-constexpr size_t kTcSmemBudget = 220 * 1024;  // stages + split-K receive buffer
+constexpr int kTileM = 128;       // weight rows per accumulator (MMA M)
+constexpr int kKTile = 128;       // bytes (= E4M3 elements) of k per chunk: one 128-byte swizzle atom
+constexpr int kATileBytes = kTileM * kKTile;  // one weight tile of the tiled layout (16 KB)
+constexpr size_t kTcSmemCap = 226 * 1024;     // dynamic shared memory per CTA
 constexpr int kPrefetchBytes = 256 * 1024;  // weights a CTA pulls into L2 before its dependency wait
 constexpr int kMaxStages = 8;
 constexpr int kDownPairMinN = 64;
@@ -53,6 +53,8 @@ constexpr int kSplitMaxT = 16;  // gate/up k-steps split over a CTA pair up to t
 
 struct TcArgs {
   int d, F, E;
+  const uint8_t* w;    // tiled weights of the routed experts (gate/up or down)
+  const uint8_t* wsh;  // the shared expert's, same layout
   const Tile* tiles;
   const int* n_tiles;
   const float* sx;      // [R] activation scales (gate/up)
@@ -78,14 +80,23 @@ struct TcCtl {
   int abort;
 };
 
-template <int kN, bool kGateUp, int kA_, int kSplit_>
+// kA accumulators of kN columns (gate/up: gate and up rows of the same 128 outputs; down:
+// 1 or 2 blocks of 128 output rows); a stage holds kC consecutive 128-byte k-chunks: the kA
+// weight tiles of each chunk (one contiguous copy for gate/up, one per block for down) and the
+// kN activation rows of those chunks (one 3-D tensor-map box).
+template <int kN, bool kGateUp, int kA_, int kSplit_, int kC_>
 struct TcCfg {
-  static constexpr int kA = kA_;  // A tiles per stage: gate/up 2 (gate and up rows); down 1 or 2 row blocks
+  static constexpr int kA = kA_;
   static constexpr int kSplit = kSplit_;  // CTAs (one cluster) sharing an item's k-steps
-  static constexpr int kStageBytes = kA * kATileBytes + kN * kKTile;
+  static constexpr int kC = kC_;
+  static constexpr int kABytes = kA * kC * kATileBytes;
+  static constexpr int kBBytes = kC * kN * kKTile;
+  static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRecvBytes = kSplit == 2 ? kA * kTileM * kN * 4 : 0;  // [kA][kN cols][128 rows] fp32
   static constexpr int kStages =
-      int(std::min<size_t>(kMaxStages, (kTcSmemBudget - kRecvBytes - 2048) / kStageBytes));
+      int(std::min<size_t>(kMaxStages, (kTcSmemCap - kRecvBytes - 1024 - sizeof(TcCtl)) / kStageBytes));
+  static_assert(kStages >= 2, "at least a double-buffered stage ring");
+  static_assert(kStageBytes % 1024 == 0 && (kN * kKTile) % 1024 == 0, "stages and chunks keep the swizzle atoms aligned");
   static constexpr int kColsPerAcc = kA * kN;
   static constexpr int kBufs = (2 * kColsPerAcc <= 512) ? 2 : 1;
   static constexpr int kTmemCols = (kBufs * kColsPerAcc <= 32)    ? 32
@@ -97,12 +108,10 @@ struct TcCfg {
       size_t(kStages) * kStageBytes + kRecvBytes + 1024 /* alignment slack */ + sizeof(TcCtl);
 };
 
-
-template <int kN, bool kGateUp, int kA, int kSplit>
+template <int kN, bool kGateUp, int kA, int kSplit, int kC>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_expert_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_wsh,
-                const __grid_constant__ CUtensorMap map_x, TcArgs a) {
-  using C = TcCfg<kN, kGateUp, kA, kSplit>;
+    k_expert_tc(const __grid_constant__ CUtensorMap map_x, TcArgs a) {
+  using C = TcCfg<kN, kGateUp, kA, kSplit, kC>;
   static_assert(!kGateUp || kA == 2, "gate/up stages hold the gate and the up rows");
   static_assert(kSplit == 1 || kSplit == 2, "items are split over one or two CTAs");
   extern __shared__ uint8_t tc_smem_raw[];
@@ -144,16 +153,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // launch overlaps started: readable before the dependency wait
   const int n_tiles = *a.n_tiles;
   const int nblk = kGateUp ? a.F / kTileM : a.d / (kTileM * kA);  // items per tile
-  const int KT = (kGateUp ? a.d : a.F) / kKTile;                  // k-steps per item
-  const int kt_lo = rank * KT / kSplit, kt_hi = (rank + 1) * KT / kSplit;  // this CTA's share
+  const int KT = (kGateUp ? a.d : a.F) / kKTile;                  // 128-byte k-chunks per item
+  const int KS = KT / kC;                                          // stages per item
+  const int ks_lo = rank * KS / kSplit, ks_hi = (rank + 1) * KS / kSplit;  // this CTA's share
   const int total = n_tiles * nblk;
-  auto stage_a = [&](int s, int i) { return smem + size_t(s) * C::kStageBytes + i * kATileBytes; };
-  auto stage_b = [&](int s) { return smem + size_t(s) * C::kStageBytes + C::kA * kATileBytes; };
-
-  auto weight_row = [&](const Tile& tl, int nb) {  // first weight row of an item's A tile 0
-    return (tl.group == a.E ? 0 : tl.group * (kGateUp ? 2 * a.F : a.d)) + nb * kTileM * (kGateUp ? 1 : kA);
+  const int nb_rows = (kGateUp ? a.F : a.d) / kTileM;              // 128-row blocks per expert
+  auto stage_a = [&](int s) { return smem + size_t(s) * C::kStageBytes; };
+  auto stage_b = [&](int s) { return smem + size_t(s) * C::kStageBytes + C::kABytes; };
+  // weight tile (accumulator ai, chunk c) of a stage
+  auto a_tile = [&](int s, int ai, int c) {
+    return stage_a(s) + (kGateUp ? (c * 2 + ai) : (ai * kC + c)) * kATileBytes;
   };
-  const int a1_off = kGateUp ? a.F : kTileM;  // rows from A tile 0 to A tile 1: the up rows, or the next block
+  // tiled-layout source of an item's block ai (down) or of its gate/up pairs, first chunk j
+  auto w_src = [&](const Tile& tl, int nb, int ai, int j) {
+    const bool shared = tl.group == a.E;
+    const size_t e = shared ? 0 : size_t(tl.group);
+    const uint8_t* base = shared ? a.wsh : a.w;
+    if (kGateUp) return base + ((e * nb_rows + nb) * KT + j) * 2 * size_t(kATileBytes);
+    return base + ((e * nb_rows + size_t(nb) * kA + ai) * KT + j) * size_t(kATileBytes);
+  };
+  constexpr uint32_t kCopyBytes = kGateUp ? 2 * kC * kATileBytes : kC * kATileBytes;  // per weight copy
+  constexpr int kCopies = kGateUp ? 1 : kA;
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
@@ -162,12 +182,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int budget = kPrefetchBytes;
       for (int item = unit; item < total && budget > 0; item += n_units) {
         const Tile tl = a.tiles[item / nblk];
-        const CUtensorMap* mw = tl.group == a.E ? &map_wsh : &map_w;
-        const int wrow = weight_row(tl, item % nblk);
-        for (int kt = kt_lo; kt < kt_hi && budget > 0; ++kt, budget -= kA * kATileBytes) {
-          tma_prefetch_2d(mw, kt * kKTile, wrow);
-          if (kA == 2) tma_prefetch_2d(mw, kt * kKTile, wrow + a1_off);
-        }
+        for (int ks = ks_lo; ks < ks_hi && budget > 0; ++ks, budget -= kCopies * int(kCopyBytes))
+          for (int ai = 0; ai < kCopies; ++ai) prefetch_l2_bulk(w_src(tl, item % nblk, ai, ks * kC), kCopyBytes);
       }
       pdl_begin();
       const uint64_t pol = policy_evict_first();
@@ -176,10 +192,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int item = unit; item < total && !stop; item += n_units) {
         const Tile tl = a.tiles[item / nblk];
         const int nb = item % nblk;
-        const bool shared = tl.group == a.E;
-        const CUtensorMap* mw = shared ? &map_wsh : &map_w;
-        const int wrow = weight_row(tl, nb);
-        for (int kt = kt_lo; kt < kt_hi; ++kt, ++it) {
+        for (int ks = ks_lo; ks < ks_hi; ++ks, ++it) {
           const int s = it % C::kStages, use = it / C::kStages;
           if (!mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort)) {
             report_timeout_flag(a.status_flags, 11);
@@ -187,9 +200,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&ctl->full[s], C::kStageBytes);
-          tma_load_2d_hint(stage_a(s, 0), mw, kt * kKTile, wrow, &ctl->full[s], pol);
-          if (kA == 2) tma_load_2d_hint(stage_a(s, 1), mw, kt * kKTile, wrow + a1_off, &ctl->full[s], pol);
-          tma_load_2d(stage_b(s), &map_x, kt * kKTile, tl.row0, &ctl->full[s]);
+#pragma unroll
+          for (int ai = 0; ai < kCopies; ++ai)
+            bulk_g2s_stream(stage_a(s) + ai * kCopyBytes, w_src(tl, nb, ai, ks * kC), kCopyBytes, &ctl->full[s], pol);
+          tma_load_3d(stage_b(s), &map_x, 0, tl.row0, ks * kC, &ctl->full[s]);
         }
       }
       // wait for the loads still in flight (bounded, regardless of abort)
@@ -215,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         const uint32_t d0 = tmem + uint32_t(b * C::kColsPerAcc);
-        for (int kt = kt_lo; kt < kt_hi; ++kt, ++it) {
+        for (int ks = ks_lo; ks < ks_hi; ++ks, ++it) {
           const int s = it % C::kStages, use = it / C::kStages;
           if (!mbar_wait(&ctl->full[s], use & 1, &ctl->abort)) {
             report_timeout_flag(a.status_flags, 13);
@@ -223,14 +237,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t da0 = sw128_desc(stage_a(s, 0));
-          const uint64_t da1 = kA == 2 ? sw128_desc(stage_a(s, 1)) : 0;
-          const uint64_t db = sw128_desc(stage_b(s));
 #pragma unroll
-          for (int kk = 0; kk < kKTile / 32; ++kk) {
-            const uint32_t acc = (kt > kt_lo || kk > 0) ? 1u : 0u;
-            tc_mma_f8(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            if (kA == 2) tc_mma_f8(d0 + kN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+          for (int c = 0; c < kC; ++c) {
+            const uint64_t db = sw128_desc(stage_b(s) + c * kN * kKTile);
+            uint64_t da[kA];
+#pragma unroll
+            for (int ai = 0; ai < kA; ++ai) da[ai] = sw128_desc(a_tile(s, ai, c));
+#pragma unroll
+            for (int kk = 0; kk < kKTile / 32; ++kk) {
+              const uint32_t acc = (ks > ks_lo || c > 0 || kk > 0) ? 1u : 0u;
+#pragma unroll
+              for (int ai = 0; ai < kA; ++ai)  // accumulators interleaved
+                tc_mma_f8(d0 + uint32_t(ai * kN), da[ai] + 2 * kk, db + 2 * kk, idesc, acc);
+            }
           }
           tc_commit(&ctl->empty[s]);
         }
@@ -381,11 +400,10 @@ int sm_count() {
   return sms;
 }
 
-template <int kN, bool kGateUp, int kA, int kSplit>
-cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mwsh, const CUtensorMap& mx, const TcArgs& a,
-                      long long max_items, cudaStream_t s) {
-  using C = TcCfg<kN, kGateUp, kA, kSplit>;
-  static cudaError_t attr = cudaFuncSetAttribute(k_expert_tc<kN, kGateUp, kA, kSplit>,
+template <int kN, bool kGateUp, int kA, int kSplit, int kC>
+cudaError_t launch_tc(const CUtensorMap& mx, const TcArgs& a, long long max_items, cudaStream_t s) {
+  using C = TcCfg<kN, kGateUp, kA, kSplit, kC>;
+  static cudaError_t attr = cudaFuncSetAttribute(k_expert_tc<kN, kGateUp, kA, kSplit, kC>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
   if (attr != cudaSuccess) return attr;
   // one CTA (or one CTA pair) per SM
@@ -404,19 +422,36 @@ cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mwsh, const CUte
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = kSplit == 2 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_expert_tc<kN, kGateUp, kA, kSplit>, mw, mwsh, mx, a);
+  return cudaLaunchKernelEx(&cfg, k_expert_tc<kN, kGateUp, kA, kSplit, kC>, mx, a);
 }
 
-template <bool kGateUp, int kA>
-cudaError_t launch_tc_n(int kN, const CUtensorMap& mw, const CUtensorMap& mwsh, const CUtensorMap& mx,
-                        const TcArgs& a, long long max_items, bool split, cudaStream_t s) {
-  switch (kN) {
-    case 16: return split ? launch_tc<16, kGateUp, kA, 2>(mw, mwsh, mx, a, max_items, s)
-                          : launch_tc<16, kGateUp, kA, 1>(mw, mwsh, mx, a, max_items, s);
-    case 32: return launch_tc<32, kGateUp, kA, 1>(mw, mwsh, mx, a, max_items, s);
-    case 64: return launch_tc<64, kGateUp, kA, 1>(mw, mwsh, mx, a, max_items, s);
-    case 128: return launch_tc<128, kGateUp, kA, 1>(mw, mwsh, mx, a, max_items, s);
+// Gate/up: decode tiles (16 or 32 token rows) take two k-chunks per stage (64 KB of weights in
+// one copy); wider tiles one chunk (their activation boxes are larger).
+cudaError_t launch_gateup_n(int kN, int kC, bool split, const CUtensorMap& mx, const TcArgs& a, long long items,
+                            cudaStream_t s) {
+  if (kN == 16 && kC == 2) return split ? launch_tc<16, true, 2, 2, 2>(mx, a, items, s)
+                                        : launch_tc<16, true, 2, 1, 2>(mx, a, items, s);
+  if (kN == 16) return split ? launch_tc<16, true, 2, 2, 1>(mx, a, items, s) : launch_tc<16, true, 2, 1, 1>(mx, a, items, s);
+  if (kN == 32 && kC == 2) return launch_tc<32, true, 2, 1, 2>(mx, a, items, s);
+  if (kN == 32) return launch_tc<32, true, 2, 1, 1>(mx, a, items, s);
+  if (kN == 64) return launch_tc<64, true, 2, 1, 1>(mx, a, items, s);
+  if (kN == 128) return launch_tc<128, true, 2, 1, 1>(mx, a, items, s);
+  return cudaErrorInvalidValue;
+}
+
+// Down: decode tiles take an item's whole k range (ffn = 640: five chunks, 80 KB in one
+// copy) per stage; wider tiles pair two 128-row blocks per stage, one chunk at a time.
+cudaError_t launch_down_n(int kN, int kA, int kC, const CUtensorMap& mx, const TcArgs& a, long long items,
+                          cudaStream_t s) {
+  if (kA == 2) {
+    if (kN == 64) return launch_tc<64, false, 2, 1, 1>(mx, a, items, s);
+    if (kN == 128) return launch_tc<128, false, 2, 1, 1>(mx, a, items, s);
+    return cudaErrorInvalidValue;
   }
+  if (kN == 16) return kC == 5 ? launch_tc<16, false, 1, 1, 5>(mx, a, items, s) : launch_tc<16, false, 1, 1, 1>(mx, a, items, s);
+  if (kN == 32) return kC == 5 ? launch_tc<32, false, 1, 1, 5>(mx, a, items, s) : launch_tc<32, false, 1, 1, 1>(mx, a, items, s);
+  if (kN == 64) return launch_tc<64, false, 1, 1, 1>(mx, a, items, s);
+  if (kN == 128) return launch_tc<128, false, 1, 1, 1>(mx, a, items, s);
   return cudaErrorInvalidValue;
 }
 
@@ -436,6 +471,8 @@ TcArgs tc_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.sh = reinterpret_cast<const float*>(base + ws.sh);
   a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
   a.status_flags = reinterpret_cast<int*>(base + ws.status);
+  a.w = nullptr;
+  a.wsh = nullptr;
   return a;
 }
 
@@ -456,34 +493,37 @@ int tc_rows_per_tile(int T) {
 }
 
 cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  if (!L.tiled) return cudaErrorInvalidValue;
   const int kN = tc_rows_per_tile(T);
-  CUtensorMap mw, mwsh, mx;
-  if (!make_map(&mw, L.wgu, uint64_t(L.E) * 2 * L.F, L.d, kTileM) ||
-      !make_map(&mwsh, L.sh_wgu, uint64_t(2) * L.F, L.d, kTileM) ||
-      !make_map(&mx, base + ws.xq, uint64_t(ws.R_alloc), L.d, kN))
-    return cudaErrorInvalidValue;
+  const int KT = L.d / kKTile;
+  const int kC = (kN <= 32 && KT % 2 == 0) ? 2 : 1;
+  CUtensorMap mx;
+  if (!make_map_chunks(&mx, base + ws.xq, uint64_t(ws.R_alloc), L.d, kN, kC)) return cudaErrorInvalidValue;
+  TcArgs a = tc_args(L, ws, base);
+  a.w = L.wgu;
+  a.wsh = L.sh_wgu;
   const long long items = max_tc_tiles(L, T, kN) * (L.F / kTileM);
   // a handful of tokens touch few experts: fewer items than SMs, so the k-steps of each item
-  // are split over a CTA pair (measured: 28.7 -> 26.6 us for 8 tokens; no gain from 32 tokens up)
+  // are split over a CTA pair
   const bool split = T <= kSplitMaxT;
-  return launch_tc_n<true, 2>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, split, s);
+  return launch_gateup_n(kN, kC, split, mx, a, items, s);
 }
 
 cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
+  if (!L.tiled) return cudaErrorInvalidValue;
   const int kN = tc_rows_per_tile(T);
-  CUtensorMap mw, mwsh, mx;
-  if (!make_map(&mw, L.wd, uint64_t(L.E) * L.d, L.F, kTileM) ||
-      !make_map(&mwsh, L.sh_wd, uint64_t(L.d), L.F, kTileM) ||
-      !make_map(&mx, base + ws.qh, uint64_t(ws.R_alloc), L.F, kN))
-    return cudaErrorInvalidValue;
+  const int KT = L.F / kKTile;
   // two 128-row blocks per item (two accumulators fed from one activation stage) where d allows
   // and the tiles are wide enough for the activation traffic to matter
-  if (L.d % (2 * kTileM) == 0 && kN >= kDownPairMinN) {
-    const long long items = max_tc_tiles(L, T, kN) * (L.d / (2 * kTileM));
-    return launch_tc_n<false, 2>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, false, s);
-  }
-  const long long items = max_tc_tiles(L, T, kN) * (L.d / kTileM);
-  return launch_tc_n<false, 1>(kN, mw, mwsh, mx, tc_args(L, ws, base), items, false, s);
+  const int kA = (L.d % (2 * kTileM) == 0 && kN >= kDownPairMinN) ? 2 : 1;
+  const int kC = (kA == 1 && kN <= 32 && KT == 5) ? 5 : 1;
+  CUtensorMap mx;
+  if (!make_map_chunks(&mx, base + ws.qh, uint64_t(ws.R_alloc), L.F, kN, kC)) return cudaErrorInvalidValue;
+  TcArgs a = tc_args(L, ws, base);
+  a.w = L.wd;
+  a.wsh = L.sh_wd;
+  const long long items = max_tc_tiles(L, T, kN) * (L.d / (kA * kTileM));
+  return launch_down_n(kN, kA, kC, mx, a, items, s);
 }
 
 }  // namespace moe

@@ -86,6 +86,25 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.moe_forward_stack(arr, 0, p, 4, None, 0, ws, 1 << 40, None) == -1
     assert lib.moe_forward_stack(arr, 1, p, 4, None, 0, ws, 16, None) == -3
     assert lib.moe_dispatch(p, 4, 384, 7, p, p, p, p, ws, 1 << 40, None) == -2
+    # weight layouts: an unknown layout, a tiled fp32 layer, a tiled layer with ffn % 128 != 0
+    bad_layout = _layer(binding)
+    bad_layout.w_layout = 5
+    assert fwd(p, 1, 4, ctypes.byref(bad_layout), None, None, None, None, p, 0, 0, ws, 1 << 40, None) == -1
+    tiled_f32 = _layer(binding, wdt=0)
+    tiled_f32.w_layout = binding.LAYOUT_TILED
+    assert fwd(p, 1, 4, ctypes.byref(tiled_f32), None, None, None, None, p, 0, 0, ws, 1 << 40, None) == -1
+    tiled_odd = _layer(binding, F=576)
+    tiled_odd.w_layout = binding.LAYOUT_TILED
+    assert fwd(p, 1, 4, ctypes.byref(tiled_odd), None, None, None, None, p, 0, 0, ws, 1 << 40, None) == -2
+    # packing: needs E4M3 rows with d, ffn multiples of 128, and four aligned destinations
+    pack = lib.moe_pack_weights
+    assert pack(ctypes.byref(_layer(binding, F=576)), p, p, p, p, None) == -2
+    tiled = _layer(binding)
+    tiled.w_layout = binding.LAYOUT_TILED
+    assert pack(ctypes.byref(tiled), p, p, p, p, None) == -1
+    assert pack(ctypes.byref(good), p, None, p, p, None) == -1
+    assert pack(ctypes.byref(good), p, p + 8, p, p, None) == -1
+    assert pack(None, p, p, p, p, None) == -1
 
 
 def test_status_strings(lib):

@@ -29,10 +29,25 @@ def moe():
     return m
 
 
+class KolibriLayers:
+    """The Kolibri-shaped layer's host weights and the device layer in both weight layouts:
+    tiled (tcgen05 expert kernels, the default) and rows (weight-streaming kernels).
+    Unpacks as (weights, tiled layer)."""
+
+    def __init__(self, w, tiled, rows):
+        self.w, self.tiled, self.rows = w, tiled, rows
+
+    def __iter__(self):
+        return iter((self.w, self.tiled))
+
+    def for_path(self, path):
+        return self.rows if path == "stream" else self.tiled
+
+
 @pytest.fixture(scope="module")
 def kolibri(moe):
     w = g.kolibri_layer(g.SEED_DECODE)
-    return w, moe.Layer.from_host(w)
+    return KolibriLayers(w, moe.Layer.from_host(w), moe.Layer.from_host(w, tiled=False))
 
 
 @pytest.fixture(scope="module")
@@ -58,6 +73,57 @@ def test_device_e4m3_encoder_matches_oracle(moe):
     ref0 = np.where(ref == 0x80, 0, ref)
     bad = np.nonzero(got0 != ref0)[0]
     assert bad.size == 0, [(float(v[i]), int(got[i]), int(ref[i])) for i in bad[:10]]
+
+
+def _tiled_reference(rows: np.ndarray, block_rows: int, gate_up: bool, F: int) -> np.ndarray:
+    """The tiled layout as include/libmoe.h states it, built with numpy from the row layout:
+    16 KB tiles of 128 rows x 128 bytes, 16-byte chunk c of row r stored at chunk c ^ (r % 8)."""
+    E, R, K = rows.shape
+    tiles = []
+    for e in range(E):
+        for n in range((F if gate_up else R) // 128):
+            for j in range(K // 128):
+                for half in ((0, 1) if gate_up else (None,)):
+                    r0 = (half * F if gate_up else 0) + n * 128
+                    tile = rows[e, r0:r0 + 128, j * 128:(j + 1) * 128].reshape(128, 8, 16)
+                    out = np.empty_like(tile)
+                    for r in range(128):
+                        out[r, np.arange(8) ^ (r % 8)] = tile[r]
+                    tiles.append(out.reshape(-1))
+    return np.concatenate(tiles)
+
+
+def test_pack_weights_matches_the_documented_tiled_layout(moe):
+    """moe_pack_weights against a numpy construction of the layout the header documents, on
+    a small E4M3 layer (3 experts, d = 384, ffn = 256), byte for byte."""
+    w = g.make_layer(41, 384, 256, 8, fp8=True, bias_var=None)
+    rows = moe.Layer.from_host(w, tiled=False)
+    tiled = rows.tiled()
+    torch.cuda.synchronize()
+    E, d, F = 8, 384, 256
+    got = tiled.tensors["w_gate_up"].cpu().numpy().reshape(-1)
+    want = _tiled_reference(w.Wgu.reshape(E, 2 * F, d), 128, True, F)
+    assert np.array_equal(got, want)
+    got = tiled.tensors["w_down"].cpu().numpy().reshape(-1)
+    assert np.array_equal(got, _tiled_reference(w.Wd.reshape(E, d, F), 128, False, F))
+    got = tiled.tensors["sh_gate_up"].cpu().numpy().reshape(-1)
+    assert np.array_equal(got, _tiled_reference(w.sh_Wgu.reshape(1, 2 * F, d), 128, True, F))
+    got = tiled.tensors["sh_down"].cpu().numpy().reshape(-1)
+    assert np.array_equal(got, _tiled_reference(w.sh_Wd.reshape(1, d, F), 128, False, F))
+
+
+def test_layouts_and_paths(moe, kolibri):
+    """The tiled layer runs on the tcgen05 kernels (AUTO and TC), the row layer on the
+    streaming kernels (AUTO and STREAM); asking for the other path is MOE_ERR_UNSUPPORTED."""
+    x = to_dev_x(g.make_x(g.SEED_DECODE, 8, 2048, bf16=True))
+    ws = moe.workspace(kolibri.tiled, 8)
+    y_t, _, _ = moe.forward(x, kolibri.tiled, ws)
+    y_r, _, _ = moe.forward(x, kolibri.rows, ws)
+    assert torch.isfinite(y_t).all() and torch.isfinite(y_r).all()
+    for L, flags in ((kolibri.tiled, 1), (kolibri.rows, 2)):
+        with pytest.raises(moe.binding.MoeError) as err:
+            moe.forward(x, L, ws, flags=flags)
+        assert err.value.status == -2
 
 
 # ------------------------------------------------------------------------ router ---------
@@ -185,7 +251,7 @@ def test_tiny_fp32_layer_free_then_forced(moe, tiny):
 @pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("T", [1, 8, 64])
 def test_decode_layer(moe, kolibri, T, path):
-    w, L = kolibri
+    w, L = kolibri.w, kolibri.for_path(path)
     x = g.make_x(g.SEED_DECODE, T, w.d, bf16=True)
     ws = moe.workspace(L, T)
     y, ids, wt = moe.forward(to_dev_x(x), L, ws, flags=PATHS[path])
@@ -198,7 +264,7 @@ def test_decode_layer(moe, kolibri, T, path):
 
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_prefill_2048_free_then_4x512_forced(moe, kolibri, path):
-    w, L = kolibri
+    w, L = kolibri.w, kolibri.for_path(path)
     T = 2048
     x = g.make_x(g.SEED_PREFILL, T, w.d, bf16=True)
     ws = moe.workspace(L, T)
@@ -218,7 +284,7 @@ def test_prefill_2048_free_then_4x512_forced(moe, kolibri, path):
 
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_batched_decode_zipf_forced(moe, kolibri, path):
-    w, L = kolibri
+    w, L = kolibri.w, kolibri.for_path(path)
     T = 128
     x = g.make_x(g.SEED_ZIPF, T, w.d, bf16=True)
     fid = g.zipf_ids(g.SEED_ZIPF, 0, T, 384, 6, 1.1)
@@ -234,7 +300,7 @@ def test_batched_decode_zipf_forced(moe, kolibri, path):
 @pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("T", [0, 37, 333, 1500])
 def test_ragged_token_counts(moe, kolibri, T, path):
-    w, L = kolibri
+    w, L = kolibri.w, kolibri.for_path(path)
     x = g.make_x(77, max(T, 1), w.d, bf16=True)[:T]
     ws = moe.workspace(L, max(T, 1))
     y, ids, wt = moe.forward(to_dev_x(x), L, ws, flags=PATHS[path])
