@@ -50,6 +50,7 @@ constexpr int kPrefetchBytes = 256 * 1024;  // weights a CTA pulls into L2 befor
 constexpr int kMaxStages = 8;
 constexpr int kDownPairMinN = 64;
 constexpr int kSplitMaxT = 16;  // gate/up k-steps split over a CTA pair up to this many tokens
+constexpr int kGateUpPairChunkMaxN = 32;  // gate/up stages of two k-chunks up to this tile width
 
 struct TcArgs {
   int d, F, E;
@@ -434,8 +435,8 @@ cudaError_t launch_gateup_n(int kN, int kC, bool split, const CUtensorMap& mx, c
   if (kN == 16) return split ? launch_tc<16, true, 2, 2, 1>(mx, a, items, s) : launch_tc<16, true, 2, 1, 1>(mx, a, items, s);
   if (kN == 32 && kC == 2) return launch_tc<32, true, 2, 1, 2>(mx, a, items, s);
   if (kN == 32) return launch_tc<32, true, 2, 1, 1>(mx, a, items, s);
-  if (kN == 64) return launch_tc<64, true, 2, 1, 1>(mx, a, items, s);
-  if (kN == 128) return launch_tc<128, true, 2, 1, 1>(mx, a, items, s);
+  if (kN == 64) return kC == 2 ? launch_tc<64, true, 2, 1, 2>(mx, a, items, s) : launch_tc<64, true, 2, 1, 1>(mx, a, items, s);
+  if (kN == 128) return kC == 2 ? launch_tc<128, true, 2, 1, 2>(mx, a, items, s) : launch_tc<128, true, 2, 1, 1>(mx, a, items, s);
   return cudaErrorInvalidValue;
 }
 
@@ -496,7 +497,7 @@ cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char*
   if (!L.tiled) return cudaErrorInvalidValue;
   const int kN = tc_rows_per_tile(T);
   const int KT = L.d / kKTile;
-  const int kC = (kN <= 32 && KT % 2 == 0) ? 2 : 1;
+  const int kC = (kN <= kGateUpPairChunkMaxN && KT % 2 == 0) ? 2 : 1;
   CUtensorMap mx;
   if (!make_map_chunks(&mx, base + ws.xq, uint64_t(ws.R_alloc), L.d, kN, kC)) return cudaErrorInvalidValue;
   TcArgs a = tc_args(L, ws, base);
