@@ -116,7 +116,13 @@ enum {
   OR_MUT_SWAP_GATE_UP = 7,     // silu applied to the up projection instead of the gate
   OR_MUT_SCALE_AXIS = 8,       // weight scale of the neighbouring output row
   OR_MUT_DISPATCH_SHIFT = 9,   // dispatch: each routed group's offset shifted by one row
+  OR_MUT_BIASED_WEIGHTS = 10,  // selection-only bias mode, but the weights use the biased score too
 };
+
+// How the per-expert bias enters: OR_BIAS_SCORE adds it to the logits (selection and weights);
+// OR_BIAS_SELECT adds it to the selection score only, the weights being the renormalised
+// softmax of the unbiased logits.
+enum { OR_BIAS_SCORE = 0, OR_BIAS_SELECT = 1 };
 
 enum { OR_ACT_W8A8 = 0, OR_ACT_W8A16 = 1 };
 
@@ -135,6 +141,7 @@ typedef struct {
   const float* sh_sgu;     // [2, ffn]
   const void* sh_Wd;       // [d, ffn]
   const float* sh_sd;      // [d]
+  int bias_mode;           // OR_BIAS_SCORE (default) or OR_BIAS_SELECT
 } oracle_layer;
 
 float oracle_e4m3_decode(uint8_t c) { return kDec.v[c]; }
@@ -148,7 +155,8 @@ void oracle_bf16_rne_n(const float* v, int64_t n, uint16_t* out) {
 }
 
 // ------------------------------------------------------------------- router ---------------
-// [P2-gate], [P2-1]: logits[e] = (sum_k x[k] * Wr[e,k]) + b[e], in fp32.
+// [P2-gate], [P2-1]: logits[e] = (sum_k x[k] * Wr[e,k]) + b[e], in fp32 (without b in the
+// selection-only bias mode: there the bias enters the selection score alone).
 void oracle_router_logits(const oracle_layer* L, const float* xf, float* logits) {
   for (int e = 0; e < L->E; ++e) {
     const float* w = L->Wr + size_t(e) * L->d;
@@ -158,7 +166,7 @@ void oracle_router_logits(const oracle_layer* L, const float* xf, float* logits)
     } else {
       for (int k = 0; k < L->d; ++k) acc += xf[k] * w[k];
     }
-    float b = L->bias ? L->bias[e] : 0.0f;
+    float b = (L->bias && L->bias_mode == OR_BIAS_SCORE) ? L->bias[e] : 0.0f;
     logits[e] = (L->mutant == OR_MUT_UNBIASED_SELECT) ? acc : acc + b;
     if (L->mutant == OR_MUT_BF16_ROUTER) logits[e] = bf16_to_f32(f32_to_bf16(logits[e]));
   }
@@ -284,6 +292,8 @@ void oracle_expert(const oracle_layer* L, int e, const float* xf, float* ye) {
 // ---------------------------------------------------------------- one token ---------------
 // Routing of one token.  forced_ids (k ids, in the order given) replaces the selection
 // [P1-gate]; forced_w (k weights, used as given) replaces the renormalised softmax.
+// logits_out: the router logits (unbiased in the selection-only mode); p_out: the
+// probabilities the selection ranks (softmax of logits + bias in that mode).
 // Returns 0, or -4 when a forced id is out of range or repeated.
 int oracle_route_token(const oracle_layer* L, const float* xf, const int32_t* forced_ids,
                        const float* forced_w, int32_t* ids, float* w, float* logits_out, float* p_out) {
@@ -304,6 +314,19 @@ int oracle_route_token(const oracle_layer* L, const float* xf, const int32_t* fo
       oracle_topk(p.data(), E, k, OR_MUT_NONE, ids);
       p.swap(pb);
       logits.swap(lb);
+    } else if (L->bias_mode == OR_BIAS_SELECT && L->bias) {
+      // select on softmax(logits + b); weights from softmax(logits) unless the planted bug
+      std::vector<float> lb(static_cast<size_t>(E)), pb(static_cast<size_t>(E));
+      for (int e = 0; e < E; ++e) lb[size_t(e)] = logits[size_t(e)] + L->bias[e];
+      oracle_softmax(lb.data(), E, pb.data());
+      oracle_topk(pb.data(), E, k, L->mutant, ids);
+      for (int i = 0; i < k; ++i) if (ids[i] < 0 || ids[i] >= E) return -4;
+      oracle_renorm(L->mutant == OR_MUT_BIASED_WEIGHTS ? pb.data() : p.data(), ids, k, L->mutant, w);
+      if (logits_out) for (int e = 0; e < E; ++e) logits_out[e] = logits[size_t(e)];
+      if (p_out) for (int e = 0; e < E; ++e) p_out[e] = pb[size_t(e)];
+      for (int i = 0; i < k; ++i)
+        for (int j = 0; j < i; ++j) if (ids[j] == ids[i]) return -4;
+      return 0;
     } else {
       oracle_topk(p.data(), E, k, L->mutant, ids);
     }

@@ -17,14 +17,16 @@ _SRC = os.path.join(_HERE, "oracle.cpp")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 MUT_NONE, MUT_BF16_ROUTER, MUT_UNBIASED_SELECT, MUT_HIGH_INDEX_TIE, MUT_NO_RENORM, MUT_NO_SHARED, \
-    MUT_SORTED_SUM, MUT_SWAP_GATE_UP, MUT_SCALE_AXIS, MUT_DISPATCH_SHIFT = range(10)
+    MUT_SORTED_SUM, MUT_SWAP_GATE_UP, MUT_SCALE_AXIS, MUT_DISPATCH_SHIFT, MUT_BIASED_WEIGHTS = range(11)
 MUTANTS = {
     "bf16_router": MUT_BF16_ROUTER, "unbiased_select": MUT_UNBIASED_SELECT,
     "high_index_tie": MUT_HIGH_INDEX_TIE, "no_renorm": MUT_NO_RENORM, "no_shared": MUT_NO_SHARED,
     "sorted_sum": MUT_SORTED_SUM, "swap_gate_up": MUT_SWAP_GATE_UP, "scale_axis": MUT_SCALE_AXIS,
-    "dispatch_shift": MUT_DISPATCH_SHIFT,
+    "dispatch_shift": MUT_DISPATCH_SHIFT, "biased_weights": MUT_BIASED_WEIGHTS,
 }
 ACT_W8A8, ACT_W8A16 = 0, 1
+# the per-expert bias: added to the logits (selection and weights), or to the selection only
+BIAS_SCORE, BIAS_SELECT = 0, 1
 
 
 class OracleLayer(ctypes.Structure):
@@ -34,7 +36,7 @@ class OracleLayer(ctypes.Structure):
                 ("Wgu", ctypes.c_void_p), ("sgu", ctypes.c_void_p),
                 ("Wd", ctypes.c_void_p), ("sd", ctypes.c_void_p),
                 ("sh_Wgu", ctypes.c_void_p), ("sh_sgu", ctypes.c_void_p),
-                ("sh_Wd", ctypes.c_void_p), ("sh_sd", ctypes.c_void_p)]
+                ("sh_Wd", ctypes.c_void_p), ("sh_sd", ctypes.c_void_p), ("bias_mode", ctypes.c_int)]
 
 
 _lib = None
@@ -93,12 +95,13 @@ def _p(a: Optional[np.ndarray]):
 class Layer:
     """Binds a gen.moegen.LayerWeights (host numpy arrays) to the oracle's C struct."""
 
-    def __init__(self, w, k: int = 6, act_mode: int = ACT_W8A8, mutant: int = MUT_NONE):
+    def __init__(self, w, k: int = 6, act_mode: int = ACT_W8A8, mutant: int = MUT_NONE,
+                 bias_mode: int = BIAS_SCORE):
         self.w = w
         self.k = k
         self.s = OracleLayer(w.d, w.ffn, w.E, k, 1 if w.fp8 else 0, act_mode, mutant,
                              _p(w.Wr), _p(w.bias), _p(w.Wgu), _p(w.sgu), _p(w.Wd), _p(w.sd),
-                             _p(w.sh_Wgu), _p(w.sh_sgu), _p(w.sh_Wd), _p(w.sh_sd))
+                             _p(w.sh_Wgu), _p(w.sh_sgu), _p(w.sh_Wd), _p(w.sh_sd), bias_mode)
 
     @property
     def ptr(self):

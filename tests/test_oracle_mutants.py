@@ -71,8 +71,18 @@ def test_clean_oracle_passes_the_suite(data):
     assert suite(w, x, o.Layer(w), o.Layer(w)) == []
 
 
+# a mistake that only exists in one bias mode is planted in that mode (both layers)
+MUTANT_BIAS_MODE = {"biased_weights": o.BIAS_SELECT}
+
+
 @pytest.mark.parametrize("name", sorted(o.MUTANTS))
 def test_each_planted_mistake_is_caught(data, name):
     w, x = data
-    fails = suite(w, x, o.Layer(w, mutant=o.MUTANTS[name]), o.Layer(w))
+    bm = MUTANT_BIAS_MODE.get(name, o.BIAS_SCORE)
+    fails = suite(w, x, o.Layer(w, mutant=o.MUTANTS[name], bias_mode=bm), o.Layer(w, bias_mode=bm))
     assert fails, f"mutant {name} passed every check"
+
+
+def test_clean_oracle_passes_the_suite_in_the_selection_only_bias_mode(data):
+    w, x = data
+    assert suite(w, x, o.Layer(w, bias_mode=o.BIAS_SELECT), o.Layer(w, bias_mode=o.BIAS_SELECT)) == []

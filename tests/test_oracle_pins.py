@@ -208,6 +208,41 @@ def test_forced_equals_free_bit_exact(tiny):
     assert np.array_equal(forced["y"].view(np.uint32), free["y"].view(np.uint32))
 
 
+def test_selection_only_bias_against_float64_definition():
+    """Selection-only bias mode (the per-expert bias ranks the experts, the weights come from
+    the unbiased softmax), against float64 numpy: logits = x Wr^T without the bias; ids = the
+    six largest logits + b (lowest index first on ties); w = softmax of the unbiased logits
+    over those six.  A large bias on one expert forces it into every token's set while its
+    weight stays what its own logit gives."""
+    w = g.make_layer(51, 256, 128, 384, fp8=True, bias_var=0.5)
+    w.bias[7] = 50.0  # expert 7 always selected, first
+    x = g.make_x(52, 24, 256, bf16=True)
+    xf = g.bf16_bits_to_f32(x).astype(np.float64)
+    L = o.Layer(w, bias_mode=o.BIAS_SELECT)
+    out = o.layer_forward(L, x, want_probs=True)
+    raw = xf @ w.Wr.astype(np.float64).T
+    for t in range(x.shape[0]):
+        assert np.max(np.abs(out["logits"][t] - raw[t])) < 1e-5 * np.max(np.abs(raw[t]))
+        score = raw[t] + w.bias.astype(np.float64)
+        order = np.lexsort((np.arange(384), -score))[:6]
+        assert np.array_equal(out["ids"][t], order)
+        assert out["ids"][t][0] == 7
+        e = np.exp(raw[t][order] - raw[t][order].max())
+        np.testing.assert_allclose(out["w"][t], e / e.sum(), rtol=2e-6, atol=1e-7)
+    # the same ids under the score mode carry different weights (the bias changes them there)
+    s_out = o.layer_forward(o.Layer(w), x, forced_ids=out["ids"])
+    assert not np.allclose(s_out["w"], out["w"], atol=1e-3)
+
+
+def test_selection_only_bias_with_zero_bias_equals_score_mode():
+    w = g.make_layer(53, 256, 128, 384, fp8=True, bias_var=None)
+    x = g.make_x(54, 16, 256, bf16=True)
+    a = o.layer_forward(o.Layer(w, bias_mode=o.BIAS_SELECT), x)
+    b = o.layer_forward(o.Layer(w), x)
+    for key in ("ids", "w", "y"):
+        assert np.array_equal(a[key].view(np.uint32), b[key].view(np.uint32))
+
+
 def test_combine_is_in_slot_order(tiny):
     """y is bit-identical to y_shared + w_0 y_0 + ... + w_5 y_5 accumulated left to right in
     fp32 (numpy float32 ops, no fused multiply-add), from the oracle's own expert outputs."""
