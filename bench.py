@@ -209,8 +209,7 @@ def run_ours(args):
     base = moe.Layer.from_host(w, tiled=(args.path != "stream"))
     layers = [base]
     for _ in range(args.copies - 1):  # copies at other addresses: same values, no L2 reuse between steps
-        layers.append(moe.Layer(**{k: (v.clone() if v is not None else None) for k, v in base.tensors.items()},
-                                layout=base.layout))
+        layers.append(base.clone())
     T = args.tokens
     x_host = g.make_x(g.SEED_DECODE, T, D, bf16=True)
     x = torch.from_numpy(x_host.view(np.int16).copy()).cuda().view(torch.bfloat16)

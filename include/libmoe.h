@@ -75,6 +75,13 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
  * contiguous copy of 32-80 KB); the weight-streaming kernels read the row layout. */
 typedef enum { MOE_LAYOUT_ROWS = 0, MOE_LAYOUT_TILED = 1 } moe_layout;
 
+/* How router_bias enters the routing (page "We Ported Aleph Alpha's Kolibri to a MacBook.
+ * Our Own Gate Said No.", section 1: "router score plus a per-expert selection bias").
+ *   MOE_BIAS_SCORE   logits = x Wr^T + b: the bias shifts both the selection and the weights.
+ *   MOE_BIAS_SELECT  logits = x Wr^T: the experts are ranked on logits + b, and the weights are
+ *                    the softmax of the unbiased logits renormalised over the selected six. */
+typedef enum { MOE_BIAS_SCORE = 0, MOE_BIAS_SELECT = 1 } moe_bias_mode;
+
 /* One layer: borrowed device pointers.  Shapes with d = d_model, F = ffn, E = n_experts.
  *   w_router     [E, d]  fp32            router_bias [E] fp32 or NULL
  *   w_gate_up    [E, 2, F, d]            gate rows (index 0) then up rows (index 1)
@@ -97,6 +104,7 @@ typedef struct {
   const void* sh_down;
   const float* sh_s_down;
   moe_layout w_layout; /* order of the four E4M3 weight tensors (MOE_LAYOUT_ROWS for fp32) */
+  moe_bias_mode bias_mode; /* MOE_BIAS_SCORE (a zero-initialised struct) or MOE_BIAS_SELECT */
 } moe_layer;
 
 /* Flags for moe_forward / moe_forward_stack: which expert kernels run.  0 = automatic: the
@@ -126,7 +134,8 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
  *   k           must equal layer->top_k (6)
  *   ids_out     [T, k] int32: selected experts, descending probability, lowest index on ties
  *   w_out       [T, k] fp32: renormalised softmax weights of the selected experts
- *   logits_out  [T, E] fp32 router logits (bias included), or NULL */
+ *   logits_out  [T, E] fp32 router logits (bias included under MOE_BIAS_SCORE, not under
+ *               MOE_BIAS_SELECT), or NULL */
 moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, int k,
                      int32_t* ids_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes,
                      moe_stream_t stream);

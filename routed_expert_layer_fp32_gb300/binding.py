@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 LAYOUT_ROWS, LAYOUT_TILED = 0, 1
+BIAS_SCORE, BIAS_SELECT = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC = 0, 1, 2
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
           -4: "MOE_ERR_BAD_FORCED_ID", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_CUDA"}
@@ -43,7 +44,8 @@ class MoeLayerC(ctypes.Structure):
                 ("w_gate_up", ctypes.c_void_p), ("s_gate_up", ctypes.c_void_p),
                 ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
                 ("sh_gate_up", ctypes.c_void_p), ("sh_s_gate_up", ctypes.c_void_p),
-                ("sh_down", ctypes.c_void_p), ("sh_s_down", ctypes.c_void_p), ("w_layout", ctypes.c_int)]
+                ("sh_down", ctypes.c_void_p), ("sh_s_down", ctypes.c_void_p), ("w_layout", ctypes.c_int),
+                ("bias_mode", ctypes.c_int)]
 
 
 _lib = None
@@ -121,11 +123,12 @@ class Layer:
 
     FP8 layers take uint8 E4M3 codes (or torch.float8_e4m3fn tensors) and fp32 scales; the
     four weight tensors keep their shapes ([E,2,F,d], [E,d,F], [2,F,d], [d,F]) in either byte
-    order (`layout`: LAYOUT_ROWS, or LAYOUT_TILED as written by moe_pack_weights)."""
+    order (`layout`: LAYOUT_ROWS, or LAYOUT_TILED as written by moe_pack_weights).
+    `bias_mode`: BIAS_SCORE (the bias is added to the logits) or BIAS_SELECT (it only ranks)."""
 
     def __init__(self, w_router, router_bias, w_gate_up, w_down, sh_gate_up, sh_down,
                  s_gate_up=None, s_down=None, sh_s_gate_up=None, sh_s_down=None, top_k: int = 6,
-                 layout: int = LAYOUT_ROWS):
+                 layout: int = LAYOUT_ROWS, bias_mode: int = BIAS_SCORE):
         self.tensors = dict(w_router=w_router, router_bias=router_bias, w_gate_up=w_gate_up, w_down=w_down,
                             sh_gate_up=sh_gate_up, sh_down=sh_down, s_gate_up=s_gate_up, s_down=s_down,
                             sh_s_gate_up=sh_s_gate_up, sh_s_down=sh_s_down)
@@ -133,10 +136,11 @@ class Layer:
         assert two == 2
         fp8 = w_gate_up.dtype in (torch.uint8, torch.float8_e4m3fn)
         self.d, self.F, self.E, self.k, self.fp8, self.layout = d, F, E, top_k, fp8, layout
+        self.bias_mode = bias_mode
         self.c = MoeLayerC(d, F, E, top_k, MOE_E4M3 if fp8 else MOE_F32,
                            _ptr(w_router), _ptr(router_bias), _ptr(w_gate_up), _ptr(s_gate_up), _ptr(w_down),
                            _ptr(s_down), _ptr(sh_gate_up), _ptr(sh_s_gate_up), _ptr(sh_down), _ptr(sh_s_down),
-                           layout)
+                           layout, bias_mode)
 
     def tiled(self) -> "Layer":
         """The same layer with its E4M3 weights rewritten in the tiled layout (moe_pack_weights)."""
@@ -145,17 +149,22 @@ class Layer:
         out = {k: torch.empty_like(t[k]) for k in ("w_gate_up", "w_down", "sh_gate_up", "sh_down")}
         _check(lib().moe_pack_weights(self.ref, _ptr(out["w_gate_up"]), _ptr(out["w_down"]), _ptr(out["sh_gate_up"]),
                                       _ptr(out["sh_down"]), _stream()), "moe_pack_weights")
-        return Layer(**{**t, **out}, top_k=self.k, layout=LAYOUT_TILED)
+        return Layer(**{**t, **out}, top_k=self.k, layout=LAYOUT_TILED, bias_mode=self.bias_mode)
+
+    def clone(self) -> "Layer":
+        """A copy at other device addresses (same values, layout and bias mode)."""
+        return Layer(**{k: (v.clone() if v is not None else None) for k, v in self.tensors.items()}, top_k=self.k,
+                     layout=self.layout, bias_mode=self.bias_mode)
 
     @classmethod
-    def from_host(cls, w, device="cuda", top_k: int = 6, tiled: Optional[bool] = None):
+    def from_host(cls, w, device="cuda", top_k: int = 6, tiled: Optional[bool] = None, bias_mode: int = BIAS_SCORE):
         """From a gen.moegen.LayerWeights-like object of numpy arrays.  tiled=None: the tiled
         layout (tensor-core expert kernels) whenever the weights are E4M3 with d_model and ffn
         multiples of 128; the row layout (weight-streaming kernels) otherwise."""
         def dev(a):
             return None if a is None else torch.from_numpy(a).to(device)
         rows = cls(dev(w.Wr), dev(w.bias), dev(w.Wgu), dev(w.Wd), dev(w.sh_Wgu), dev(w.sh_Wd),
-                   dev(w.sgu), dev(w.sd), dev(w.sh_sgu), dev(w.sh_sd), top_k=top_k)
+                   dev(w.sgu), dev(w.sd), dev(w.sh_sgu), dev(w.sh_sd), top_k=top_k, bias_mode=bias_mode)
         if tiled is None:
             tiled = rows.fp8 and rows.d % 128 == 0 and rows.F % 128 == 0
         if not tiled:

@@ -30,6 +30,7 @@ moe_status check_layer(const moe_layer* L) {
       !aligned16(L->sh_down))
     return MOE_ERR_INVALID_ARG;
   if (L->w_layout != MOE_LAYOUT_ROWS && L->w_layout != MOE_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
+  if (L->bias_mode != MOE_BIAS_SCORE && L->bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
   if (L->w_dtype == MOE_E4M3) {
     if (!L->s_gate_up || !L->s_down || !L->sh_s_gate_up || !L->sh_s_down) return MOE_ERR_INVALID_ARG;
     if (L->w_layout == MOE_LAYOUT_TILED ? !(L->d_model % 128 == 0 && L->ffn % 128 == 0) : !stream_ok(*L))
@@ -51,6 +52,7 @@ LayerDev to_dev(const moe_layer* L) {
   d.k = L->top_k;
   d.fp8 = L->w_dtype == MOE_E4M3;
   d.tiled = L->w_layout == MOE_LAYOUT_TILED;
+  d.bias_sel = L->bias_mode == MOE_BIAS_SELECT && L->router_bias != nullptr;
   d.Wr = L->w_router;
   d.bias = L->router_bias;
   d.wgu = static_cast<const uint8_t*>(L->w_gate_up);

@@ -189,7 +189,11 @@ namespace moe {
 struct LayerDev {
   int d, F, E, k;
   bool fp8;
-  bool tiled;  // E4M3 weights in the tiled layout (MOE_LAYOUT_TILED)
+  bool tiled;     // E4M3 weights in the tiled layout (MOE_LAYOUT_TILED)
+  bool bias_sel;  // MOE_BIAS_SELECT: the bias ranks the experts but stays out of the logits
+  // the bias added to the logits the routers write, and the one the selection adds on top
+  const float* logit_bias() const { return bias_sel ? nullptr : bias; }
+  const float* sel_bias() const { return bias_sel ? bias : nullptr; }
   const float* Wr;
   const float* bias;
   const uint8_t* wgu;

@@ -80,6 +80,7 @@ extern "C" moe_status moe_route_noalloc(const void* x, moe_dtype x_dtype, int T,
   L.fp8 = layer->w_dtype == MOE_E4M3;
   L.Wr = layer->w_router;
   L.bias = layer->router_bias;
+  L.bias_sel = layer->bias_mode == MOE_BIAS_SELECT && layer->router_bias != nullptr;
 
   if (cudaMemsetAsync(st, 0, kNoAllocStatusBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_router_logits(x, x_dtype == MOE_BF16, T, L, logits, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -34,7 +34,8 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
 }
 
 // Free selection of one token by one warp, written out with its weights.  Lane l holds the keys
-// of experts l + 32 j (j < kPer).  Each of the kTopK rounds takes the warp's largest key (one
+// of experts l + 32 j (j < kPer).  With sel_bias (the selection-only bias mode) the keys rank
+// logit + bias while the weights use the logits alone.  Each of the kTopK rounds takes the warp's largest key (one
 // warp reduction), then the lowest expert index holding it (a second reduction), and the lane
 // owning that expert drops it: the same experts in the same order as kTopK rounds of "larger
 // logit, or equal logit and lower index" over all E logits (softmax is monotone in the logit,
@@ -45,14 +46,22 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
 // (made visible by a fence and a ticket) are seen.
 template <int kPer>
 __device__ __forceinline__ void select_write_free_t(const float* row, int E, int lane, int32_t* ids_row,
-                                                    float* w_row) {
+                                                    float* w_row, const float* sel_bias) {
   // every load unconditional and in bounds (a clamped index), so all are in flight at once
   float raw[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) raw[j] = __ldcg(row + min(lane + 32 * j, E - 1));
   uint32_t key[kPer];
+  if (sel_bias) {
+    float b[kPer];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) key[j] = lane + 32 * j < E ? logit_key(raw[j]) : 0u;
+    for (int j = 0; j < kPer; ++j) b[j] = __ldg(sel_bias + min(lane + 32 * j, E - 1));
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) key[j] = lane + 32 * j < E ? logit_key(raw[j] + b[j]) : 0u;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) key[j] = lane + 32 * j < E ? logit_key(raw[j]) : 0u;
+  }
   uint32_t best = 0u;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) best = max(best, key[j]);
@@ -75,9 +84,22 @@ __device__ __forceinline__ void select_write_free_t(const float* row, int E, int
       }
     }
     sel[r] = M != 0u ? int(I) : -1;
-    val[r] = M != 0u ? key_logit(M) : 0.0f;
+    if (sel_bias) {  // the weight needs the winner's own logit: its lane hands it over
+      float mine = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (j == int(I >> 5)) mine = raw[j];
+      const float v = __shfl_sync(0xffffffffu, mine, int(I & 31u));
+      val[r] = M != 0u ? v : 0.0f;
+    } else {
+      val[r] = M != 0u ? key_logit(M) : 0.0f;
+    }
   }
-  const float m = val[0];
+  // the largest selected logit (slot 0 unless the bias reordered them)
+  float m = val[0];
+#pragma unroll
+  for (int r = 1; r < kTopK; ++r)
+    if (sel[r] >= 0) m = fmaxf(m, val[r]);
   float ex[kTopK], s = 0.0f;
 #pragma unroll
   for (int r = 0; r < kTopK; ++r) {
@@ -93,12 +115,13 @@ __device__ __forceinline__ void select_write_free_t(const float* row, int E, int
   }
 }
 
-__device__ __forceinline__ void select_write_free(const float* row, int E, int lane, int32_t* ids_row, float* w_row) {
-  if (E <= 128) select_write_free_t<4>(row, E, lane, ids_row, w_row);
-  else if (E <= 256) select_write_free_t<8>(row, E, lane, ids_row, w_row);
-  else if (E <= 384) select_write_free_t<12>(row, E, lane, ids_row, w_row);
-  else if (E <= 512) select_write_free_t<16>(row, E, lane, ids_row, w_row);
-  else select_write_free_t<kMaxExperts / 32>(row, E, lane, ids_row, w_row);
+__device__ __forceinline__ void select_write_free(const float* row, int E, int lane, int32_t* ids_row, float* w_row,
+                                                  const float* sel_bias) {
+  if (E <= 128) select_write_free_t<4>(row, E, lane, ids_row, w_row, sel_bias);
+  else if (E <= 256) select_write_free_t<8>(row, E, lane, ids_row, w_row, sel_bias);
+  else if (E <= 384) select_write_free_t<12>(row, E, lane, ids_row, w_row, sel_bias);
+  else if (E <= 512) select_write_free_t<16>(row, E, lane, ids_row, w_row, sel_bias);
+  else select_write_free_t<kMaxExperts / 32>(row, E, lane, ids_row, w_row, sel_bias);
 }
 
 // Weights of a forced selection: softmax over the valid selected logits (max subtracted, summed
@@ -231,8 +254,9 @@ constexpr int kRdE = 16, kRdK = 256, kRdT = 64, kRdThreads = 256;
 // them (every expert group's logits for those tokens are written by then) picks top-k and
 // weights for those tokens, a warp per token, as k_select does, and resets the ticket.
 __device__ __forceinline__ void decode_router_tail(const float* part, int Tb, int E, const float* __restrict__ bias,
-                                                   float* logits, int k, int32_t* __restrict__ ids,
-                                                   float* __restrict__ wts, int* tickets, int* last_flag) {
+                                                   const float* sel_bias, float* logits, int k,
+                                                   int32_t* __restrict__ ids, float* __restrict__ wts, int* tickets,
+                                                   int* last_flag) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x;
@@ -271,7 +295,7 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int Tb, in
       const int warp = tid >> 5, lane = tid & 31;
       for (int t = t_lo + warp; t < t_hi; t += kRdThreads / 32) {
         const size_t row = size_t(t_base + t);
-        select_write_free(logits + row * E, E, lane, ids + row * k, wts + row * k);
+        select_write_free(logits + row * E, E, lane, ids + row * k, wts + row * k, sel_bias);
       }
     }
   }
@@ -284,9 +308,10 @@ constexpr int kRdLd = kRdK + 4;
 constexpr size_t kRdSmemF32 = size_t(kRdE + kRdT) * kRdLd * 4 + size_t(kRdT) * kRdE * 4 + 16;
 __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float* __restrict__ x, int T, int d, int E,
                                                                   const float* __restrict__ Wr,
-                                                                  const float* __restrict__ bias, float* logits,
-                                                                  int k, int32_t* __restrict__ ids,
-                                                                  float* __restrict__ wts, int* tickets) {
+                                                                  const float* __restrict__ bias,
+                                                                  const float* sel_bias, float* logits, int k,
+                                                                  int32_t* __restrict__ ids, float* __restrict__ wts,
+                                                                  int* tickets) {
   extern __shared__ __align__(16) uint8_t rd_smem[];
   float* ws = reinterpret_cast<float*>(rd_smem);  // [kRdE][kRdLd]
   float* xs = ws + kRdE * kRdLd;                   // [kRdT][kRdLd]
@@ -348,7 +373,7 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float
     part[(2 * tg + 1) * kRdE + eg] = acc[1][0];
     part[(2 * tg + 1) * kRdE + eg + 8] = acc[1][1];
   }
-  decode_router_tail(part, Tb, E, bias, logits, k, ids, wts, tickets, last_flag);
+  decode_router_tail(part, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, last_flag);
 }
 
 // bf16 x: tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).  Wr rows are split on
@@ -396,9 +421,10 @@ __device__ __forceinline__ void split3(float2 v, uint32_t& hi, uint32_t& mid, ui
 
 __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv_bfloat16* __restrict__ x, int T, int d,
                                                                    int E, const float* __restrict__ Wr,
-                                                                   const float* __restrict__ bias, float* logits,
-                                                                   int k, int32_t* __restrict__ ids,
-                                                                   float* __restrict__ wts, int* tickets) {
+                                                                   const float* __restrict__ bias,
+                                                                   const float* sel_bias, float* logits, int k,
+                                                                   int32_t* __restrict__ ids, float* __restrict__ wts,
+                                                                   int* tickets) {
   extern __shared__ __align__(16) uint8_t rd_smem[];
   float* ws = reinterpret_cast<float*>(rd_smem);                                  // [kRdE][kRmWLd]
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(rd_smem + kRmOffX);        // [kRdT][kRmXLd]
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv
     }
     *reinterpret_cast<float4*>(part + t * kRdE + c) = sum;
   }
-  decode_router_tail(part, Tb, E, bias, logits, k, ids, wts, tickets, last_flag);
+  decode_router_tail(part, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, last_flag);
 }
 
 // Prefill-sized router: SIMT tiled GEMM, 64 tokens x 64 experts per CTA, 4x4 per thread.
@@ -538,13 +564,14 @@ __global__ void __launch_bounds__(256) k_router_gemm(const XT* __restrict__ x, i
 __global__ void __launch_bounds__(256, 2) k_select(const float* __restrict__ logits,
                                                 const int32_t* __restrict__ forced_ids,
                                                 const float* __restrict__ forced_w, int T, int E, int k,
-                                                int32_t* __restrict__ ids, float* __restrict__ w, DevStatus* st) {
+                                                int32_t* __restrict__ ids, float* __restrict__ w, DevStatus* st,
+                                                const float* sel_bias) {
   pdl_begin();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   if (!forced_ids) {
-    select_write_free(logits + size_t(t) * E, E, lane, ids + size_t(t) * k, w + size_t(t) * k);
+    select_write_free(logits + size_t(t) * E, E, lane, ids + size_t(t) * k, w + size_t(t) * k, sel_bias);
     return;
   }
   int sel = -1;      // lane i < k holds slot i's expert
@@ -581,15 +608,17 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
   if (T <= 32) {
     dim3 grid((L.E + 7) / 8);
     if (x_bf16)
-      k_router_warp<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias, logits);
+      k_router_warp<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
+                                                        logits);
     else
-      k_router_warp<float><<<grid, 256, 0, s>>>((const float*)x, T, L.d, L.E, L.Wr, L.bias, logits);
+      k_router_warp<float><<<grid, 256, 0, s>>>((const float*)x, T, L.d, L.E, L.Wr, L.logit_bias(), logits);
   } else {
     dim3 grid((L.E + 63) / 64, (T + 63) / 64);
     if (x_bf16)
       return launch_pdl(k_router_gemm<__nv_bfloat16>, grid, dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr,
-                        L.bias, logits);
-    return launch_pdl(k_router_gemm<float>, grid, dim3(256), 0, s, (const float*)x, T, L.d, L.E, L.Wr, L.bias, logits);
+                        L.logit_bias(), logits);
+    return launch_pdl(k_router_gemm<float>, grid, dim3(256), 0, s, (const float*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
+                      logits);
   }
   return cudaGetLastError();
 }
@@ -621,10 +650,10 @@ cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerD
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
   if (x_bf16)
-    return cudaLaunchKernelEx(&cfg, k_router_decode_bf16, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.bias, logits,
-                              L.k, ids, wts, st->tickets);
-  return cudaLaunchKernelEx(&cfg, k_router_decode_f32, (const float*)x, T, L.d, L.E, L.Wr, L.bias, logits, L.k, ids,
-                            wts, st->tickets);
+    return cudaLaunchKernelEx(&cfg, k_router_decode_bf16, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
+                              L.sel_bias(), logits, L.k, ids, wts, st->tickets);
+  return cudaLaunchKernelEx(&cfg, k_router_decode_f32, (const float*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
+                            L.sel_bias(), logits, L.k, ids, wts, st->tickets);
 }
 
 cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s) {
@@ -640,14 +669,15 @@ cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDe
   const dim3 grid((L.E + kRsmE - 1) / kRsmE);
   if (x_bf16)
     return launch_pdl(k_router_small<__nv_bfloat16>, grid, dim3(threads), smem, s, (const __nv_bfloat16*)x, T, L.d, L.E,
-                      L.Wr, L.bias, logits);
-  return launch_pdl(k_router_small<float>, grid, dim3(threads), smem, s, (const float*)x, T, L.d, L.E, L.Wr, L.bias,
+                      L.Wr, L.logit_bias(), logits);
+  return launch_pdl(k_router_small<float>, grid, dim3(threads), smem, s, (const float*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
                     logits);
 }
 
 cudaError_t launch_select(const float* logits, const int32_t* forced_ids, const float* forced_w, int T,
                           const LayerDev& L, int32_t* ids, float* w, DevStatus* st, cudaStream_t s) {
-  return launch_pdl(k_select, dim3((T + 7) / 8), dim3(256), 0, s, logits, forced_ids, forced_w, T, L.E, L.k, ids, w, st);
+  return launch_pdl(k_select, dim3((T + 7) / 8), dim3(256), 0, s, logits, forced_ids, forced_w, T, L.E, L.k, ids, w, st,
+                    L.sel_bias());
 }
 
 }  // namespace moe

@@ -59,7 +59,8 @@ struct RtCtl {
 
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_router_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
-                const float* __restrict__ bias, int T, int d, int E, int n_half, int n_a, int n_b, int tmem_cols,
+                const float* __restrict__ bias, const float* __restrict__ sel_bias, int T, int d, int E, int n_half,
+                int n_a, int n_b, int tmem_cols,
                 float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int k,
                 int* status_flags) {
   extern __shared__ uint8_t rt_smem_raw[];
@@ -203,10 +204,11 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_wait(&ctl->mma_done, 0, &zero);
     }
   } else {  // epilogue: one token per TMEM lane, logits = acc + bias
-    // With ids != nullptr the epilogue also selects: a sorted list of the kTopK best
-    // (larger logit first, lower index first on equal logits; the scan visits experts in
-    // increasing index, so an equal later logit never displaces an earlier one), then the
-    // softmax over the selected logits, summed in slot order.
+    // With ids != nullptr the epilogue also selects: a sorted list of the kTopK best scores
+    // (larger first, lower index first on equal scores; the scan visits experts in increasing
+    // index, so an equal later score never displaces an earlier one), then the softmax over
+    // the selected logits, summed in slot order.  The score is the logit, plus sel_bias in the
+    // selection-only bias mode.
     const int q = warp & 3;
     int jt = 0;
     for (int j = 0; tile_of(j, rank) < n_items; ++j, ++jt) {
@@ -218,11 +220,12 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       tc_fence_after();
       const int t = item * kRtM + q * 32 + lane;
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16);
-      float tv[kTopK];
+      float tv[kTopK], tl[kTopK];  // scores and their logits
       int ti[kTopK];
 #pragma unroll
       for (int i = 0; i < kTopK; ++i) {
         tv[i] = -INFINITY;
+        tl[i] = -INFINITY;
         ti[i] = 0x7fffffff;
       }
       for (int c0 = 0; c0 < 2 * n_half && c0 < E; c0 += 16) {
@@ -234,9 +237,11 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             const int e = c0 + i;
             if (e < E) {
               const float lg = v[i] + (bias ? bias[e] : 0.0f);
+              const float sc = sel_bias ? lg + sel_bias[e] : lg;
               if (logits) logits[size_t(t) * E + e] = lg;
-              if (ids && (lg > tv[kTopK - 1] || (lg == tv[kTopK - 1] && e < ti[kTopK - 1]))) {
-                tv[kTopK - 1] = lg;
+              if (ids && (sc > tv[kTopK - 1] || (sc == tv[kTopK - 1] && e < ti[kTopK - 1]))) {
+                tv[kTopK - 1] = sc;
+                tl[kTopK - 1] = lg;
                 ti[kTopK - 1] = e;
 #pragma unroll
                 for (int j2 = kTopK - 1; j2 > 0; --j2) {
@@ -244,6 +249,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                     const float fv = tv[j2];
                     tv[j2] = tv[j2 - 1];
                     tv[j2 - 1] = fv;
+                    const float fl = tl[j2];
+                    tl[j2] = tl[j2 - 1];
+                    tl[j2 - 1] = fl;
                     const int fi = ti[j2];
                     ti[j2] = ti[j2 - 1];
                     ti[j2 - 1] = fi;
@@ -255,10 +263,14 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         }
       }
       if (ids && t < T) {
+        float m = tl[0];  // the largest selected logit (slot 0 unless the bias reordered them)
+#pragma unroll
+        for (int i = 1; i < kTopK; ++i)
+          if (i < k) m = fmaxf(m, tl[i]);
         float ex[kTopK], sum = 0.0f;
 #pragma unroll
         for (int i = 0; i < kTopK; ++i) {
-          ex[i] = i < k ? expf(tv[i] - tv[0]) : 0.0f;
+          ex[i] = i < k ? expf(tl[i] - m) : 0.0f;
           sum += ex[i];
         }
 #pragma unroll
@@ -336,8 +348,8 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_router_tc, mx, mw, L.bias, T, L.d, L.E, n_half, n_a, n_b, tmem_cols, logits, ids,
-                            wts, L.k, &st->flags);
+  return cudaLaunchKernelEx(&cfg, k_router_tc, mx, mw, L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half, n_a, n_b,
+                            tmem_cols, logits, ids, wts, L.k, &st->flags);
 }
 
 }  // namespace moe

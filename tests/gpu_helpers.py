@@ -18,11 +18,11 @@ def to_host_bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def check_free_layer(w, x, y_gpu, ids_gpu, w_gpu, nthreads=None, where=""):
+def check_free_layer(w, x, y_gpu, ids_gpu, w_gpu, nthreads=None, where="", bias_mode=o.BIAS_SCORE):
     """Free routing: ids within the near-tie rule of the oracle's; then the outputs against
     the oracle run with the GPU's ids forced (weights from the oracle's own router)."""
     nt = nthreads or o.default_threads()
-    L = o.Layer(w)
+    L = o.Layer(w, bias_mode=bias_mode)
     ref = o.layer_forward(L, x, want_probs=True, nthreads=nt)
     ids = ids_gpu.cpu().numpy()
     ok, bad, ndiff = parity.ids_ok(ids, ref["ids"], ref["p"], w.E)
@@ -35,9 +35,9 @@ def check_free_layer(w, x, y_gpu, ids_gpu, w_gpu, nthreads=None, where=""):
     return ref, msg, ndiff
 
 
-def check_forced_layer(w, x, forced_ids, forced_w, y_gpu, ids_gpu, nthreads=None, where=""):
+def check_forced_layer(w, x, forced_ids, forced_w, y_gpu, ids_gpu, nthreads=None, where="", bias_mode=o.BIAS_SCORE):
     nt = nthreads or o.default_threads()
-    ref = o.layer_forward(o.Layer(w), x, forced_ids=forced_ids, forced_w=forced_w, nthreads=nt)
+    ref = o.layer_forward(o.Layer(w, bias_mode=bias_mode), x, forced_ids=forced_ids, forced_w=forced_w, nthreads=nt)
     assert np.array_equal(ids_gpu.cpu().numpy(), forced_ids), f"{where}: forced ids not bit-exact"
     oky, msg = parity.outputs_ok(y_gpu.float().cpu().numpy(), ref["y"])
     assert oky, f"{where}: outputs: {msg}"

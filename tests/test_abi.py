@@ -96,6 +96,11 @@ def test_host_validation_rejects_before_any_launch(lib):
     tiled_odd = _layer(binding, F=576)
     tiled_odd.w_layout = binding.LAYOUT_TILED
     assert fwd(p, 1, 4, ctypes.byref(tiled_odd), None, None, None, None, p, 0, 0, ws, 1 << 40, None) == -2
+    # an unknown bias mode
+    bad_bias = _layer(binding)
+    bad_bias.bias_mode = 2
+    assert fwd(p, 1, 4, ctypes.byref(bad_bias), None, None, None, None, p, 0, 0, ws, 1 << 40, None) == -1
+    assert lib.moe_route(p, 1, 4, ctypes.byref(bad_bias), 6, p, p, None, ws, 1 << 40, None) == -1
     # packing: needs E4M3 rows with d, ffn multiples of 128, and four aligned destinations
     pack = lib.moe_pack_weights
     assert pack(ctypes.byref(_layer(binding, F=576)), p, p, p, p, None) == -2

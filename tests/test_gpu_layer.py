@@ -180,6 +180,56 @@ def test_router_shapes(moe, d, E, T, bf16):
     assert moe.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("T,E,d", [(64, 384, 2048), (100, 384, 1024), (300, 384, 2048), (40, 1000, 256),
+                                   (300, 1000, 512)])
+def test_selection_only_bias_routing(moe, T, E, d):
+    """MOE_BIAS_SELECT on every router: the decode router (mma.sync, ticketed selection), the
+    tensor-core router with its epilogue selection, and the SIMT router + selection kernel
+    (E = 1000).  Logits carry no bias; ids pass the near-tie rule on the oracle's selection
+    probabilities (softmax of logits + bias); weights are the renormalised unbiased softmax."""
+    w = g.make_layer(61 + d, d, 64, E, fp8=True, bias_var=0.5)
+    L = moe.Layer.from_host(w, bias_mode=moe.binding.BIAS_SELECT)
+    x = g.make_x(62 + d, T, d, bf16=True)
+    ws = moe.workspace(L, T)
+    ids, wt, lg = moe.route(to_dev_x(x), L, ws, logits=True)
+    ref = o.layer_forward(o.Layer(w, bias_mode=o.BIAS_SELECT), x, want_probs=True, nthreads=o.default_threads())
+    lg = lg.cpu().numpy()
+    err = np.max(np.abs(lg - ref["logits"]), axis=1) / np.max(np.abs(ref["logits"]), axis=1)
+    assert err.max() < 3e-5, err.max()
+    ids = ids.cpu().numpy()
+    ok, bad, _ = parity.ids_ok(ids, ref["ids"], ref["p"], E)
+    assert ok, bad
+    same = np.all(ids == ref["ids"], axis=1)
+    assert same.mean() > 0.9
+    assert np.max(np.abs(wt.cpu().numpy()[same] - ref["w"][same])) < 1e-5
+    # both modes rank on logits + bias, so they pick the same experts; only the weights differ
+    score = o.layer_forward(o.Layer(w), x)
+    assert np.array_equal(score["ids"], ref["ids"])
+    assert np.max(np.abs(score["w"] - ref["w"])) > 1e-2
+    assert moe.get_status(ws) == 0
+
+
+def test_selection_only_bias_layer_free_and_forced(moe, kolibri):
+    """A full decode layer (tiled weights, tcgen05 experts) in MOE_BIAS_SELECT: free routing
+    against the oracle in that mode, then forced ids with the weights left to the router
+    (the unbiased softmax), then the planted 'biased weights' mistake must fail."""
+    w = kolibri.w
+    L = moe.Layer.from_host(w, bias_mode=moe.binding.BIAS_SELECT)
+    T = 64
+    x = g.make_x(63, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    check_free_layer(w, x, y, ids, wt, where="select-only free", bias_mode=o.BIAS_SELECT)
+    fid = ids.cpu().numpy()
+    y2, ids2, _ = moe.forward(to_dev_x(x), L, ws, forced_ids=ids)
+    check_forced_layer(w, x, fid, None, y2, ids2, where="select-only forced", bias_mode=o.BIAS_SELECT)
+    mut = o.layer_forward(o.Layer(w, bias_mode=o.BIAS_SELECT, mutant=o.MUTANTS["biased_weights"]), x,
+                          nthreads=o.default_threads())
+    same = np.all(mut["ids"] == fid, axis=1)
+    assert same.any() and not parity.weights_ok(wt.cpu().numpy()[same], mut["w"][same])[0]
+    assert moe.get_status(ws) == 0
+
+
 def test_router_fp32_tiny(moe, tiny):
     w, L = tiny
     x = g.make_x(g.SEED_TINY, 32, w.d, bf16=False)
