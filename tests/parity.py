@@ -79,3 +79,20 @@ def weights_ok(w, w_ref, tol=1e-5):
         return True, "empty"
     err = float(np.max(np.abs(w - w_ref)))
     return err <= tol, f"max|w err|={err:.3e}"
+
+
+def routing_diagnostics(logits, ids, logits_ref, ids_ref) -> dict:
+    """The router comparison the pages report ("We Ported Aleph Alpha's Kolibri to a MacBook.
+    Our Own Gate Said No.", section "Taking it apart"): the router-logit error normalised by the
+    spread of each reference row (max |dlogit| / std of the reference logits), and how often the
+    selected experts disagree: as sets per token, and slot by slot."""
+    lg = np.asarray(logits, np.float64)
+    lr = np.asarray(logits_ref, np.float64)
+    sigma = lr.std(axis=1)
+    sig_err = np.max(np.abs(lg - lr), axis=1) / np.where(sigma > 0, sigma, 1.0)
+    ids = np.asarray(ids)
+    ids_ref = np.asarray(ids_ref)
+    set_diff = np.array([set(a) != set(b) for a, b in zip(ids.tolist(), ids_ref.tolist())])
+    return {"sigma_err_max": float(sig_err.max()), "sigma_err_mean": float(sig_err.mean()),
+            "token_set_disagreement": float(set_diff.mean()),
+            "slot_disagreement": float(np.mean(ids != ids_ref))}

@@ -401,3 +401,15 @@ def test_golden_facts_match_the_workloads():
     gw = facts["gemma_first_wave_rows"]["value"]
     assert gw["prompts"] * gw["padded_len"] * gw["top_k"] == gw["rows"] and gw["rows"] % 64 == 0
     assert all(r % 64 for r in facts["gather_rowcounts_wrong_on_m5"]["value"])
+
+
+def test_routing_diagnostics_on_constructed_rows():
+    """The diagnostics helper on rows whose answers are known by construction."""
+    ref = np.array([[0.0, 1.0, 2.0, 3.0], [1.0, 1.0, 3.0, 3.0]], np.float32)  # stds 1.118..., 1.0
+    got = ref.copy()
+    got[1, 2] += 0.5
+    d = parity.routing_diagnostics(got, np.array([[3, 2], [2, 3]]), ref, np.array([[3, 2], [3, 1]]))
+    assert d["sigma_err_max"] == pytest.approx(0.5)
+    assert d["sigma_err_mean"] == pytest.approx(0.25)
+    assert d["token_set_disagreement"] == pytest.approx(0.5)  # {2,3} vs {1,3} in the second token
+    assert d["slot_disagreement"] == pytest.approx(0.5)       # slots differ in the second token only
