@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "tma.cuh"
+#include "dispatch_dev.cuh"
 
 using namespace moe;
 
@@ -103,11 +104,17 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
     return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
   MOE_TRY(mark(0));
-  bool selected = false;  // the decode and tensor-core routers select in-kernel under free routing
+  bool selected = false;    // the decode and tensor-core routers select in-kernel under free routing
+  bool dispatched = false;  // the decode router also dispatches then
   if (!(forced_ids && forced_w)) {
     if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
       selected = !forced_ids;
-      MOE_TRY(launch_router_decode(x, x_bf16, T, L, logits, selected ? ids : nullptr, selected ? w : nullptr, st, s));
+      // under free routing the router's last selecting CTA also dispatches
+      dispatched = selected && L.E < 512;
+      DispatchOut dsp;
+      dispatch_outputs(lay, base, counts, offsets, perm, pos, &dsp);
+      MOE_TRY(launch_router_decode(x, x_bf16, T, L, logits, selected ? ids : nullptr, selected ? w : nullptr, st,
+                                   dispatched ? &dsp : nullptr, rows_per_tile, s));
     } else if (T <= kRouterSmallMaxT && L.d <= 8192) {
       MOE_TRY(launch_router_small(x, x_bf16, T, L, logits, s));
     } else if (T > kRouterSmallMaxT && router_tc_supported(L, x_bf16)) {
@@ -121,7 +128,7 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   MOE_TRY(mark(1));
   if (!selected) MOE_TRY(launch_select(logits, forced_ids, forced_w, T, L, ids, w, st, s));
   MOE_TRY(mark(2));
-  MOE_TRY(launch_dispatch(ids, T, L.E, L.k, rows_per_tile, lay, base, counts, offsets, perm, pos, s));
+  if (!dispatched) MOE_TRY(launch_dispatch(ids, T, L.E, L.k, rows_per_tile, lay, base, counts, offsets, perm, pos, s));
   MOE_TRY(mark(3));
   MOE_TRY(launch_act_quant(x, x_bf16, T, L, pos, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
   MOE_TRY(mark(4));
@@ -215,7 +222,7 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + lay.logits);
   DevStatus* st = reinterpret_cast<DevStatus*>(base + lay.status);
   if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
-    MOE_TRY(launch_router_decode(x, x_dtype == MOE_BF16, T, L, logits, ids_out, w_out, st, s));
+    MOE_TRY(launch_router_decode(x, x_dtype == MOE_BF16, T, L, logits, ids_out, w_out, st, nullptr, 0, s));
     return MOE_OK;
   } else if (T <= kRouterSmallMaxT && L.d <= 8192)
     MOE_TRY(launch_router_small(x, x_dtype == MOE_BF16, T, L, logits, s));

@@ -19,7 +19,7 @@ struct DevStatus {
   int flags;        // bit 0: bad forced id, bit 1: timeout
   int bad_forced;   // number of rejected forced slots
   int timeout_site; // where a bounded wait gave up (0 = none)
-  int pad0;
+  int dispatch_ticket;  // decode router: selecting CTAs done, the last one dispatches; 0 between launches
   int tickets[16];  // decode router: CTAs done per (token block, token sub-block); 0 between launches
   int pad[44];
 };
@@ -221,13 +221,18 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
 // Decode router (T <= kRouterSmallMaxT, d % 256 == 0, d <= 2048): k split over the CTAs of a
 // thread-block cluster, partials summed through distributed shared memory; deterministic.
 // Writes logits; with ids/wts not NULL it also selects the top-k (free routing), using the
-// ticket counters in st (zero between launches).
+// ticket counters in st (zero between launches), and with dsp not NULL its last selecting CTA
+// also runs the dispatch (E < 512).
+struct DispatchOut;
 cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, int32_t* ids,
-                                 float* wts, DevStatus* st, cudaStream_t s);
+                                 float* wts, DevStatus* st, const DispatchOut* dsp, int rows_per_tile, cudaStream_t s);
 // Decode router (T <= kRouterSmallMaxT, d <= 8192): all of k per CTA, deterministic.
 cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
 
 
+// The dispatch outputs run_layer hands to the decode router.
+void dispatch_outputs(const WsLayout& ws, char* base, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
+                      DispatchOut* o);
 cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_per_tile, const WsLayout& ws,
                             char* base, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
                             cudaStream_t s);

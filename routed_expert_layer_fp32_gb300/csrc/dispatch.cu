@@ -10,6 +10,7 @@
 // earlier token, so the order is stable), and the group's highest lane advances the counter.
 // The per-warp counts are combined by prefix sums across warps, CTAs and experts.
 #include "common.cuh"
+#include "dispatch_dev.cuh"
 
 namespace moe {
 namespace {
@@ -17,67 +18,6 @@ namespace {
 constexpr int kWarps = 32;  // warps per dispatch CTA (1024 threads)
 constexpr int kTokensPerWarp = kDispatchChunk / kWarps;
 
-template <class F>
-__device__ __forceinline__ void warp_walk(const int32_t* __restrict__ ids, int t0, int t1, int k, int E, int* cnt,
-                                          F f) {
-  const int lane = threadIdx.x & 31;
-  const int tpi = 32 / k;
-  const int tl = lane / k, s = lane - (lane / k) * k;
-  for (int base = t0; base < t1; base += tpi) {
-    const int t = base + tl;
-    int e = (tl < tpi && t < t1) ? ids[size_t(t) * k + s] : -1;
-    if (e >= E) e = -1;  // out-of-range ids get no row
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    if (e >= 0) f(t, s, cnt[e] + __popc(m & ((1u << lane) - 1u)));
-    __syncwarp();
-    if (e >= 0 && (31 - __clz(m)) == lane) cnt[e] += __popc(m);
-    __syncwarp();
-  }
-}
-
-// Exclusive scan of n <= 2 * blockDim ints in shared memory (blockDim = 1024).  Returns the
-// total to every thread.
-__device__ int block_exclusive_scan(int* a, int n, int* warp_tot) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i0 = 2 * tid, i1 = 2 * tid + 1;
-  const int v0 = i0 < n ? a[i0] : 0, v1 = i1 < n ? a[i1] : 0;
-  int s = v0 + v1, incl = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int wt = lane < (blockDim.x >> 5) ? warp_tot[lane] : 0, wi = wt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
-    }
-    warp_tot[lane] = wi - wt;  // exclusive warp offsets
-    if (lane == 31) warp_tot[32] = wi;
-  }
-  __syncthreads();
-  const int ex = warp_tot[warp] + incl - s;
-  const int total = warp_tot[32];
-  __syncthreads();
-  if (i0 < n) a[i0] = ex;
-  if (i1 < n) a[i1] = ex + v0;
-  __syncthreads();
-  return total;
-}
-
-struct DispatchOut {
-  int32_t* counts;
-  int32_t* offsets;
-  int32_t* perm;
-  int32_t* pos;
-  int32_t* chunk_base;  // [n_chunks, E]: counts per chunk, then their exclusive prefix
-  Tile* tiles;
-  int32_t* n_tiles;
-};
 
 // Phase 1 (per CTA): per-warp counts of the chunk -> chunk totals [chunk][e].
 // Warps of this CTA that own tokens (the rest skip every per-warp loop).
@@ -223,97 +163,30 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
   scatter_chunk(ids, T, E, k, smem, o);
 }
 
-// T <= kDispatchChunk and E < 512: one CTA of 256 threads, every count in shared memory.
-// Warp w owns the run of tokens [w*tpw, (w+1)*tpw); per-warp counts become per-warp row
-// bases by a prefix over the warps, then over the experts.
-constexpr int kLeanWarps = 8;
-__global__ void __launch_bounds__(kLeanWarps * 32) k_dispatch_lean(const int32_t* __restrict__ ids, int T, int E, int k,
-                                                                  int rows_per_tile, DispatchOut o) {
+__global__ void __launch_bounds__(kLeanWarps * 32) k_dispatch_lean(const int32_t* __restrict__ ids_g, int T, int E,
+                                                                  int k, int rows_per_tile, DispatchOut o) {
   pdl_begin();
   extern __shared__ int lean_smem[];
-  int* wcnt = lean_smem;             // [kLeanWarps][E]
-  int* tot = lean_smem + kLeanWarps * E;  // [E + 1]
-  __shared__ int warp_tot[33];
-  const int warp = threadIdx.x >> 5;
-  const int tpw = (T + kLeanWarps - 1) / kLeanWarps;
-  const int t0 = min(T, warp * tpw), t1 = min(T, t0 + tpw);
-  for (int i = threadIdx.x; i < kLeanWarps * E; i += blockDim.x) wcnt[i] = 0;
-  __syncthreads();
-  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < kLeanWarps; ++w) {
-      const int v = wcnt[w * E + e];
-      wcnt[w * E + e] = run;
-      run += v;
-    }
-    tot[e] = run;
-    o.counts[e] = run;
-  }
-  __syncthreads();
-  block_exclusive_scan(tot, E, warp_tot);  // tot[e] = offset of expert e
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    o.offsets[e] = tot[e];
-    for (int w = 0; w < kLeanWarps; ++w) wcnt[w * E + e] += tot[e];
-  }
-  if (threadIdx.x == 0) {
-    o.counts[E] = T;
-    o.offsets[E] = k * T;
-    o.offsets[E + 1] = (k + 1) * T;
-  }
-  __syncthreads();
-  // tile list, shared expert first: tile counts per group, scanned
-  int* ntile = tot;  // reused: [E + 1] tiles per group (shared expert first)
-  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
-    const int g = q == 0 ? E : q - 1;
-    const int c = g == E ? T : o.counts[g];
-    ntile[q] = (c + rows_per_tile - 1) / rows_per_tile;
-  }
-  __syncthreads();
-  const int total_tiles = block_exclusive_scan(ntile, E + 1, warp_tot);
-  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
-    const int g = q == 0 ? E : q - 1;
-    const int c = g == E ? T : o.counts[g];
-    const int base_row = g == E ? k * T : o.offsets[g];
-    int ti = ntile[q];
-    for (int r = 0; r < c; r += rows_per_tile, ++ti) {
-      Tile tl;
-      tl.group = g;
-      tl.row0 = base_row + r;
-      tl.nrows = min(rows_per_tile, c - r);
-      tl.pad = 0;
-      o.tiles[ti] = tl;
-    }
-  }
-  if (threadIdx.x == 0) *o.n_tiles = total_tiles;
-  // rows: invalid slots get pos = -1; valid ones are placed in token order
-  for (int i = (threadIdx.x & 31); i < (t1 - t0) * k; i += 32) {
-    const int t = t0 + i / k;
-    const int e = ids[size_t(t) * k + (i % k)];
-    if (e < 0 || e >= E) o.pos[size_t(t) * k + (i % k)] = -1;
-  }
-  int32_t* perm = o.perm;
-  int32_t* pos = o.pos;
-  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [&](int t, int s, int row) {
-    perm[row] = t;
-    pos[size_t(t) * k + s] = row;
-  });
-  for (int t = threadIdx.x; t < T; t += blockDim.x) perm[size_t(k) * T + t] = t;
+  dispatch_lean_body(ids_g, T, E, k, rows_per_tile, o, lean_smem);
 }
 
 }  // namespace
 
+void dispatch_outputs(const WsLayout& ws, char* base, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
+                      DispatchOut* o) {
+  o->counts = counts;
+  o->offsets = offsets;
+  o->perm = perm;
+  o->pos = pos;
+  o->chunk_base = reinterpret_cast<int32_t*>(base + ws.chunk_counts);
+  o->tiles = reinterpret_cast<Tile*>(base + ws.tiles);
+  o->n_tiles = reinterpret_cast<int32_t*>(base + ws.n_tiles);
+}
+
 cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_per_tile, const WsLayout& ws, char* base,
                             int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos, cudaStream_t s) {
   DispatchOut o;
-  o.counts = counts;
-  o.offsets = offsets;
-  o.perm = perm;
-  o.pos = pos;
-  o.chunk_base = reinterpret_cast<int32_t*>(base + ws.chunk_counts);
-  o.tiles = reinterpret_cast<Tile*>(base + ws.tiles);
-  o.n_tiles = reinterpret_cast<int32_t*>(base + ws.n_tiles);
+  dispatch_outputs(ws, base, counts, offsets, perm, pos, &o);
   const size_t smem = size_t(kWarps) * E * sizeof(int);
   const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
   // opt in once per process to the largest per-warp counter table (E <= kMaxExperts); later
@@ -327,7 +200,7 @@ cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_pe
   }();
   if (attr != cudaSuccess) return attr;
   if (n_chunks == 1 && E < 512) {
-    const size_t lean = size_t(kLeanWarps * E + E + 1) * sizeof(int);
+    const size_t lean = size_t(lean_dispatch_smem_ints(T, E, k)) * sizeof(int);
     return launch_pdl(k_dispatch_lean, dim3(1), dim3(kLeanWarps * 32), lean, s, ids, T, E, k, rows_per_tile, o);
   }
   if (n_chunks == 1) {

@@ -45,7 +45,8 @@ template <typename XT, bool kFp8>
 __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, int k,
                                                    const int32_t* __restrict__ pos, void* __restrict__ xq,
                                                    float* __restrict__ sx) {
-  pdl_begin();
+  // x was written before the router ran: its scale is found before the wait for the dispatch
+  // kernel, whose row positions are needed only for the stores
   __shared__ float red[8];
   const int t = blockIdx.x;
   const XT* xr = x + size_t(t) * d;
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int
   __syncthreads();
   amax = red[0];
   const float s = kFp8 ? (amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f) : 1.0f;
+  pdl_begin();
   int rows[kTopK + 1];
   int nr = 0;
   for (int i = 0; i < k; ++i) {

@@ -6,6 +6,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "dispatch_dev.cuh"
 
 namespace moe {
 namespace {
@@ -247,16 +248,18 @@ __global__ void __launch_bounds__(512) k_router_small(const XT* __restrict__ x, 
 // cluster.  Each CTA computes partial logits [64 tokens][16 experts] over its k-slice; then
 // decode_router_tail sums the cluster's partials and selects.
 constexpr int kRdE = 16, kRdK = 256, kRdT = 64, kRdThreads = 256;
+static_assert(kRdThreads == kLeanWarps * 32, "the router's CTAs run the one-CTA dispatch");
 
 // Cluster rank r sums the n_slice partials of token sub-block r through distributed shared
 // memory in rank order (deterministic) and writes logits + bias.  With ids != NULL, the CTAs
 // that wrote token sub-block r of token block z then count themselves on a ticket; the last of
 // them (every expert group's logits for those tokens are written by then) picks top-k and
 // weights for those tokens, a warp per token, as k_select does, and resets the ticket.
-__device__ __forceinline__ void decode_router_tail(const float* part, int Tb, int E, const float* __restrict__ bias,
-                                                   const float* sel_bias, float* logits, int k,
-                                                   int32_t* __restrict__ ids, float* __restrict__ wts, int* tickets,
-                                                   int* last_flag) {
+__device__ __forceinline__ void decode_router_tail(const float* part, int T, int Tb, int E,
+                                                   const float* __restrict__ bias, const float* sel_bias, float* logits,
+                                                   int k, int32_t* __restrict__ ids, float* __restrict__ wts,
+                                                   int* tickets, int* dispatch_ticket, const DispatchOut& dsp,
+                                                   int rows_per_tile, int* scratch, int* last_flag) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x;
@@ -297,6 +300,20 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int Tb, in
         const size_t row = size_t(t_base + t);
         select_write_free(logits + row * E, E, lane, ids + row * k, wts + row * k, sel_bias);
       }
+      if (dsp.counts) {
+        // the selecting CTAs count themselves; the last (every token's ids written by then)
+        // runs the dispatch in this CTA, on its staging memory
+        __syncthreads();
+        if (tid == 0) {
+          int old;
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(dispatch_ticket) : "memory");
+          const int last = old == int(gridDim.z) * n_slice - 1;
+          if (last) *dispatch_ticket = 0;  // ready for the next launch
+          *last_flag = last ? 2 : 1;
+        }
+        __syncthreads();
+        if (*last_flag == 2) dispatch_lean_body(ids, T, E, k, rows_per_tile, dsp, scratch);
+      }
     }
   }
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -311,7 +328,8 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float
                                                                   const float* __restrict__ bias,
                                                                   const float* sel_bias, float* logits, int k,
                                                                   int32_t* __restrict__ ids, float* __restrict__ wts,
-                                                                  int* tickets) {
+                                                                  int* tickets, int* dispatch_ticket, DispatchOut dsp,
+                                                                  int rows_per_tile) {
   extern __shared__ __align__(16) uint8_t rd_smem[];
   float* ws = reinterpret_cast<float*>(rd_smem);  // [kRdE][kRdLd]
   float* xs = ws + kRdE * kRdLd;                   // [kRdT][kRdLd]
@@ -373,7 +391,8 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float
     part[(2 * tg + 1) * kRdE + eg] = acc[1][0];
     part[(2 * tg + 1) * kRdE + eg + 8] = acc[1][1];
   }
-  decode_router_tail(part, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, last_flag);
+  decode_router_tail(part, T, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, dispatch_ticket, dsp,
+                     rows_per_tile, reinterpret_cast<int*>(rd_smem), last_flag);
 }
 
 // bf16 x: tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).  Wr rows are split on
@@ -424,7 +443,8 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv
                                                                    const float* __restrict__ bias,
                                                                    const float* sel_bias, float* logits, int k,
                                                                    int32_t* __restrict__ ids, float* __restrict__ wts,
-                                                                   int* tickets) {
+                                                                   int* tickets, int* dispatch_ticket, DispatchOut dsp,
+                                                                   int rows_per_tile) {
   extern __shared__ __align__(16) uint8_t rd_smem[];
   float* ws = reinterpret_cast<float*>(rd_smem);                                  // [kRdE][kRmWLd]
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(rd_smem + kRmOffX);        // [kRdT][kRmXLd]
@@ -436,13 +456,15 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv
   const int e0 = blockIdx.x * kRdE, k0 = blockIdx.y * kRdK, t_base = blockIdx.z * kRdT;
   const int Tb = min(kRdT, T - t_base);
   const int n_tiles = (Tb + 7) >> 3;
-  pdl_begin();
+  // the router weights depend on no earlier kernel: their copies start before the wait for
+  // the kernel that writes x
 #pragma unroll
   for (int j = 0; j < 4; ++j) {  // Wr slice: 16 rows x 64 chunks of 16 bytes
     const int i = tid + kRdThreads * j, r = i >> 6, c = (i & 63) * 4;
     const bool ok = e0 + r < E;
     cp_async16(ws + r * kRmWLd + c, ok ? Wr + size_t(e0 + r) * d + k0 + c : Wr, ok ? 16 : 0);
   }
+  pdl_begin();
 #pragma unroll
   for (int j = 0; j < 8; ++j) {  // x slice: 64 rows x 32 chunks of 16 bytes (rows past the tokens zero-filled)
     const int i = tid + kRdThreads * j, t = i >> 5, c = (i & 31) * 8;
@@ -504,7 +526,8 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv
     }
     *reinterpret_cast<float4*>(part + t * kRdE + c) = sum;
   }
-  decode_router_tail(part, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, last_flag);
+  decode_router_tail(part, T, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, dispatch_ticket, dsp,
+                     rows_per_tile, reinterpret_cast<int*>(rd_smem), last_flag);
 }
 
 // Prefill-sized router: SIMT tiled GEMM, 64 tokens x 64 experts per CTA, 4x4 per thread.
@@ -624,7 +647,7 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
 }
 
 cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, int32_t* ids,
-                                 float* wts, DevStatus* st, cudaStream_t s) {
+                                 float* wts, DevStatus* st, const DispatchOut* dsp, int rows_per_tile, cudaStream_t s) {
   if (T > kRouterSmallMaxT || L.d % kRdK || L.d / kRdK > 8) return cudaErrorInvalidValue;
   const int n_slice = L.d / kRdK;
   static cudaError_t attr = [] {
@@ -649,11 +672,14 @@ cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerD
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
+  DispatchOut none{};
+  const DispatchOut d = (dsp && ids) ? *dsp : none;  // dispatch only after a selection, and only if asked
+  if (d.counts && !(L.E < 512 && T <= kDispatchChunk)) return cudaErrorInvalidValue;
   if (x_bf16)
     return cudaLaunchKernelEx(&cfg, k_router_decode_bf16, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
-                              L.sel_bias(), logits, L.k, ids, wts, st->tickets);
+                              L.sel_bias(), logits, L.k, ids, wts, st->tickets, &st->dispatch_ticket, d, rows_per_tile);
   return cudaLaunchKernelEx(&cfg, k_router_decode_f32, (const float*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
-                            L.sel_bias(), logits, L.k, ids, wts, st->tickets);
+                            L.sel_bias(), logits, L.k, ids, wts, st->tickets, &st->dispatch_ticket, d, rows_per_tile);
 }
 
 cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s) {
