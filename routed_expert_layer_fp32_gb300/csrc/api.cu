@@ -138,7 +138,7 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   MOE_TRY(mark(6));
   MOE_TRY(use_tc ? launch_down_tc(L, T, lay, base, s) : launch_down_stream(L, T, lay, base, s));
   MOE_TRY(mark(7));
-  MOE_TRY(launch_combine(reinterpret_cast<const float*>(base + lay.y_rows), pos, w, T, L, y, y_dtype, residual_add, s));
+  MOE_TRY(launch_combine(base + lay.y_rows, pos, w, T, L, y, y_dtype, residual_add, s));
   MOE_TRY(mark(8));
   return MOE_OK;
 }

@@ -76,7 +76,7 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   w.h = take(R * F * 4);
   w.qh = take(size_t(w.R_alloc) * F);
   w.sh = take(R * 4);
-  w.y_rows = take(R * d * 4);
+  w.y_rows = take(R * d * (f32w ? 4 : 2));  // expert output rows: bf16 for E4M3 layers
   w.total = o;
   return w;
 }
@@ -246,7 +246,7 @@ int tc_rows_per_tile(int T);
 cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
-cudaError_t launch_combine(const float* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L,
+cudaError_t launch_combine(const void* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L,
                            void* y, moe_dtype y_dtype, bool residual_add, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
 }  // namespace moe

@@ -118,7 +118,7 @@ struct ExpertArgs {
   float* h;           // [R, F]
   uint8_t* qh;        // [R, F]
   float* sh;          // [R]
-  float* y_rows;      // [R, d]
+  void* y_rows;       // [R, d]: bf16 rows (E4M3 layers) or fp32 rows (fp32 layers)
 };
 
 constexpr int kTG = kStreamRows / 8;     // token groups of 8 rows per tile
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_down_fp8(ExpertArgs a, int* 
         const int m = m0 + gq + ((c & 2) ? 8 : 0);
         if (r < tl.nrows) {
           const int row = tl.row0 + r;
-          a.y_rows[size_t(row) * a.d + m] = acc[tg][c] * a.sh[row] * sdn[m];
+          static_cast<__nv_bfloat16*>(a.y_rows)[size_t(row) * a.d + m] = __float2bfloat16_rn(acc[tg][c] * a.sh[row] * sdn[m]);
         }
       }
     }
@@ -467,53 +467,77 @@ __global__ void __launch_bounds__(256) k_down_f32(ExpertArgs a) {
       float s = 0.0f;
       for (int n = lane; n < a.F; n += 32) s = fmaf(hr[n], wr[n], s);
       s = warp_sum(s);
-      if (lane == 0) a.y_rows[size_t(tl.row0 + r) * a.d + m] = s;
+      if (lane == 0) static_cast<float*>(a.y_rows)[size_t(tl.row0 + r) * a.d + m] = s;
     }
   }
 }
 
 // ------------------------------------------------------------ combine ----------------------
-// y[t] = Y[shared row of t] + sum_i w[t,i] Y[pos[t,i]] in slot order; optionally
-// r <- bf16(r + y) on a bf16 residual held in `out`.
-template <typename OT, bool kResidual>
-__global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_rows, const int32_t* __restrict__ pos,
+// y[t] = Y[shared row of t] + sum_i w[t,i] Y[pos[t,i]] in slot order, in fp32; optionally
+// r <- bf16(r + y) on a bf16 residual held in `out`.  Y holds bf16 rows (E4M3 layers) or fp32
+// rows (fp32 layers).  One CTA per token, eight consecutive columns per thread and pass: the
+// seven row loads of a pass are all issued before the first add, so a pass costs one memory
+// latency, not seven.
+__device__ __forceinline__ void load_row8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load_row8(const __nv_bfloat16* p, float (&v)[8]) {
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(p), v);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <typename OT, bool kResidual, typename YT>
+__global__ void __launch_bounds__(256) k_combine(const YT* __restrict__ y_rows, const int32_t* __restrict__ pos,
                                                  const float* __restrict__ w, int T, int d, int k, OT* __restrict__ out) {
-  pdl_begin();
   const int t = blockIdx.x;
+  // the slots come from the dispatch, which completed before the kernel this launch overlaps
+  // started: read before the dependency wait
   int rows[kTopK];
   float wt[kTopK];
-  for (int i = 0; i < k; ++i) {
-    rows[i] = pos[size_t(t) * k + i];
-    wt[i] = w[size_t(t) * k + i];
+#pragma unroll
+  for (int i = 0; i < kTopK; ++i) {
+    rows[i] = i < k ? pos[size_t(t) * k + i] : -1;
+    wt[i] = i < k ? w[size_t(t) * k + i] : 0.0f;
   }
-  const float* ysh = y_rows + (size_t(k) * T + t) * d;
-  for (int m = threadIdx.x * 4; m < d; m += blockDim.x * 4) {
-    float4 acc = *reinterpret_cast<const float4*>(ysh + m);
-    for (int i = 0; i < k; ++i) {
-      if (rows[i] < 0) continue;
-      const float4 v = *reinterpret_cast<const float4*>(y_rows + size_t(rows[i]) * d + m);
-      acc.x = fmaf(wt[i], v.x, acc.x);
-      acc.y = fmaf(wt[i], v.y, acc.y);
-      acc.z = fmaf(wt[i], v.z, acc.z);
-      acc.w = fmaf(wt[i], v.w, acc.w);
-    }
+  pdl_begin();
+  const YT* ysh = y_rows + (size_t(k) * T + t) * d;
+  for (int m = threadIdx.x * 8; m < d; m += blockDim.x * 8) {
+    float acc[8], v[kTopK][8];
+    load_row8(ysh + m, acc);
+#pragma unroll
+    for (int i = 0; i < kTopK; ++i)
+      if (rows[i] >= 0) load_row8(y_rows + size_t(rows[i]) * d + m, v[i]);
+#pragma unroll
+    for (int i = 0; i < kTopK; ++i)
+      if (rows[i] >= 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(wt[i], v[i][j], acc[j]);
+      }
     OT* o = out + size_t(t) * d + m;
     if constexpr (sizeof(OT) == 4) {
-      *reinterpret_cast<float4*>(o) = acc;
+      *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     } else {
       if (kResidual) {
-        const uint2 r = *reinterpret_cast<const uint2*>(o);
-        acc.x += __uint_as_float(r.x << 16);
-        acc.y += __uint_as_float(r.x & 0xffff0000u);
-        acc.z += __uint_as_float(r.y << 16);
-        acc.w += __uint_as_float(r.y & 0xffff0000u);
+        float r[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(o), r);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += r[j];
       }
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo);
-      u.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(o) = u;
+      *reinterpret_cast<uint4*>(o) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
   }
 }
@@ -571,7 +595,7 @@ ExpertArgs expert_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.h = reinterpret_cast<float*>(base + ws.h);
   a.qh = reinterpret_cast<uint8_t*>(base + ws.qh);
   a.sh = reinterpret_cast<float*>(base + ws.sh);
-  a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
+  a.y_rows = base + ws.y_rows;
   return a;
 }
 
@@ -630,15 +654,23 @@ cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, cha
   return launch_pdl(k_down_f32, dim3(int(std::min<long long>(items, (long long)sms * 16))), dim3(256), 0, s, a);
 }
 
-cudaError_t launch_combine(const float* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
-                           moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+template <typename YT>
+cudaError_t launch_combine_t(const YT* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
+                             moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
   if (y_dtype == MOE_F32)
-    return launch_pdl(k_combine<float, false>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k, (float*)y);
+    return launch_pdl(k_combine<float, false, YT>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k, (float*)y);
   if (residual_add)
-    return launch_pdl(k_combine<__nv_bfloat16, true>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+    return launch_pdl(k_combine<__nv_bfloat16, true, YT>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
                       (__nv_bfloat16*)y);
-  return launch_pdl(k_combine<__nv_bfloat16, false>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+  return launch_pdl(k_combine<__nv_bfloat16, false, YT>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
                     (__nv_bfloat16*)y);
+}
+
+cudaError_t launch_combine(const void* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
+                           moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+  if (L.fp8)
+    return launch_combine_t(static_cast<const __nv_bfloat16*>(y_rows), pos, w, T, L, y, y_dtype, residual_add, s);
+  return launch_combine_t(static_cast<const float*>(y_rows), pos, w, T, L, y, y_dtype, residual_add, s);
 }
 
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s) {

@@ -65,7 +65,7 @@ struct TcArgs {
   const float* sh_sd;   // [d]
   float* h;             // [R, F]
   const float* sh;      // [R] h scales (down)
-  float* y_rows;        // [R, d]
+  __nv_bfloat16* y_rows;  // [R, d] expert output rows (bf16 activations)
   int* status_flags;
 };
 
@@ -360,15 +360,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float yv[16];
           load_acc(ai, c0, yv);
           const float sh_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sh[tl.row0 + c0 + lane] : 0.0f;
-          float* yp = a.y_rows + size_t(tl.row0 + c0) * a.d + m;
+          __nv_bfloat16* yp = a.y_rows + size_t(tl.row0 + c0) * a.d + m;
           if (c0 + 16 <= tl.nrows) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) yp[size_t(i) * a.d] = yv[i] * __shfl_sync(0xffffffffu, sh_l, i) * sdm;
+            for (int i = 0; i < 16; ++i)
+              yp[size_t(i) * a.d] = __float2bfloat16_rn(yv[i] * __shfl_sync(0xffffffffu, sh_l, i) * sdm);
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float shv = __shfl_sync(0xffffffffu, sh_l, i);
-              if (c0 + i < tl.nrows) yp[size_t(i) * a.d] = yv[i] * shv * sdm;
+              if (c0 + i < tl.nrows) yp[size_t(i) * a.d] = __float2bfloat16_rn(yv[i] * shv * sdm);
             }
           }
         }
@@ -470,7 +471,7 @@ TcArgs tc_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.sh_sd = L.sh_sd;
   a.h = reinterpret_cast<float*>(base + ws.h);
   a.sh = reinterpret_cast<const float*>(base + ws.sh);
-  a.y_rows = reinterpret_cast<float*>(base + ws.y_rows);
+  a.y_rows = reinterpret_cast<__nv_bfloat16*>(base + ws.y_rows);
   a.status_flags = reinterpret_cast<int*>(base + ws.status);
   a.w = nullptr;
   a.wsh = nullptr;
