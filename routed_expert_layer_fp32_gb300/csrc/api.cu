@@ -130,7 +130,7 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   MOE_TRY(mark(2));
   if (!dispatched) MOE_TRY(launch_dispatch(ids, T, L.E, L.k, rows_per_tile, lay, base, counts, offsets, perm, pos, s));
   MOE_TRY(mark(3));
-  MOE_TRY(launch_act_quant(x, x_bf16, T, L, pos, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
+  MOE_TRY(launch_act_quant(x, x_bf16, T, L, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
   MOE_TRY(mark(4));
   MOE_TRY(use_tc ? launch_gateup_tc(L, T, lay, base, s) : launch_gateup_stream(L, T, lay, base, s));
   MOE_TRY(mark(5));

@@ -71,8 +71,8 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   w.pos = take(size_t(T) * k * 4);
   w.n_tiles = take(16);
   w.tiles = take(size_t(w.max_tiles) * sizeof(Tile));
-  w.xq = take(size_t(w.R_alloc) * d * (f32w ? 4 : 1));
-  w.sx = take(R * 4);
+  w.xq = take(size_t(T) * d * (f32w ? 4 : 1));  // activation rows in token order
+  w.sx = take(size_t(T) * 4);
   w.h = take(R * F * 4);
   w.qh = take(size_t(w.R_alloc) * F);
   w.sh = take(R * 4);
@@ -236,8 +236,8 @@ void dispatch_outputs(const WsLayout& ws, char* base, int32_t* counts, int32_t* 
 cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_per_tile, const WsLayout& ws,
                             char* base, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
                             cudaStream_t s);
-cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
-                             float* sx, cudaStream_t s);
+cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, void* xq, float* sx,
+                             cudaStream_t s);
 cudaError_t launch_gateup_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_hquant(const LayerDev& L, int T, const WsLayout& ws, char* base, int rows_per_tile, cudaStream_t s);
 // tcgen05 grouped GEMMs (prefill and decode): E4M3 weights with d % 128 == 0, ffn % 128 == 0.

@@ -20,7 +20,8 @@ namespace {
 
 // ------------------------------------------------------------ activation quantisation -----
 // One CTA per token: sx = max|x| / 448 (1 if the row is zero), q = E4M3(x / sx), written to
-// the token's k routed rows (pos) and to its shared-expert row k*T + t.
+// the token's row of xq (token order: the expert kernels gather rows through perm).  The
+// fp32-weight path stores x itself, as fp32.
 template <typename XT>
 __device__ __forceinline__ void load8(const XT* p, float (&v)[8]);
 template <>
@@ -42,11 +43,10 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
 }
 
 template <typename XT, bool kFp8>
-__global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, int k,
-                                                   const int32_t* __restrict__ pos, void* __restrict__ xq,
+__global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, void* __restrict__ xq,
                                                    float* __restrict__ sx) {
-  // x was written before the router ran: its scale is found before the wait for the dispatch
-  // kernel, whose row positions are needed only for the stores
+  // x was written before the kernel this launch overlaps started: its scale is found before
+  // the dependency wait; the stores wait (the previous layer's expert kernels read xq)
   __shared__ float red[8];
   const int t = blockIdx.x;
   const XT* xr = x + size_t(t) * d;
@@ -69,13 +69,6 @@ __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int
   amax = red[0];
   const float s = kFp8 ? (amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f) : 1.0f;
   pdl_begin();
-  int rows[kTopK + 1];
-  int nr = 0;
-  for (int i = 0; i < k; ++i) {
-    int r = pos[size_t(t) * k + i];
-    if (r >= 0) rows[nr++] = r;
-  }
-  rows[nr++] = k * T + t;
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float v[8];
     load8(xr + c, v);
@@ -86,18 +79,14 @@ __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int
         lo |= uint32_t(e4m3_code2(__fdiv_rn(v[i], s), __fdiv_rn(v[i + 1], s))) << (8 * i);
         hi |= uint32_t(e4m3_code2(__fdiv_rn(v[4 + i], s), __fdiv_rn(v[5 + i], s))) << (8 * i);
       }
-      for (int j = 0; j < nr; ++j)
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(xq) + size_t(rows[j]) * d + c) = make_uint2(lo, hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(xq) + size_t(t) * d + c) = make_uint2(lo, hi);
     } else {
-      for (int j = 0; j < nr; ++j) {
-        float* dst = reinterpret_cast<float*>(xq) + size_t(rows[j]) * d + c;
-        *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
-      }
+      float* dst = reinterpret_cast<float*>(xq) + size_t(t) * d + c;
+      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
     }
   }
-  if (threadIdx.x == 0)
-    for (int j = 0; j < nr; ++j) sx[rows[j]] = s;
+  if (threadIdx.x == 0) sx[t] = s;
 }
 
 // ------------------------------------------------------------ gate/up, FP8 -----------------
@@ -113,8 +102,9 @@ struct ExpertArgs {
   const float* sh_sd;
   const Tile* tiles;
   const int* n_tiles;
-  const uint8_t* xq;  // [R, d] E4M3 (or fp32 for the fp32 path)
-  const float* sx;    // [R]
+  const int32_t* perm;  // [R] token of each row
+  const uint8_t* xq;    // [T, d] E4M3 in token order (or fp32 for the fp32 path)
+  const float* sx;      // [T]
   float* h;           // [R, F]
   uint8_t* qh;        // [R, F]
   float* sh;          // [R]
@@ -204,7 +194,8 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
       // lanes 0..15: gate rows n0 + lane; lanes 16..31: up rows n0 + lane - 16
       const uint8_t* src = Wg + (lane < 16 ? size_t(n0 + lane) : size_t(a.F + n0 + lane - 16)) * a.d;
       bulk_g2s_stream(st + lane * rs, src, a.d, &ctl->full[s], pol);
-      if (lane < tl.nrows) bulk_g2s(st + (32 + lane) * rs, a.xq + size_t(tl.row0 + lane) * a.d, a.d, &ctl->full[s]);
+      if (lane < tl.nrows)
+        bulk_g2s(st + (32 + lane) * rs, a.xq + size_t(a.perm[tl.row0 + lane]) * a.d, a.d, &ctl->full[s]);
     }
     pipe_drain(ctl, kGuStages, j);
     return;
@@ -277,7 +268,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
         const int n = n0 + gq + ((c & 2) ? 8 : 0);
         if (r < tl.nrows) {
           const int row = tl.row0 + r;
-          const float sx = a.sx[row];
+          const float sx = a.sx[a.perm[row]];
           const float gv = gsum * sx * sg[n];
           const float uv = usum * sx * su[n];
           a.h[size_t(row) * a.F + n] = silu(gv) * uv;
@@ -438,7 +429,7 @@ __global__ void __launch_bounds__(256) k_gateup_f32(ExpertArgs a) {
     const float* wg = Wg + size_t(n) * a.d;
     const float* wu = Wg + size_t(a.F + n) * a.d;
     for (int r = 0; r < tl.nrows; ++r) {
-      const float* xr = xf + size_t(tl.row0 + r) * a.d;
+      const float* xr = xf + size_t(a.perm[tl.row0 + r]) * a.d;
       float gs = 0.0f, us = 0.0f;
       for (int k = lane; k < a.d; k += 32) {
         gs = fmaf(xr[k], wg[k], gs);
@@ -560,18 +551,17 @@ int num_sms() {
 
 }  // namespace
 
-cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, const int32_t* pos, void* xq,
-                             float* sx, cudaStream_t s) {
+cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, void* xq, float* sx,
+                             cudaStream_t s) {
   if (x_bf16) {
     if (L.fp8)
-      return launch_pdl(k_act_quant<__nv_bfloat16, true>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, L.k,
-                        pos, xq, sx);
-    return launch_pdl(k_act_quant<__nv_bfloat16, false>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, L.k,
-                      pos, xq, sx);
+      return launch_pdl(k_act_quant<__nv_bfloat16, true>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, xq,
+                        sx);
+    return launch_pdl(k_act_quant<__nv_bfloat16, false>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, xq,
+                      sx);
   }
-  if (L.fp8)
-    return launch_pdl(k_act_quant<float, true>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, L.k, pos, xq, sx);
-  return launch_pdl(k_act_quant<float, false>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, L.k, pos, xq, sx);
+  if (L.fp8) return launch_pdl(k_act_quant<float, true>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, xq, sx);
+  return launch_pdl(k_act_quant<float, false>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, xq, sx);
 }
 
 namespace {
@@ -590,6 +580,7 @@ ExpertArgs expert_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.sh_sd = L.sh_sd;
   a.tiles = reinterpret_cast<const Tile*>(base + ws.tiles);
   a.n_tiles = reinterpret_cast<const int*>(base + ws.n_tiles);
+  a.perm = reinterpret_cast<const int32_t*>(base + ws.perm);
   a.xq = reinterpret_cast<const uint8_t*>(base + ws.xq);
   a.sx = reinterpret_cast<const float*>(base + ws.sx);
   a.h = reinterpret_cast<float*>(base + ws.h);

@@ -13,8 +13,10 @@
 // that scales its quantisation is taken afterwards, by the h-quantisation pass).  Down produces
 // y_e[token][m] for 128 output columns m.
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA loads into a ring of shared-memory
-// stages (128-byte swizzle, the layout the MMA descriptors name); warp 1 owns the TMEM
+// Warp roles (320 threads): warp 0 fills a ring of shared-memory stages (128-byte swizzle, the
+// layout the MMA descriptors name): lane 0 copies the weight tiles, and for gate/up the lanes
+// gather the tile's activation rows by token (TMA tile::gather4 on the token-order E4M3 rows,
+// so the activations are quantised once per token, not once per routed copy); warp 1 owns the TMEM
 // allocation and its lane 0 issues tcgen05.mma and tcgen05.commit (the commit frees a stage
 // when its MMAs have read it, and marks an accumulator ready after the last k-step); warps
 // 2-9 (two per TMEM lane quarter, each half of the token columns) read the accumulators
@@ -58,7 +60,9 @@ struct TcArgs {
   const uint8_t* wsh;  // the shared expert's, same layout
   const Tile* tiles;
   const int* n_tiles;
-  const float* sx;      // [R] activation scales (gate/up)
+  const int32_t* perm;  // [R] token of each row (gate/up gathers activation rows through it)
+  const uint8_t* xq;    // [T, d] E4M3 activations in token order (gate/up)
+  const float* sx;      // [T] activation scales, token order (gate/up)
   const float* sgu;     // [E, 2, F]
   const float* sh_sgu;  // [2, F]
   const float* sd;      // [E, d]
@@ -84,9 +88,14 @@ struct TcCtl {
 // kA accumulators of kN columns (gate/up: gate and up rows of the same 128 outputs; down:
 // 1 or 2 blocks of 128 output rows); a stage holds kC consecutive 128-byte k-chunks: the kA
 // weight tiles of each chunk (one contiguous copy for gate/up, one per block for down) and the
-// kN activation rows of those chunks (one 3-D tensor-map box).
+// kN activation rows of those chunks (gate/up: gathered by token, four rows per TMA gather;
+// down: one 3-D tensor-map box of h rows).
 template <int kN, bool kGateUp, int kA_, int kSplit_, int kC_>
 struct TcCfg {
+  // gate/up activation rows: wide tiles gather with per-lane cp.async (16 bytes each; TMA's
+  // cost per request makes 512-byte gathers slow at 128 rows per stage), narrow ones with
+  // TMA gather4
+  static constexpr bool kLdgsts = kGateUp && kN >= 64;
   static constexpr int kA = kA_;
   static constexpr int kSplit = kSplit_;  // CTAs (one cluster) sharing an item's k-steps
   static constexpr int kC = kC_;
@@ -127,7 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->full[s], C::kLdgsts ? 33 : 1);  // + one cp.async arrival per producer lane
       mbar_init(&ctl->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -176,46 +185,94 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t kCopyBytes = kGateUp ? 2 * kC * kATileBytes : kC * kATileBytes;  // per weight copy
   constexpr int kCopies = kGateUp ? 1 : kA;
 
-  if (warp == 0) {
-    if (lane == 0) {  // ------------------------------------------------ TMA producer
-      // Weights need nothing from the kernel this launch overlaps: pull this CTA's first
-      // items into L2 while that kernel runs (up to kPrefetchBytes), then wait for it.
+  if (warp == 0) {  // -------------------------------------------------- TMA producer warp
+    // Weights need nothing from the kernel this launch overlaps: pull this CTA's first items
+    // into L2 while that kernel runs (up to kPrefetchBytes), then wait for it.
+    if (lane == 0) {
       int budget = kPrefetchBytes;
       for (int item = unit; item < total && budget > 0; item += n_units) {
         const Tile tl = a.tiles[item / nblk];
         for (int ks = ks_lo; ks < ks_hi && budget > 0; ++ks, budget -= kCopies * int(kCopyBytes))
           for (int ai = 0; ai < kCopies; ++ai) prefetch_l2_bulk(w_src(tl, item % nblk, ai, ks * kC), kCopyBytes);
       }
-      pdl_begin();
-      const uint64_t pol = policy_evict_first();
-      int it = 0;
-      bool stop = false;
-      for (int item = unit; item < total && !stop; item += n_units) {
-        const Tile tl = a.tiles[item / nblk];
-        const int nb = item % nblk;
-        for (int ks = ks_lo; ks < ks_hi; ++ks, ++it) {
-          const int s = it % C::kStages, use = it / C::kStages;
-          if (!mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort)) {
-            report_timeout_flag(a.status_flags, 11);
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&ctl->full[s], C::kStageBytes);
+    }
+    pdl_begin();
+    // Lane 0 waits for a free stage and copies the weights; gate/up activation rows are
+    // gathered by token (perm) with tile::gather4, lane l bringing rows 4l..4l+3 of the tile
+    // (rows past the tile's end repeat its first token; their columns are never read).
+    // Down reads h rows, already in row order, as one 3-D box.
+    const uint64_t pol = policy_evict_first();
+    int it = 0;
+    bool stop = false;
+    for (int item = unit; item < total && !stop; item += n_units) {
+      const Tile tl = a.tiles[item / nblk];
+      const int nb = item % nblk;
+      // the tokens of this lane's rows: gather4 lanes own rows 4l..4l+3; cp.async lanes own
+      // 16-byte column l % 8 of rows l / 8 + 4j
+      constexpr int kG = C::kLdgsts ? kN / 4 : 4;
+      int g[kG];
+#pragma unroll
+      for (int i = 0; i < kG; ++i) g[i] = 0;
+      if (kGateUp) {
+        const int first = a.perm[tl.row0];
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+          const int r = C::kLdgsts ? (lane >> 3) + 4 * i : 4 * lane + i;
+          g[i] = (r < tl.nrows && (C::kLdgsts || 4 * lane < kN)) ? a.perm[tl.row0 + r] : first;
+        }
+      }
+      for (int ks = ks_lo; ks < ks_hi; ++ks, ++it) {
+        const int s = it % C::kStages, use = it / C::kStages;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&ctl->empty[s], (use & 1) ^ 1, &ctl->abort) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) report_timeout_flag(a.status_flags, 11);
+          stop = true;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&ctl->full[s], C::kLdgsts ? C::kABytes : C::kStageBytes);
 #pragma unroll
           for (int ai = 0; ai < kCopies; ++ai)
             bulk_g2s_stream(stage_a(s) + ai * kCopyBytes, w_src(tl, nb, ai, ks * kC), kCopyBytes, &ctl->full[s], pol);
-          tma_load_3d(stage_b(s), &map_x, 0, tl.row0, ks * kC, &ctl->full[s]);
+          if (!kGateUp) tma_load_3d(stage_b(s), &map_x, 0, tl.row0, ks * kC, &ctl->full[s]);
+        }
+        if (C::kLdgsts) {
+          // row r, 16-byte column cc of chunk c lands at (c kN + r) 128 + (cc ^ r % 8) 16: the
+          // 128-byte swizzle the MMA descriptor names
+          const int cc = lane & 7;
+#pragma unroll
+          for (int c = 0; c < kC; ++c) {
+            uint8_t* dst = stage_b(s) + c * kN * kKTile;
+            const size_t col = size_t(ks * kC + c) * kKTile + cc * 16;
+#pragma unroll
+            for (int i = 0; i < kG; ++i) {
+              const int r = (lane >> 3) + 4 * i;
+              cp_async16(dst + r * kKTile + ((cc ^ (r & 7)) << 4), a.xq + size_t(g[i]) * a.d + col);
+            }
+          }
+          cp_async_arrive_noinc(&ctl->full[s]);
+        } else if (kGateUp) {
+          __syncwarp();
+          if (4 * lane < kN) {
+#pragma unroll
+            for (int c = 0; c < kC; ++c)
+              tma_gather4(stage_b(s) + (c * kN + 4 * lane) * kKTile, &map_x, (ks * kC + c) * kKTile, g[0], g[1], g[2],
+                          g[3], &ctl->full[s]);
+          }
         }
       }
-      // wait for the loads still in flight (bounded, regardless of abort)
+    }
+    // wait for the loads still in flight (bounded, regardless of abort)
+    if (lane == 0) {
       for (int s = 0; s < C::kStages && s < it; ++s) {
         const int last_use = (it - 1 - s) / C::kStages;
         int zero = 0;
         mbar_wait(&ctl->full[s], last_use & 1, &zero);
       }
-    } else {
-      pdl_begin();
     }
+    __syncwarp();
   } else if (warp == 1) {
     pdl_begin();
     if (lane == 0) {  // ------------------------------------------------ MMA issuer
@@ -238,6 +295,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
+          if (C::kLdgsts) fence_proxy_async_smem();  // the activation rows were written by cp.async
 #pragma unroll
           for (int c = 0; c < kC; ++c) {
             const uint64_t db = sw128_desc(stage_b(s) + c * kN * kKTile);
@@ -329,7 +387,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           load_acc(0, c0, gv);
           load_acc(1, c0, uv);
           // lane i < 16 fetches the scale of token c0 + i; shuffles hand it to every lane
-          const float sx_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sx[tl.row0 + c0 + lane] : 0.0f;
+          const float sx_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sx[a.perm[tl.row0 + c0 + lane]] : 0.0f;
           float* hp = a.h + size_t(tl.row0 + c0) * a.F + n;
           if (c0 + 16 <= tl.nrows) {
 #pragma unroll
@@ -464,6 +522,8 @@ TcArgs tc_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.E = L.E;
   a.tiles = reinterpret_cast<const Tile*>(base + ws.tiles);
   a.n_tiles = reinterpret_cast<const int*>(base + ws.n_tiles);
+  a.perm = reinterpret_cast<const int32_t*>(base + ws.perm);
+  a.xq = reinterpret_cast<const uint8_t*>(base + ws.xq);
   a.sx = reinterpret_cast<const float*>(base + ws.sx);
   a.sgu = L.sgu;
   a.sh_sgu = L.sh_sgu;
@@ -499,8 +559,8 @@ cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char*
   const int kN = tc_rows_per_tile(T);
   const int KT = L.d / kKTile;
   const int kC = (kN <= kGateUpPairChunkMaxN && KT % 2 == 0) ? 2 : 1;
-  CUtensorMap mx;
-  if (!make_map_chunks(&mx, base + ws.xq, uint64_t(ws.R_alloc), L.d, kN, kC)) return cudaErrorInvalidValue;
+  CUtensorMap mx;  // activation rows in token order, gathered four rows at a time
+  if (!make_map_bytes(&mx, base + ws.xq, uint64_t(T), L.d, 1, 1)) return cudaErrorInvalidValue;
   TcArgs a = tc_args(L, ws, base);
   a.w = L.wgu;
   a.wsh = L.sh_wgu;

@@ -28,6 +28,29 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// TMA gather of four rows (tile::gather4): 128 bytes starting at byte column x of rows r0..r3
+// of a 2-D map whose box is {128 bytes, 1 row}, landing as four consecutive 128-byte rows at
+// smem_dst with the map's 128-byte swizzle (the swizzle follows the destination address, so
+// rows land as they would from a box load of the same rows).
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
+                                           int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The calling thread's cp.async copies issued so far arrive on `bar` when they complete; the
+// arrival is one of the barrier's expected arrivals (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Orders shared-memory writes made through the generic proxy (cp.async, st.shared) that this
+// thread has observed before its later async-proxy operations (tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gmem, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");

@@ -50,11 +50,11 @@ def test_workspace_bytes_on_host(lib):
     big = lib.moe_workspace_bytes(ctypes.byref(L), 16384)
     assert 0 < small < big
     # the largest buffers: the per-row expert outputs [7T, d] (bf16 for an E4M3 layer) and the
-    # E4M3 activation rows [7T, d]
-    assert big >= 7 * 16384 * 2048 * 3
+    # E4M3 activation rows [T, d] (token order)
+    assert big >= 7 * 16384 * 2048 * 2 + 16384 * 2048
     # an fp32 layer keeps fp32 expert outputs and fp32 activation rows
     big32 = lib.moe_workspace_bytes(ctypes.byref(_layer(binding, wdt=0)), 16384)
-    assert big32 >= 7 * 16384 * 2048 * 8
+    assert big32 >= 7 * 16384 * 2048 * 4 + 16384 * 2048 * 4
     assert lib.moe_workspace_bytes(ctypes.byref(_layer(binding, k=5)), 8) == 0
     assert lib.moe_workspace_bytes(None, 8) == 0
 
