@@ -37,7 +37,7 @@ ROUTER_BYTES = E * D * 4 + E * 4                         # fp32 router weights +
 GATEUP_EXPERT_BYTES = 2 * FFN * D + 2 * FFN * 4
 N_COPIES = 8
 HEADLINE_T = 64
-KERNELS_PER_FORWARD = 6  # router (selects, then dispatches in its last CTA), act_quant, gate_up, h_quant, down, combine (free routing, T <= 128)
+KERNELS_PER_FORWARD = 5  # router (quantises x, selects, then dispatches in its last CTA), gate_up, h_quant, down, combine (free routing, T <= 128)
 PATH_FLAGS = {"auto": 0, "stream": 1, "tc": 2}
 
 

@@ -106,15 +106,19 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   MOE_TRY(mark(0));
   bool selected = false;    // the decode and tensor-core routers select in-kernel under free routing
   bool dispatched = false;  // the decode router also dispatches then
+  bool quantised = false;   // the bf16 decode router also quantises the activations (E4M3 layers)
   if (!(forced_ids && forced_w)) {
     if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
       selected = !forced_ids;
       // under free routing the router's last selecting CTA also dispatches
       dispatched = selected && L.E < 512;
+      quantised = x_bf16 && L.fp8;
       DispatchOut dsp;
       dispatch_outputs(lay, base, counts, offsets, perm, pos, &dsp);
       MOE_TRY(launch_router_decode(x, x_bf16, T, L, logits, selected ? ids : nullptr, selected ? w : nullptr, st,
-                                   dispatched ? &dsp : nullptr, rows_per_tile, s));
+                                   dispatched ? &dsp : nullptr, rows_per_tile,
+                                   quantised ? reinterpret_cast<uint8_t*>(base + lay.xq) : nullptr,
+                                   quantised ? reinterpret_cast<float*>(base + lay.sx) : nullptr, s));
     } else if (T <= kRouterSmallMaxT && L.d <= 8192) {
       MOE_TRY(launch_router_small(x, x_bf16, T, L, logits, s));
     } else if (T > kRouterSmallMaxT && router_tc_supported(L, x_bf16)) {
@@ -130,7 +134,7 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   MOE_TRY(mark(2));
   if (!dispatched) MOE_TRY(launch_dispatch(ids, T, L.E, L.k, rows_per_tile, lay, base, counts, offsets, perm, pos, s));
   MOE_TRY(mark(3));
-  MOE_TRY(launch_act_quant(x, x_bf16, T, L, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
+  if (!quantised) MOE_TRY(launch_act_quant(x, x_bf16, T, L, base + lay.xq, reinterpret_cast<float*>(base + lay.sx), s));
   MOE_TRY(mark(4));
   MOE_TRY(use_tc ? launch_gateup_tc(L, T, lay, base, s) : launch_gateup_stream(L, T, lay, base, s));
   MOE_TRY(mark(5));
@@ -222,7 +226,7 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + lay.logits);
   DevStatus* st = reinterpret_cast<DevStatus*>(base + lay.status);
   if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
-    MOE_TRY(launch_router_decode(x, x_dtype == MOE_BF16, T, L, logits, ids_out, w_out, st, nullptr, 0, s));
+    MOE_TRY(launch_router_decode(x, x_dtype == MOE_BF16, T, L, logits, ids_out, w_out, st, nullptr, 0, nullptr, nullptr, s));
     return MOE_OK;
   } else if (T <= kRouterSmallMaxT && L.d <= 8192)
     MOE_TRY(launch_router_small(x, x_dtype == MOE_BF16, T, L, logits, s));

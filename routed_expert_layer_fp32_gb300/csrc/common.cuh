@@ -224,8 +224,11 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
 // ticket counters in st (zero between launches), and with dsp not NULL its last selecting CTA
 // also runs the dispatch (E < 512).
 struct DispatchOut;
+// With xq (bf16 x only) the router also writes the per-token E4M3 activations and scales
+// that launch_act_quant would.
 cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, int32_t* ids,
-                                 float* wts, DevStatus* st, const DispatchOut* dsp, int rows_per_tile, cudaStream_t s);
+                                 float* wts, DevStatus* st, const DispatchOut* dsp, int rows_per_tile, uint8_t* xq,
+                                 float* sx, cudaStream_t s);
 // Decode router (T <= kRouterSmallMaxT, d <= 8192): all of k per CTA, deterministic.
 cudaError_t launch_router_small(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, cudaStream_t s);
 

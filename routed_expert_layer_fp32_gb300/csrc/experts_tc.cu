@@ -55,7 +55,7 @@ constexpr int kSplitMaxT = 16;  // gate/up k-steps split over a CTA pair up to t
 constexpr int kGateUpPairChunkMaxN = 32;  // gate/up stages of two k-chunks up to this tile width
 
 struct TcArgs {
-  int d, F, E;
+  int d, F, E, T;
   const uint8_t* w;    // tiled weights of the routed experts (gate/up or down)
   const uint8_t* wsh;  // the shared expert's, same layout
   const Tile* tiles;
@@ -159,14 +159,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  // the tile list comes from the dispatch kernel, which completed before the kernel this
-  // launch overlaps started: readable before the dependency wait
-  const int n_tiles = *a.n_tiles;
+  // The tile list is read after the dependency wait: gate/up may directly follow the kernel
+  // that writes it (the decode router dispatches in its last CTA).  Down runs two kernels
+  // after any dispatch, so its prefetch may read the list before the wait.
   const int nblk = kGateUp ? a.F / kTileM : a.d / (kTileM * kA);  // items per tile
   const int KT = (kGateUp ? a.d : a.F) / kKTile;                  // 128-byte k-chunks per item
   const int KS = KT / kC;                                          // stages per item
   const int ks_lo = rank * KS / kSplit, ks_hi = (rank + 1) * KS / kSplit;  // this CTA's share
-  const int total = n_tiles * nblk;
+  int total = 0;                                                   // items, set after the wait
   const int nb_rows = (kGateUp ? a.F : a.d) / kTileM;              // 128-row blocks per expert
   auto stage_a = [&](int s) { return smem + size_t(s) * C::kStageBytes; };
   auto stage_b = [&](int s) { return smem + size_t(s) * C::kStageBytes + C::kABytes; };
@@ -187,16 +187,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {  // -------------------------------------------------- TMA producer warp
     // Weights need nothing from the kernel this launch overlaps: pull this CTA's first items
-    // into L2 while that kernel runs (up to kPrefetchBytes), then wait for it.
+    // into L2 while that kernel runs (up to kPrefetchBytes), then wait for it.  Gate/up knows
+    // only the shared expert's items before the wait (the list starts with its ceil(T / kN)
+    // tiles); down knows its whole list.
     if (lane == 0) {
       int budget = kPrefetchBytes;
-      for (int item = unit; item < total && budget > 0; item += n_units) {
-        const Tile tl = a.tiles[item / nblk];
+      const int known = kGateUp ? ((a.T + kN - 1) / kN) * nblk : *a.n_tiles * nblk;
+      for (int item = unit; item < known && budget > 0; item += n_units) {
+        const Tile tl = kGateUp ? Tile{a.E, 0, 0, 0} : a.tiles[item / nblk];
         for (int ks = ks_lo; ks < ks_hi && budget > 0; ++ks, budget -= kCopies * int(kCopyBytes))
           for (int ai = 0; ai < kCopies; ++ai) prefetch_l2_bulk(w_src(tl, item % nblk, ai, ks * kC), kCopyBytes);
       }
     }
     pdl_begin();
+    total = *a.n_tiles * nblk;
     // Lane 0 waits for a free stage and copies the weights; gate/up activation rows are
     // gathered by token (perm) with tile::gather4, lane l bringing rows 4l..4l+3 of the tile
     // (rows past the tile's end repeat its first token; their columns are never read).
@@ -275,6 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     pdl_begin();
+    total = *a.n_tiles * nblk;
     if (lane == 0) {  // ------------------------------------------------ MMA issuer
       constexpr uint32_t idesc = idesc_e4m3(kTileM, kN);
       int it = 0, jt = 0;
@@ -321,6 +326,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {  // ------------------------------------------------------------ epilogue
     pdl_begin();
+    total = *a.n_tiles * nblk;
     // warps 2..9: lane quarter q = warp % 4 (the TMEM lanes this warp may read), column half
     // ch = (warp - 2) / 4 of the kN token columns
     const int q = warp & 3, ch = (warp - 2) >> 2;
@@ -515,8 +521,9 @@ cudaError_t launch_down_n(int kN, int kA, int kC, const CUtensorMap& mx, const T
   return cudaErrorInvalidValue;
 }
 
-TcArgs tc_args(const LayerDev& L, const WsLayout& ws, char* base) {
+TcArgs tc_args(const LayerDev& L, int T, const WsLayout& ws, char* base) {
   TcArgs a;
+  a.T = T;
   a.d = L.d;
   a.F = L.F;
   a.E = L.E;
@@ -561,7 +568,7 @@ cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char*
   const int kC = (kN <= kGateUpPairChunkMaxN && KT % 2 == 0) ? 2 : 1;
   CUtensorMap mx;  // activation rows in token order, gathered four rows at a time
   if (!make_map_bytes(&mx, base + ws.xq, uint64_t(T), L.d, 1, 1)) return cudaErrorInvalidValue;
-  TcArgs a = tc_args(L, ws, base);
+  TcArgs a = tc_args(L, T, ws, base);
   a.w = L.wgu;
   a.wsh = L.sh_wgu;
   const long long items = max_tc_tiles(L, T, kN) * (L.F / kTileM);
@@ -581,7 +588,7 @@ cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* b
   const int kC = (kA == 1 && kN <= 32 && KT == 5) ? 5 : 1;
   CUtensorMap mx;
   if (!make_map_chunks(&mx, base + ws.qh, uint64_t(ws.R_alloc), L.F, kN, kC)) return cudaErrorInvalidValue;
-  TcArgs a = tc_args(L, ws, base);
+  TcArgs a = tc_args(L, T, ws, base);
   a.w = L.wd;
   a.wsh = L.sh_wd;
   const long long items = max_tc_tiles(L, T, kN) * (L.d / (kA * kTileM));

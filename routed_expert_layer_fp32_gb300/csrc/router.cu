@@ -250,6 +250,29 @@ __global__ void __launch_bounds__(512) k_router_small(const XT* __restrict__ x, 
 constexpr int kRdE = 16, kRdK = 256, kRdT = 64, kRdThreads = 256;
 static_assert(kRdThreads == kLeanWarps * 32, "the router's CTAs run the one-CTA dispatch");
 
+// Activation quantisation fused into the bf16 decode router: cluster x (expert group x) of a
+// token block quantises tokens [q_lo, q_hi) of it.  Each of its CTAs has the max |x| of those
+// tokens over its k-slice in amax_part; after the cluster barrier every CTA takes the max over
+// the cluster's slices (exact, in any order), forms the scale max/448 (1 for a zero row) and
+// writes the E4M3 codes of its own slice, as the stand-alone quantisation kernel does.
+struct XQuant {
+  const __nv_bfloat16* xs;  // this CTA's staged x slice [kRdT][xs_ld]
+  int xs_ld;
+  const float* amax_part;   // [q_hi - q_lo] partial max |x| of this CTA's slice
+  uint8_t* xq;              // [T, d] token order; nullptr: no fused quantisation
+  float* sx;                // [T]
+  int d, k0, q_lo, q_hi;
+};
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+}
+
 // Cluster rank r sums the n_slice partials of token sub-block r through distributed shared
 // memory in rank order (deterministic) and writes logits + bias.  With ids != NULL, the CTAs
 // that wrote token sub-block r of token block z then count themselves on a ticket; the last of
@@ -259,7 +282,8 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int T, int
                                                    const float* __restrict__ bias, const float* sel_bias, float* logits,
                                                    int k, int32_t* __restrict__ ids, float* __restrict__ wts,
                                                    int* tickets, int* dispatch_ticket, const DispatchOut& dsp,
-                                                   int rows_per_tile, int* scratch, int* last_flag) {
+                                                   int rows_per_tile, int* scratch, int* last_flag,
+                                                   const XQuant& xqz) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x;
@@ -278,6 +302,29 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int T, int
     for (int r = 0; r < 8; ++r)
       if (r < n_slice) sum += v[r];
     if (e0 + e < E) logits[size_t(t_base + t) * E + e0 + e] = sum + (bias ? bias[e0 + e] : 0.0f);
+  }
+  if (xqz.xq) {  // a warp per token, a lane per 8 columns of this CTA's 256
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int i = warp; i < xqz.q_hi - xqz.q_lo; i += kRdThreads / 32) {
+      float pm[8];  // all remote loads in flight at once
+#pragma unroll
+      for (int r = 0; r < 8; ++r) pm[r] = cluster.map_shared_rank(xqz.amax_part, min(r, n_slice - 1))[i];
+      float m = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) m = fmaxf(m, pm[r]);
+      const float s = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+      const int t = xqz.q_lo + i;
+      float v[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(xqz.xs + t * xqz.xs_ld + lane * 8), v);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; j += 2) {
+        lo |= uint32_t(e4m3_code2(__fdiv_rn(v[j], s), __fdiv_rn(v[j + 1], s))) << (8 * j);
+        hi |= uint32_t(e4m3_code2(__fdiv_rn(v[4 + j], s), __fdiv_rn(v[5 + j], s))) << (8 * j);
+      }
+      *reinterpret_cast<uint2*>(xqz.xq + size_t(t_base + t) * xqz.d + xqz.k0 + lane * 8) = make_uint2(lo, hi);
+      if (rank == 0 && lane == 0) xqz.sx[t_base + t] = s;
+    }
   }
   // this CTA is done reading its peers' partials; it waits for them to be done with its own
   // only before it exits
@@ -392,7 +439,7 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float
     part[(2 * tg + 1) * kRdE + eg + 8] = acc[1][1];
   }
   decode_router_tail(part, T, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, dispatch_ticket, dsp,
-                     rows_per_tile, reinterpret_cast<int*>(rd_smem), last_flag);
+                     rows_per_tile, reinterpret_cast<int*>(rd_smem), last_flag, XQuant{});
 }
 
 // bf16 x: tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).  Wr rows are split on
@@ -409,7 +456,8 @@ constexpr int kRmXLd = kRdK + 8;   // bf16 per staged x row: ldmatrix rows are c
 constexpr size_t kRmOffX = size_t(kRdE) * kRmWLd * 4;
 constexpr size_t kRmOffWpart = kRmOffX + size_t(kRdT) * kRmXLd * 2;
 constexpr size_t kRmOffPart = kRmOffWpart + size_t(kRdThreads / 32) * kRdT * kRmLd * 4;
-constexpr size_t kRdSmemBf16 = kRmOffPart + size_t(kRdT) * kRdE * 4 + 16;
+constexpr size_t kRmOffAmax = kRmOffPart + size_t(kRdT) * kRdE * 4;  // [kRdT] partial max |x| (fused quantisation)
+constexpr size_t kRdSmemBf16 = kRmOffAmax + size_t(kRdT) * 4 + 16;
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -444,13 +492,14 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv
                                                                    const float* sel_bias, float* logits, int k,
                                                                    int32_t* __restrict__ ids, float* __restrict__ wts,
                                                                    int* tickets, int* dispatch_ticket, DispatchOut dsp,
-                                                                   int rows_per_tile) {
+                                                                   int rows_per_tile, uint8_t* xq, float* sx) {
   extern __shared__ __align__(16) uint8_t rd_smem[];
   float* ws = reinterpret_cast<float*>(rd_smem);                                  // [kRdE][kRmWLd]
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(rd_smem + kRmOffX);        // [kRdT][kRmXLd]
   float* wpart = reinterpret_cast<float*>(rd_smem + kRmOffWpart);                  // [8 warps][kRdT][kRmLd]
   float* part = reinterpret_cast<float*>(rd_smem + kRmOffPart);                    // [kRdT][kRdE]
-  int* last_flag = reinterpret_cast<int*>(part + kRdT * kRdE);
+  float* amax_part = reinterpret_cast<float*>(rd_smem + kRmOffAmax);               // [kRdT]
+  int* last_flag = reinterpret_cast<int*>(amax_part + kRdT);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, q = lane & 3;
   const int e0 = blockIdx.x * kRdE, k0 = blockIdx.y * kRdK, t_base = blockIdx.z * kRdT;
@@ -526,8 +575,24 @@ __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_bf16(const __nv
     }
     *reinterpret_cast<float4*>(part + t * kRdE + c) = sum;
   }
+  // fused activation quantisation: this cluster's tokens, max |x| over this CTA's slice
+  XQuant xqz{xs, kRmXLd, amax_part, xq, sx, d, k0, 0, 0};
+  if (xq) {
+    const int tpc = (Tb + int(gridDim.x) - 1) / int(gridDim.x);
+    xqz.q_lo = min(Tb, int(blockIdx.x) * tpc);
+    xqz.q_hi = min(Tb, xqz.q_lo + tpc);
+    for (int i = warp; i < xqz.q_hi - xqz.q_lo; i += kRdThreads / 32) {
+      float v[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(xs + (xqz.q_lo + i) * kRmXLd + lane * 8), v);
+      float m = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+      m = warp_max(m);
+      if (lane == 0) amax_part[i] = m;
+    }
+  }
   decode_router_tail(part, T, Tb, E, bias, sel_bias, logits, k, ids, wts, tickets, dispatch_ticket, dsp,
-                     rows_per_tile, reinterpret_cast<int*>(rd_smem), last_flag);
+                     rows_per_tile, reinterpret_cast<int*>(rd_smem), last_flag, xqz);
 }
 
 // Prefill-sized router: SIMT tiled GEMM, 64 tokens x 64 experts per CTA, 4x4 per thread.
@@ -647,8 +712,10 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
 }
 
 cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, int32_t* ids,
-                                 float* wts, DevStatus* st, const DispatchOut* dsp, int rows_per_tile, cudaStream_t s) {
+                                 float* wts, DevStatus* st, const DispatchOut* dsp, int rows_per_tile, uint8_t* xq,
+                                 float* sx, cudaStream_t s) {
   if (T > kRouterSmallMaxT || L.d % kRdK || L.d / kRdK > 8) return cudaErrorInvalidValue;
+  if (xq && (!x_bf16 || !sx)) return cudaErrorInvalidValue;
   const int n_slice = L.d / kRdK;
   static cudaError_t attr = [] {
     cudaError_t e1 = cudaFuncSetAttribute(k_router_decode_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -677,7 +744,8 @@ cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerD
   if (d.counts && !(L.E < 512 && T <= kDispatchChunk)) return cudaErrorInvalidValue;
   if (x_bf16)
     return cudaLaunchKernelEx(&cfg, k_router_decode_bf16, (const __nv_bfloat16*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
-                              L.sel_bias(), logits, L.k, ids, wts, st->tickets, &st->dispatch_ticket, d, rows_per_tile);
+                              L.sel_bias(), logits, L.k, ids, wts, st->tickets, &st->dispatch_ticket, d, rows_per_tile,
+                              xq, sx);
   return cudaLaunchKernelEx(&cfg, k_router_decode_f32, (const float*)x, T, L.d, L.E, L.Wr, L.logit_bias(),
                             L.sel_bias(), logits, L.k, ids, wts, st->tickets, &st->dispatch_ticket, d, rows_per_tile);
 }

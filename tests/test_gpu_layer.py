@@ -312,6 +312,21 @@ def test_decode_layer(moe, kolibri, T, path):
     assert moe.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_back_to_back_forwards_see_their_own_routing(moe, kolibri, T):
+    """Forwards on one workspace with different inputs, launched back to back without a host
+    synchronisation: each must use its own routing (tile list, permutation) and its own
+    quantised activations, not the previous call's.  At decode the router writes both, and
+    the expert kernel that follows overlaps it (programmatic dependent launch)."""
+    w, L = kolibri
+    ws = moe.workspace(L, T)
+    xs = [g.make_x(200 + i, T, w.d, bf16=True) for i in range(3)]
+    outs = [moe.forward(to_dev_x(x), L, ws) for x in xs]
+    for i, (x, (y, ids, wt)) in enumerate(zip(xs, outs)):
+        check_free_layer(w, x, y, ids, wt, where=f"T={T} call {i}")
+    assert moe.get_status(ws) == 0
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_prefill_2048_free_then_4x512_forced(moe, kolibri, path):
     w, L = kolibri.w, kolibri.for_path(path)
