@@ -26,14 +26,25 @@ __device__ __forceinline__ int active_warps(int T) {
   return min(kWarps, (n + kTokensPerWarp - 1) / kTokensPerWarp);
 }
 
+// The chunk's ids, staged in shared memory with every load issued at once (the walks then
+// read shared memory, not one L2 round trip per step).  Returns the chunk's token count.
+__device__ __forceinline__ int stage_chunk_ids(const int32_t* ids, int T, int k, int* ids_s) {
+  const int c0 = blockIdx.x * kDispatchChunk;
+  const int n = min(T - c0, kDispatchChunk);
+  for (int i = threadIdx.x; i < n * k; i += blockDim.x) ids_s[i] = __ldcg(ids + size_t(c0) * k + i);
+  return n;
+}
+
+// smem: [kWarps][E] per-warp counters, then the chunk's ids [kDispatchChunk][k]
 __device__ void count_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, int32_t* chunk_row) {
   const int warp = threadIdx.x >> 5;
   const int nw = active_warps(T);
+  int* ids_s = wcnt + kWarps * E;
+  const int n = stage_chunk_ids(ids, T, k, ids_s);
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  const int t0 = blockIdx.x * kDispatchChunk + warp * kTokensPerWarp;
-  const int t1 = min(T, t0 + kTokensPerWarp);
-  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
+  const int t0 = min(n, warp * kTokensPerWarp), t1 = min(n, t0 + kTokensPerWarp);  // chunk-relative
+  warp_walk(ids_s, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
@@ -47,10 +58,16 @@ __device__ void scan_and_tiles(int T, int E, int k, int n_chunks, int rows_per_t
                                int* sm_a, int* warp_tot) {
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      int v = o.chunk_base[size_t(c) * E + e];
-      o.chunk_base[size_t(c) * E + e] = run;
-      run += v;
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {  // eight chunks' loads in flight at once
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < n_chunks ? o.chunk_base[size_t(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < n_chunks) {
+          o.chunk_base[size_t(c0 + j) * E + e] = run;
+          run += v[j];
+        }
     }
     sm_a[e] = run;
     o.counts[e] = run;
@@ -94,11 +111,13 @@ __device__ void scan_and_tiles(int T, int E, int k, int n_chunks, int rows_per_t
 __device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, const DispatchOut& o) {
   const int warp = threadIdx.x >> 5;
   const int nw = active_warps(T);
+  int* ids_s = wcnt + kWarps * E;
+  const int n = stage_chunk_ids(ids, T, k, ids_s);
+  const int cbase = blockIdx.x * kDispatchChunk;  // token index of the chunk's first token
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  const int t0 = blockIdx.x * kDispatchChunk + warp * kTokensPerWarp;
-  const int t1 = min(T, t0 + kTokensPerWarp);
-  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
+  const int t0 = min(n, warp * kTokensPerWarp), t1 = min(n, t0 + kTokensPerWarp);  // chunk-relative
+  warp_walk(ids_s, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = o.offsets[e] + o.chunk_base[size_t(blockIdx.x) * E + e];
@@ -114,12 +133,12 @@ __device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt
   // invalid slots (id < 0) get no row
   for (int i = (threadIdx.x & 31); i < (t1 - t0) * k; i += 32) {
     const int t = t0 + i / k;
-    const int e = ids[size_t(t) * k + (i % k)];
-    if (e < 0 || e >= E) pos[size_t(t) * k + (i % k)] = -1;
+    const int e = ids_s[t * k + (i % k)];
+    if (e < 0 || e >= E) pos[size_t(cbase + t) * k + (i % k)] = -1;
   }
-  warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [&](int t, int s, int row) {
-    perm[row] = t;
-    pos[size_t(t) * k + s] = row;
+  warp_walk(ids_s, t0, t1, k, E, wcnt + warp * E, [&](int t, int s, int row) {
+    perm[row] = cbase + t;
+    pos[size_t(cbase + t) * k + s] = row;
   });
   for (int t = blockIdx.x * kDispatchChunk + threadIdx.x; t < min(T, (blockIdx.x + 1) * kDispatchChunk); t += blockDim.x)
     perm[size_t(k) * T + t] = t;
@@ -187,12 +206,12 @@ cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_pe
                             int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos, cudaStream_t s) {
   DispatchOut o;
   dispatch_outputs(ws, base, counts, offsets, perm, pos, &o);
-  const size_t smem = size_t(kWarps) * E * sizeof(int);
+  const size_t smem = (size_t(kWarps) * E + size_t(kDispatchChunk) * k) * sizeof(int);
   const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
   // opt in once per process to the largest per-warp counter table (E <= kMaxExperts); later
   // calls (also inside a stream capture) only launch
   static cudaError_t attr = [] {
-    const int most = int(size_t(kWarps) * kMaxExperts * sizeof(int));
+    const int most = int((size_t(kWarps) * kMaxExperts + size_t(kDispatchChunk) * kTopK) * sizeof(int));
     cudaError_t e1 = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     cudaError_t e2 = cudaFuncSetAttribute(k_dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     cudaError_t e3 = cudaFuncSetAttribute(k_dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, most);

@@ -492,43 +492,58 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <typename OT, bool kResidual, typename YT>
 __global__ void __launch_bounds__(256) k_combine(const YT* __restrict__ y_rows, const int32_t* __restrict__ pos,
                                                  const float* __restrict__ w, int T, int d, int k, OT* __restrict__ out) {
-  const int t = blockIdx.x;
-  // the slots come from the dispatch, which completed before the kernel this launch overlaps
-  // started: read before the dependency wait
+  // A few CTAs per SM walk the tokens; a token's slots (rows and weights) are loaded while the
+  // previous token's rows are in flight.  The first token's slots come from the dispatch,
+  // which completed before the kernel this launch overlaps started: read before the wait.
   int rows[kTopK];
   float wt[kTopK];
+  auto load_slots = [&](int t, int (&r)[kTopK], float (&ww)[kTopK]) {
 #pragma unroll
-  for (int i = 0; i < kTopK; ++i) {
-    rows[i] = i < k ? pos[size_t(t) * k + i] : -1;
-    wt[i] = i < k ? w[size_t(t) * k + i] : 0.0f;
-  }
+    for (int i = 0; i < kTopK; ++i) {
+      const bool ok = t < T && i < k;
+      r[i] = ok ? pos[size_t(t) * k + i] : -1;
+      ww[i] = ok ? w[size_t(t) * k + i] : 0.0f;
+    }
+  };
+  int t = blockIdx.x;
+  load_slots(t, rows, wt);
   pdl_begin();
-  const YT* ysh = y_rows + (size_t(k) * T + t) * d;
-  for (int m = threadIdx.x * 8; m < d; m += blockDim.x * 8) {
-    float acc[8], v[kTopK][8];
-    load_row8(ysh + m, acc);
+  for (; t < T; t += gridDim.x) {
+    int nrows[kTopK];
+    float nwt[kTopK];
+    load_slots(t + int(gridDim.x), nrows, nwt);
+    const YT* ysh = y_rows + (size_t(k) * T + t) * d;
+    for (int m = threadIdx.x * 8; m < d; m += blockDim.x * 8) {
+      float acc[8], v[kTopK][8];
+      load_row8(ysh + m, acc);
 #pragma unroll
-    for (int i = 0; i < kTopK; ++i)
-      if (rows[i] >= 0) load_row8(y_rows + size_t(rows[i]) * d + m, v[i]);
+      for (int i = 0; i < kTopK; ++i)
+        if (rows[i] >= 0) load_row8(y_rows + size_t(rows[i]) * d + m, v[i]);
 #pragma unroll
-    for (int i = 0; i < kTopK; ++i)
-      if (rows[i] >= 0) {
+      for (int i = 0; i < kTopK; ++i)
+        if (rows[i] >= 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(wt[i], v[i][j], acc[j]);
+          for (int j = 0; j < 8; ++j) acc[j] = fmaf(wt[i], v[i][j], acc[j]);
+        }
+      OT* o = out + size_t(t) * d + m;
+      if constexpr (sizeof(OT) == 4) {
+        *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        if (kResidual) {
+          float r[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(o), r);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] += r[j];
+        }
+        *reinterpret_cast<uint4*>(o) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
       }
-    OT* o = out + size_t(t) * d + m;
-    if constexpr (sizeof(OT) == 4) {
-      *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    } else {
-      if (kResidual) {
-        float r[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(o), r);
+    }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] += r[j];
-      }
-      *reinterpret_cast<uint4*>(o) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    for (int i = 0; i < kTopK; ++i) {
+      rows[i] = nrows[i];
+      wt[i] = nwt[i];
     }
   }
 }
@@ -645,15 +660,18 @@ cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, cha
   return launch_pdl(k_down_f32, dim3(int(std::min<long long>(items, (long long)sms * 16))), dim3(256), 0, s, a);
 }
 
+constexpr int kCombineCtasPerSm = 3;  // 256 threads of ~74 registers
+
 template <typename YT>
 cudaError_t launch_combine_t(const YT* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
                              moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+  const dim3 grid(std::max(1, std::min(T, num_sms() * kCombineCtasPerSm)));
   if (y_dtype == MOE_F32)
-    return launch_pdl(k_combine<float, false, YT>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k, (float*)y);
+    return launch_pdl(k_combine<float, false, YT>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k, (float*)y);
   if (residual_add)
-    return launch_pdl(k_combine<__nv_bfloat16, true, YT>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+    return launch_pdl(k_combine<__nv_bfloat16, true, YT>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
                       (__nv_bfloat16*)y);
-  return launch_pdl(k_combine<__nv_bfloat16, false, YT>, dim3(T), dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+  return launch_pdl(k_combine<__nv_bfloat16, false, YT>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
                     (__nv_bfloat16*)y);
 }
 

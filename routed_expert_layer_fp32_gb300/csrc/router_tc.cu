@@ -12,7 +12,10 @@
 // (E = 384: 2 x 192) so one TMEM accumulator row holds a token's full logit row.  The two CTAs
 // of a cluster work on two token tiles in lockstep and share the weight stream: each loads one
 // n_half block of every (k-slice, term) weight stage and multicasts it to both, so each CTA
-// reads half of the 4.7 MB of weight terms per tile pair from L2.  The x k-slice (16 KB) has
+// reads half of the 4.7 MB of weight terms per tile pair from L2.  The split kernel writes the
+// terms already in stage order and in the 128-byte-swizzled shared-memory layout, so a block
+// (n_half rows x 128 bytes, 24 KB) is one contiguous bulk copy: on this GPU a row-strided
+// tensor-map box of the same size streams several times slower per SM.  The x k-slice (16 KB) has
 // its own ring and is loaded once for the three terms.  Warp roles as in the expert GEMMs
 // (TMA producer, single-thread MMA issuer, four epilogue warps); bounded waits.  A CTA whose
 // pair partner has a tile but it has none still loads and releases its weight halves.
@@ -23,22 +26,56 @@
 namespace moe {
 namespace {
 
-constexpr int kRtThreads = 192;
+constexpr int kRtEpiParts = 4;                       // epilogue warps per TMEM lane quarter
+constexpr int kRtEpiWarps = 4 * kRtEpiParts;
+constexpr int kRtThreads = (2 + kRtEpiWarps) * 32;
+// partial top-k lists of parts 1..3, merged by part 0: [part-1][token][slot] score, logit, id
+constexpr size_t kRtMergeBytes = size_t(kRtEpiParts - 1) * 128 * kTopK * 12;
 constexpr int kRtM = 128;
 constexpr int kRtATile = kRtM * 128;
 constexpr size_t kRtSmemBudget = 200 * 1024;
 
-__global__ void k_router_split_w(const float* __restrict__ Wr, long long n, __nv_bfloat16* __restrict__ out) {
+// Split layout: block ((kt * 3 + term) * 2 + h) holds term `term` of experts
+// [h n_half, (h + 1) n_half) over k = [64 kt, 64 kt + 64): n_half rows of 128 bytes, the 16-byte
+// chunk c of row r stored at chunk c ^ (r % 8) (the MMA's 128-byte swizzle).  A thread converts
+// one 8-element chunk of one expert row into its three terms.
+__device__ __forceinline__ size_t split_block_offset(int kt, int term, int h, int n_half) {
+  return (size_t(kt * 3 + term) * 2 + h) * size_t(n_half) * 128;
+}
+
+__global__ void k_router_split_w(const float* __restrict__ Wr, int E, int d, int n_half, uint8_t* __restrict__ out) {
   pdl_begin();
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const float w = Wr[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    out[i] = hi;
-    out[n + i] = mid;
-    out[2 * n + i] = __float2bfloat16_rn(r2);
+  const int chunks = d / 8;  // 16-byte chunks of bf16 per expert row
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)E * chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int e = int(i / chunks), q = int(i % chunks);
+    const int kt = q >> 3, c = q & 7, h = e / n_half, r = e % n_half;
+    const float4 a = *reinterpret_cast<const float4*>(Wr + size_t(e) * d + q * 8);
+    const float4 b = *reinterpret_cast<const float4*>(Wr + size_t(e) * d + q * 8 + 4);
+    const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t t3[3][4];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      uint32_t p[3] = {0, 0, 0};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float v = w[j + u];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const float r1 = v - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+        p[0] |= uint32_t(__bfloat16_as_ushort(hi)) << (16 * u);
+        p[1] |= uint32_t(__bfloat16_as_ushort(mid)) << (16 * u);
+        p[2] |= uint32_t(__bfloat16_as_ushort(lo)) << (16 * u);
+      }
+#pragma unroll
+      for (int term = 0; term < 3; ++term) t3[term][j >> 1] = p[term];
+    }
+    const size_t in_block = size_t(r) * 128 + size_t((c ^ (r & 7)) * 16);
+#pragma unroll
+    for (int term = 0; term < 3; ++term)
+      *reinterpret_cast<uint4*>(out + split_block_offset(kt, term, h, n_half) + in_block) =
+          make_uint4(t3[term][0], t3[term][1], t3[term][2], t3[term][3]);
   }
 }
 
@@ -55,10 +92,11 @@ struct RtCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
+  int epi_ok[2][4][kRtEpiParts];  // per tile parity: each epilogue warp's accumulator wait succeeded
 };
 
 __global__ void __launch_bounds__(kRtThreads, 1)
-    k_router_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+    k_router_tc(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ w_split,
                 const float* __restrict__ bias, const float* __restrict__ sel_bias, int T, int d, int E, int n_half,
                 int n_a, int n_b, int tmem_cols,
                 float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int k,
@@ -70,6 +108,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + size_t(n_a) * kRtATile;
   RtCtl* ctl = reinterpret_cast<RtCtl*>(ring_b + size_t(n_b) * b_stage_bytes);
+  uint8_t* merge = reinterpret_cast<uint8_t*>(ctl) + (sizeof(RtCtl) + 15) / 16 * 16;  // kRtMergeBytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = int(cluster_ctarank());
   const int pair = int(blockIdx.x) / kRtC, n_pairs = int(gridDim.x) / kRtC;
@@ -83,7 +122,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_init(&ctl->empty_b[s], kRtC);
     }
     mbar_init(&ctl->acc_full, 1);
-    mbar_init(&ctl->acc_empty, 4);
+    mbar_init(&ctl->acc_empty, kRtEpiWarps);
     mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
     mbar_fence_init();
@@ -134,7 +173,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&ctl->full_b[s], b_stage_bytes);  // both halves land here
-            tma_load_2d_mc(sb(s, rank), &map_w, kt * 64, term * E + rank * n_half, &ctl->full_b[s], kBoth);
+            bulk_g2s_mc(sb(s, rank), w_split + split_block_offset(kt, term, rank, n_half), uint32_t(b_half_bytes),
+                        &ctl->full_b[s], kBoth);
           }
         }
       }
@@ -204,21 +244,36 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_wait(&ctl->mma_done, 0, &zero);
     }
   } else {  // epilogue: one token per TMEM lane, logits = acc + bias
-    // With ids != nullptr the epilogue also selects: a sorted list of the kTopK best scores
-    // (larger first, lower index first on equal scores; the scan visits experts in increasing
-    // index, so an equal later score never displaces an earlier one), then the softmax over
-    // the selected logits, summed in slot order.  The score is the logit, plus sel_bias in the
-    // selection-only bias mode.
-    const int q = warp & 3;
+    // With ids != nullptr the epilogue also selects.  The four warps of a lane quarter each scan
+    // a quarter of the experts (consecutive 16-column chunks) and keep a sorted list of the
+    // kTopK best scores (larger first, lower index first on equal scores; a scan visits its
+    // experts in increasing index, so an equal later score never displaces an earlier one).
+    // A chunk whose best score is below the list's last is skipped whole.  Part 0 merges the
+    // four lists in that same order, then forms the softmax over the selected logits, summed
+    // in slot order.  The score is the logit, plus sel_bias in the selection-only bias mode.
+    const int q = warp & 3, part = (warp - 2) >> 2;
+    float* m_sc = reinterpret_cast<float*>(merge);                       // [3][128][kTopK]
+    float* m_lg = m_sc + (kRtEpiParts - 1) * 128 * kTopK;
+    int* m_id = reinterpret_cast<int*>(m_lg + (kRtEpiParts - 1) * 128 * kTopK);
+    const int n_chunks = (E + 15) / 16;
+    const int ch_lo = part * n_chunks / kRtEpiParts, ch_hi = (part + 1) * n_chunks / kRtEpiParts;
     int jt = 0;
     for (int j = 0; tile_of(j, rank) < n_items; ++j, ++jt) {
       const int item = tile_of(j, rank);
-      if (!mbar_wait(&ctl->acc_full, jt & 1, &ctl->abort)) {
-        if (lane == 0) report_timeout_flag(status_flags, 24);
+      // the four warps of a quarter meet at named barriers: they leave on a timeout together
+      const bool ok = mbar_wait(&ctl->acc_full, jt & 1, &ctl->abort);
+      if (lane == 0) ctl->epi_ok[jt & 1][q][part] = ok ? 1 : 0;
+      named_bar_sync(1 + q, kRtEpiParts * 32);
+      bool all_ok = true;
+#pragma unroll
+      for (int p2 = 0; p2 < kRtEpiParts; ++p2) all_ok = all_ok && ctl->epi_ok[jt & 1][q][p2] != 0;
+      if (!all_ok) {
+        if (lane == 0 && !ok) report_timeout_flag(status_flags, 24);
         break;
       }
       tc_fence_after();
-      const int t = item * kRtM + q * 32 + lane;
+      const int row = q * 32 + lane;
+      const int t = item * kRtM + row;
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16);
       float tv[kTopK], tl[kTopK];  // scores and their logits
       int ti[kTopK];
@@ -228,20 +283,28 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         tl[i] = -INFINITY;
         ti[i] = 0x7fffffff;
       }
-      for (int c0 = 0; c0 < 2 * n_half && c0 < E; c0 += 16) {
+      for (int ch = ch_lo; ch < ch_hi; ++ch) {
+        const int c0 = ch * 16;
         float v[16];
         tmem_ld16(taddr + c0, v);
         if (t < T) {
+          float sc[16];
+          float cmax = -INFINITY;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int e = c0 + i;
-            if (e < E) {
-              const float lg = v[i] + (bias ? bias[e] : 0.0f);
-              const float sc = sel_bias ? lg + sel_bias[e] : lg;
-              if (logits) logits[size_t(t) * E + e] = lg;
-              if (ids && (sc > tv[kTopK - 1] || (sc == tv[kTopK - 1] && e < ti[kTopK - 1]))) {
-                tv[kTopK - 1] = sc;
-                tl[kTopK - 1] = lg;
+            v[i] = e < E ? v[i] + (bias ? bias[e] : 0.0f) : -INFINITY;
+            sc[i] = (e < E && sel_bias) ? v[i] + sel_bias[e] : v[i];
+            if (logits && e < E) logits[size_t(t) * E + e] = v[i];
+            cmax = fmaxf(cmax, sc[i]);
+          }
+          if (ids && !(cmax < tv[kTopK - 1])) {  // some score of the chunk may enter the list
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int e = c0 + i;
+              if (e < E && (sc[i] > tv[kTopK - 1] || (sc[i] == tv[kTopK - 1] && e < ti[kTopK - 1]))) {
+                tv[kTopK - 1] = sc[i];
+                tl[kTopK - 1] = v[i];
                 ti[kTopK - 1] = e;
 #pragma unroll
                 for (int j2 = kTopK - 1; j2 > 0; --j2) {
@@ -262,28 +325,72 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           }
         }
       }
-      if (ids && t < T) {
-        float m = tl[0];  // the largest selected logit (slot 0 unless the bias reordered them)
-#pragma unroll
-        for (int i = 1; i < kTopK; ++i)
-          if (i < k) m = fmaxf(m, tl[i]);
-        float ex[kTopK], sum = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kTopK; ++i) {
-          ex[i] = i < k ? expf(tl[i] - m) : 0.0f;
-          sum += ex[i];
-        }
-#pragma unroll
-        for (int i = 0; i < kTopK; ++i) {
-          if (i < k) {
-            ids[size_t(t) * k + i] = ti[i];
-            wts[size_t(t) * k + i] = ex[i] / sum;
-          }
-        }
-      }
+      // the accumulator is free for the next tile once every warp has read its columns
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->acc_empty);
+      if (ids) {  // (every warp of the quarter takes the same branches to both barriers)
+        if (part > 0) {
+#pragma unroll
+          for (int i = 0; i < kTopK; ++i) {
+            const int o = ((part - 1) * 128 + row) * kTopK + i;
+            m_sc[o] = tv[i];
+            m_lg[o] = tl[i];
+            m_id[o] = ti[i];
+          }
+        }
+        named_bar_sync(1 + q, kRtEpiParts * 32);  // the quarter's lists are written
+        if (part == 0) {
+          // merge parts 1..3 into this list, one candidate at a time, with the scan's order
+          for (int p2 = 1; p2 < kRtEpiParts; ++p2) {
+#pragma unroll
+            for (int i = 0; i < kTopK; ++i) {
+              const int o = ((p2 - 1) * 128 + row) * kTopK + i;
+              const float s = m_sc[o], lgv = m_lg[o];
+              const int e = m_id[o];
+              if (s > tv[kTopK - 1] || (s == tv[kTopK - 1] && e < ti[kTopK - 1])) {
+                tv[kTopK - 1] = s;
+                tl[kTopK - 1] = lgv;
+                ti[kTopK - 1] = e;
+#pragma unroll
+                for (int j2 = kTopK - 1; j2 > 0; --j2) {
+                  if (tv[j2] > tv[j2 - 1] || (tv[j2] == tv[j2 - 1] && ti[j2] < ti[j2 - 1])) {
+                    const float fv = tv[j2];
+                    tv[j2] = tv[j2 - 1];
+                    tv[j2 - 1] = fv;
+                    const float fl = tl[j2];
+                    tl[j2] = tl[j2 - 1];
+                    tl[j2 - 1] = fl;
+                    const int fi = ti[j2];
+                    ti[j2] = ti[j2 - 1];
+                    ti[j2 - 1] = fi;
+                  }
+                }
+              }
+            }
+          }
+          if (t < T) {
+            float m = tl[0];  // the largest selected logit (slot 0 unless the bias reordered them)
+#pragma unroll
+            for (int i = 1; i < kTopK; ++i)
+              if (i < k) m = fmaxf(m, tl[i]);
+            float ex[kTopK], sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kTopK; ++i) {
+              ex[i] = i < k ? expf(tl[i] - m) : 0.0f;
+              sum += ex[i];
+            }
+#pragma unroll
+            for (int i = 0; i < kTopK; ++i) {
+              if (i < k) {
+                ids[size_t(t) * k + i] = ti[i];
+                wts[size_t(t) * k + i] = ex[i] / sum;
+              }
+            }
+          }
+        }
+        named_bar_sync(1 + q, kRtEpiParts * 32);  // the merge buffer may be written again
+      }
     }
   }
   tc_fence_before();
@@ -314,22 +421,22 @@ bool router_tc_supported(const LayerDev& L, bool x_bf16) {
 
 cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, int32_t* ids,
                              float* wts, DevStatus* st, cudaStream_t s) {
-  const long long n = (long long)L.E * L.d;
+  const int n_half = L.E / 2;  // E % 32 == 0: two halves of a multiple of 16 experts
+  const long long n = (long long)L.E * (L.d / 8);
   cudaError_t e = launch_pdl(k_router_split_w, dim3(int(std::min<long long>((n + 255) / 256, 4096))), dim3(256), 0, s,
-                             L.Wr, n, w3);
+                             L.Wr, L.E, L.d, n_half, reinterpret_cast<uint8_t*>(w3));
   if (e != cudaSuccess) return e;
-  const int n_half = ((L.E / 2) + 15) / 16 * 16;
   const int b_stage_bytes = 2 * n_half * 128;
   // rings: x slices and weight stages, as many of each as fit (at most kRtMaxStages)
   int n_b = int(std::min<size_t>(kRtMaxStages, (kRtSmemBudget - 2 * size_t(kRtATile)) / b_stage_bytes));
   int n_a = int(std::min<size_t>(kRtMaxStages, (kRtSmemBudget - size_t(n_b) * b_stage_bytes) / kRtATile));
   if (n_b < 1 || n_a < 2) return cudaErrorInvalidValue;
   const int tmem_cols = 2 * n_half <= 256 ? 256 : 512;
-  CUtensorMap mx, mw;
-  if (!make_map_bytes(&mx, x, uint64_t(T), uint64_t(L.d), kRtM, 2) ||
-      !make_map_bytes(&mw, w3, uint64_t(3) * L.E, uint64_t(L.d), uint32_t(n_half), 2))
-    return cudaErrorInvalidValue;
-  const size_t smem = size_t(n_a) * kRtATile + size_t(n_b) * b_stage_bytes + 1024 + sizeof(RtCtl);
+  CUtensorMap mx;
+  if (!make_map_bytes(&mx, x, uint64_t(T), uint64_t(L.d), kRtM, 2)) return cudaErrorInvalidValue;
+  const size_t smem =
+      size_t(n_a) * kRtATile + size_t(n_b) * b_stage_bytes + 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
   static cudaError_t attr = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   if (attr != cudaSuccess) return attr;
   const int items = (T + kRtM - 1) / kRtM;
@@ -348,7 +455,7 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_router_tc, mx, mw, L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half, n_a, n_b,
+  return cudaLaunchKernelEx(&cfg, k_router_tc, mx, static_cast<const uint8_t*>(static_cast<const void*>(w3)), L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half, n_a, n_b,
                             tmem_cols, logits, ids, wts, L.k, &st->flags);
 }
 
