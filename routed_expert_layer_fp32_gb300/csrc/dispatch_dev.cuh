@@ -74,13 +74,17 @@ struct DispatchOut {
 // grid); warp w owns the run of tokens [w*tpw, (w+1)*tpw); per-warp counts become per-warp
 // row bases by a prefix over the warps, then over the experts.
 constexpr int kLeanWarps = 8;
-__host__ __device__ constexpr int lean_dispatch_smem_ints(int T, int E, int k) { return kLeanWarps * E + E + 1 + T * k + 33; }
+__host__ __device__ constexpr int lean_dispatch_smem_ints(int T, int E, int k) {
+  return kLeanWarps * E + 3 * (E + 1) + T * k + 33;
+}
 
 __device__ __forceinline__ void dispatch_lean_body(const int32_t* ids_g, int T, int E, int k, int rows_per_tile,
                                                    const DispatchOut& o, int* smem) {
   int* wcnt = smem;                  // [kLeanWarps][E]
-  int* tot = smem + kLeanWarps * E;  // [E + 1]
-  int* ids = tot + E + 1;            // [T * k], the staged ids
+  int* tot = smem + kLeanWarps * E;  // [E + 1] counts, then offsets
+  int* cnt = tot + E + 1;            // [E + 1] counts (the tile list reads them here, not back from global)
+  int* ntile = cnt + E + 1;          // [E + 1] tiles per group (shared expert first), then their prefix
+  int* ids = ntile + E + 1;          // [T * k], the staged ids
   int* warp_tot = ids + T * k;       // [33]
   const int warp = threadIdx.x >> 5;
   const int tpw = (T + kLeanWarps - 1) / kLeanWarps;
@@ -98,6 +102,7 @@ __device__ __forceinline__ void dispatch_lean_body(const int32_t* ids_g, int T, 
       run += v;
     }
     tot[e] = run;
+    cnt[e] = run;
     o.counts[e] = run;
   }
   __syncthreads();
@@ -113,18 +118,17 @@ __device__ __forceinline__ void dispatch_lean_body(const int32_t* ids_g, int T, 
   }
   __syncthreads();
   // tile list, shared expert first: tile counts per group, scanned
-  int* ntile = tot;  // reused: [E + 1] tiles per group (shared expert first)
   for (int q = threadIdx.x; q <= E; q += blockDim.x) {
     const int g = q == 0 ? E : q - 1;
-    const int c = g == E ? T : o.counts[g];
+    const int c = g == E ? T : cnt[g];
     ntile[q] = (c + rows_per_tile - 1) / rows_per_tile;
   }
   __syncthreads();
   const int total_tiles = block_exclusive_scan(ntile, E + 1, warp_tot);
   for (int q = threadIdx.x; q <= E; q += blockDim.x) {
     const int g = q == 0 ? E : q - 1;
-    const int c = g == E ? T : o.counts[g];
-    const int base_row = g == E ? k * T : o.offsets[g];
+    const int c = g == E ? T : cnt[g];
+    const int base_row = g == E ? k * T : tot[g];
     int ti = ntile[q];
     for (int r = 0; r < c; r += rows_per_tile, ++ti) {
       Tile tl;

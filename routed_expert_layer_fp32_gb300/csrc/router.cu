@@ -270,6 +270,8 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int T, int
 // issued up front; thread = 2 experts x 2 tokens, one sequential fp32 sum over the slice.
 constexpr int kRdLd = kRdK + 4;
 constexpr size_t kRdSmemF32 = size_t(kRdE + kRdT) * kRdLd * 4 + size_t(kRdT) * kRdE * 4 + 16;
+static_assert(size_t(lean_dispatch_smem_ints(kRouterSmallMaxT, 511, kTopK)) * 4 <= size_t(kRdE + kRdT) * kRdLd * 4,
+              "dispatch scratch");
 __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float* __restrict__ x, int T, int d, int E,
                                                                   const float* __restrict__ Wr,
                                                                   const float* __restrict__ bias,
@@ -357,6 +359,9 @@ constexpr size_t kRmOffX = size_t(kRdE) * kRmWLd * 4;
 constexpr size_t kRmOffWpart = kRmOffX + size_t(kRdT) * kRmXLd * 2;
 constexpr size_t kRmOffPart = kRmOffWpart + size_t(kRdThreads / 32) * kRdT * kRmLd * 4;
 constexpr size_t kRmOffAmax = kRmOffPart + size_t(kRdT) * kRdE * 4;  // [kRdT] partial max |x| (fused quantisation)
+// the dispatching CTA's scratch (T <= 128, E < 512) overlays the Wr and x staging only: the
+// partials after them may still be read by the cluster's other CTAs
+static_assert(size_t(lean_dispatch_smem_ints(kRouterSmallMaxT, 511, kTopK)) * 4 <= kRmOffWpart, "dispatch scratch");
 constexpr size_t kRdSmemBf16 = kRmOffAmax + size_t(kRdT) * 4 + 16;
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
