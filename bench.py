@@ -182,9 +182,10 @@ def layer_bytes(ids: np.ndarray, T: int):
 
 def gateup_bytes(U: int, T: int):
     """Algorithmic bytes of one gate/up launch: the used experts' gate/up codes and scales,
-    the E4M3 activation rows once, h written once in fp32."""
+    each token's E4M3 activation row once (the kernel gathers a token's routed copies by
+    token), h written once in fp32 for every (token, slot) and shared row."""
     R = (K + 1) * T
-    return (U + 1) * GATEUP_EXPERT_BYTES + R * D + R * FFN * 4
+    return (U + 1) * GATEUP_EXPERT_BYTES + T * D + R * FFN * 4
 
 
 # ------------------------------------------------------------------------------ ours ------
