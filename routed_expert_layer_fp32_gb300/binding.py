@@ -255,6 +255,36 @@ def forward(x: torch.Tensor, layer: Layer, ws: torch.Tensor, forced_ids=None, fo
     return y, ids, w
 
 
+class GraphedForward:
+    """One forward step on fixed buffers, captured once as a CUDA graph and replayed with one
+    launch: optionally the copy of x from pinned host memory, the layer's kernels, optionally
+    the copy of y back to pinned host memory.  For serving loops, where issuing the step's
+    launches from the host one by one costs more than the layer at decode sizes.  The buffers
+    (and their contents' shapes) are those given here; write new inputs into `x_host` (or
+    `x`) before each replay()."""
+
+    def __init__(self, x: torch.Tensor, layer: Layer, ws: torch.Tensor, out: torch.Tensor, ids: torch.Tensor,
+                 w: torch.Tensor, flags: int = PATH_AUTO, x_host: Optional[torch.Tensor] = None,
+                 y_host: Optional[torch.Tensor] = None):
+        self.buffers = (x, layer, ws, out, ids, w, x_host, y_host)  # kept alive with the graph
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # one plain call first: one-time attribute setup is not captured
+            forward(x, layer, ws, out=out, ids=ids, w=w, flags=flags)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            if x_host is not None:
+                x.copy_(x_host, non_blocking=True)
+            forward(x, layer, ws, out=out, ids=ids, w=w, flags=flags)
+            if y_host is not None:
+                y_host.copy_(out, non_blocking=True)
+
+    def replay(self):
+        self.graph.replay()
+
+
 def layer_array(layers: Sequence[Layer]):
     arr = (MoeLayerC * len(layers))(*[l.c for l in layers])
     return arr

@@ -347,6 +347,46 @@ def test_prefill_2048_free_then_4x512_forced(moe, kolibri, path):
     check_forced_layer(w, x, ids.cpu().numpy(), None, ych, ids, where="prefill 4x512 forced")
 
 
+@pytest.mark.parametrize("T", [1, 64])
+def test_graphed_forward_matches_the_call(moe, kolibri, T):
+    """GraphedForward replays (pinned host x -> device, the layer, y -> pinned host) and gives
+    what the plain call gives, bit for bit, for new inputs written between replays."""
+    w, L = kolibri
+    ws = moe.workspace(L, T)
+    x_pin = torch.empty((T, w.d), dtype=torch.bfloat16).pin_memory()
+    y_pin = torch.empty((T, w.d), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty((T, w.d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((T, w.d), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T, 6), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, 6), dtype=torch.float32, device="cuda")
+    step = moe.GraphedForward(xd, L, ws, y, ids, wt, x_host=x_pin, y_host=y_pin)
+    for seed in (401, 402):
+        x = g.make_x(seed, T, w.d, bf16=True)
+        x_pin.copy_(torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16))
+        step.replay()
+        torch.cuda.synchronize()
+        y_ref, ids_ref, w_ref = moe.forward(to_dev_x(x), L, moe.workspace(L, T), y_dtype=torch.bfloat16)
+        assert torch.equal(ids, ids_ref) and torch.equal(wt, w_ref)
+        assert torch.equal(y_pin.view(torch.int16), y_ref.cpu().view(torch.int16))
+    assert moe.get_status(ws) == 0
+
+
+@pytest.mark.parametrize("T", [8192, 9001])
+def test_large_prefill_sampled_rows(moe, kolibri, T):
+    """Large prefill (128-token tiles, ragged at T = 9001): free routing, 64 sampled rows
+    against the oracle run with the GPU's ids forced (every token is independent, so a row
+    sample is exact for those rows)."""
+    w, L = kolibri
+    x = g.make_x(300 + T, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+    rows = np.sort(np.random.default_rng(T).choice(T, 64, replace=False))
+    ref = o.layer_forward(o.Layer(w), x[rows], forced_ids=ids.cpu().numpy()[rows], nthreads=o.default_threads())
+    ok, msg = parity.outputs_ok(y.cpu().numpy()[rows], ref["y"])
+    assert ok, f"T={T}: {msg}"
+    assert moe.get_status(ws) == 0
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_batched_decode_zipf_forced(moe, kolibri, path):
     w, L = kolibri.w, kolibri.for_path(path)
