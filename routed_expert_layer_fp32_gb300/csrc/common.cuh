@@ -158,6 +158,16 @@ __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Lets the next kernel launch first, then waits.  Only for a kernel whose successor reads,
+// before its own wait, nothing this kernel's predecessor may still be writing: the successor
+// may then start while that predecessor runs (k_hquant: down's CTAs take the SMs as gate/up's
+// retire and pull their first weights into L2; down's tile list was final before gate/up
+// passed its wait).
+__device__ __forceinline__ void pdl_trigger_then_wait() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(DevStatus* st, int flag) { atomicOr(&st->flags, flag); }
 
 // Record a device-side timeout: flags |= kFlagTimeout, and the first site that gave up.

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
 // Rows are taken in order 0..R-1; rows that no tile covers (slots of rejected forced ids)
 // are quantised too, harmlessly: nothing reads them.
 __global__ void __launch_bounds__(256) k_hquant(ExpertArgs a, int R) {
-  pdl_begin();
+  pdl_trigger_then_wait();
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long row_l = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row_l < R; row_l += nwarps) {

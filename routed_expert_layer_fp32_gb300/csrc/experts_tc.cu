@@ -160,8 +160,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
 
   // The tile list is read after the dependency wait: gate/up may directly follow the kernel
-  // that writes it (the decode router dispatches in its last CTA).  Down runs two kernels
-  // after any dispatch, so its prefetch may read the list before the wait.
+  // that writes it (the decode router dispatches in its last CTA).  Down launches only once
+  // gate/up has passed its own wait (the h-quantisation kernel between them lets down launch
+  // early, while gate/up still runs), so the list is final and down's prefetch may read it
+  // before its wait.
   const int nblk = kGateUp ? a.F / kTileM : a.d / (kTileM * kA);  // items per tile
   const int KT = (kGateUp ? a.d : a.F) / kKTile;                  // 128-byte k-chunks per item
   const int KS = KT / kC;                                          // stages per item
