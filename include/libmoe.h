@@ -49,7 +49,7 @@ typedef struct CUevent_st* moe_event_t;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad dtype or shape */
-  MOE_ERR_UNSUPPORTED = -2,   /* valid request this build does not implement (e.g. k != 6) */
+  MOE_ERR_UNSUPPORTED = -2,   /* valid request this library does not implement (e.g. k != 6) */
   MOE_ERR_WORKSPACE = -3,     /* ws_bytes < moe_workspace_bytes() */
   MOE_ERR_BAD_FORCED_ID = -4, /* a forced id was out of range or repeated within a token */
   MOE_ERR_TIMEOUT = -5,       /* a device-side wait gave up */

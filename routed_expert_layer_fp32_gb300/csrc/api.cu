@@ -329,7 +329,7 @@ const char* moe_status_string(moe_status status) {
   switch (status) {
     case MOE_OK: return "ok";
     case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad dtype or shape)";
-    case MOE_ERR_UNSUPPORTED: return "unsupported by this build (e.g. top_k != 6)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported by this library (e.g. top_k != 6)";
     case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_bytes()";
     case MOE_ERR_BAD_FORCED_ID: return "a forced expert id was out of range or repeated within a token";
     case MOE_ERR_TIMEOUT: return "a device-side wait timed out";
