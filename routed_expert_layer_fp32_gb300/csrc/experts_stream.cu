@@ -45,31 +45,28 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
 template <typename XT, bool kFp8>
 __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int T, int d, void* __restrict__ xq,
                                                    float* __restrict__ sx) {
-  // x was written before the kernel this launch overlaps started: its scale is found before
-  // the dependency wait; the stores wait (the previous layer's expert kernels read xq)
-  __shared__ float red[8];
-  const int t = blockIdx.x;
-  const XT* xr = x + size_t(t) * d;
+  // A warp per token, eight tokens per CTA: a lane's loads of the row are all in flight at
+  // once and the maximum is a warp reduction.  x was written before the kernel this launch
+  // overlaps started: its scale is found before the dependency wait; the stores wait (the
+  // previous layer's expert kernels read xq).
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const bool live = t < T;
+  const XT* xr = x + size_t(live ? t : 0) * d;
   float amax = 0.0f;
-  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+#pragma unroll 8
+  for (int c = lane * 8; c < d; c += 256) {
     float v[8];
     load8(xr + c, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
   }
   amax = warp_max(amax);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-    m = warp_max(m);
-    if (threadIdx.x == 0) red[0] = m;
-  }
-  __syncthreads();
-  amax = red[0];
   const float s = kFp8 ? (amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f) : 1.0f;
   pdl_begin();
-  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+  if (!live) return;
+#pragma unroll 8
+  for (int c = lane * 8; c < d; c += 256) {
     float v[8];
     load8(xr + c, v);
     if (kFp8) {
@@ -86,7 +83,7 @@ __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int
       *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
     }
   }
-  if (threadIdx.x == 0) sx[t] = s;
+  if (lane == 0) sx[t] = s;
 }
 
 // ------------------------------------------------------------ gate/up, FP8 -----------------
@@ -489,8 +486,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <typename OT, bool kResidual, typename YT>
-__global__ void __launch_bounds__(256) k_combine(const YT* __restrict__ y_rows, const int32_t* __restrict__ pos,
+// kMinCtas: CTAs per SM the register budget allows (4 for many tokens per CTA, where the
+// extra CTA hides more latency; 3 otherwise, without the spills the 64-register cap costs)
+template <typename OT, bool kResidual, typename YT, int kMinCtas>
+__global__ void __launch_bounds__(256, kMinCtas) k_combine(const YT* __restrict__ y_rows, const int32_t* __restrict__ pos,
                                                  const float* __restrict__ w, int T, int d, int k, OT* __restrict__ out) {
   // A few CTAs per SM walk the tokens; a token's slots (rows and weights) are loaded while the
   // previous token's rows are in flight.  The first token's slots come from the dispatch,
@@ -568,15 +567,14 @@ int num_sms() {
 
 cudaError_t launch_act_quant(const void* x, bool x_bf16, int T, const LayerDev& L, void* xq, float* sx,
                              cudaStream_t s) {
+  const dim3 grid((T + 7) / 8);  // a warp per token
   if (x_bf16) {
     if (L.fp8)
-      return launch_pdl(k_act_quant<__nv_bfloat16, true>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, xq,
-                        sx);
-    return launch_pdl(k_act_quant<__nv_bfloat16, false>, dim3(T), dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, xq,
-                      sx);
+      return launch_pdl(k_act_quant<__nv_bfloat16, true>, grid, dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, xq, sx);
+    return launch_pdl(k_act_quant<__nv_bfloat16, false>, grid, dim3(256), 0, s, (const __nv_bfloat16*)x, T, L.d, xq, sx);
   }
-  if (L.fp8) return launch_pdl(k_act_quant<float, true>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, xq, sx);
-  return launch_pdl(k_act_quant<float, false>, dim3(T), dim3(256), 0, s, (const float*)x, T, L.d, xq, sx);
+  if (L.fp8) return launch_pdl(k_act_quant<float, true>, grid, dim3(256), 0, s, (const float*)x, T, L.d, xq, sx);
+  return launch_pdl(k_act_quant<float, false>, grid, dim3(256), 0, s, (const float*)x, T, L.d, xq, sx);
 }
 
 namespace {
@@ -660,19 +658,26 @@ cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, cha
   return launch_pdl(k_down_f32, dim3(int(std::min<long long>(items, (long long)sms * 16))), dim3(256), 0, s, a);
 }
 
-constexpr int kCombineCtasPerSm = 3;  // 256 threads of ~74 registers
+template <typename YT, int kMinCtas>
+cudaError_t launch_combine_k(const YT* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
+                             moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+  const dim3 grid(std::max(1, std::min(T, num_sms() * kMinCtas)));
+  if (y_dtype == MOE_F32)
+    return launch_pdl(k_combine<float, false, YT, kMinCtas>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+                      (float*)y);
+  if (residual_add)
+    return launch_pdl(k_combine<__nv_bfloat16, true, YT, kMinCtas>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d,
+                      L.k, (__nv_bfloat16*)y);
+  return launch_pdl(k_combine<__nv_bfloat16, false, YT, kMinCtas>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
+                    (__nv_bfloat16*)y);
+}
 
 template <typename YT>
 cudaError_t launch_combine_t(const YT* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
                              moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
-  const dim3 grid(std::max(1, std::min(T, num_sms() * kCombineCtasPerSm)));
-  if (y_dtype == MOE_F32)
-    return launch_pdl(k_combine<float, false, YT>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k, (float*)y);
-  if (residual_add)
-    return launch_pdl(k_combine<__nv_bfloat16, true, YT>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
-                      (__nv_bfloat16*)y);
-  return launch_pdl(k_combine<__nv_bfloat16, false, YT>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
-                    (__nv_bfloat16*)y);
+  if (T > num_sms() * 8)  // CTAs walk several tokens each
+    return launch_combine_k<YT, 4>(y_rows, pos, w, T, L, y, y_dtype, residual_add, s);
+  return launch_combine_k<YT, 3>(y_rows, pos, w, T, L, y, y_dtype, residual_add, s);
 }
 
 cudaError_t launch_combine(const void* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
