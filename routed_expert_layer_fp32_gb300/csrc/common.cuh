@@ -41,7 +41,8 @@ struct WsLayout {
   int T, R, R_alloc, n_chunks, max_tiles;
 };
 
-constexpr int kDispatchChunk = 1024;  // tokens per dispatch CTA
+constexpr int kDispatchChunk = 1024;  // up to this many tokens the dispatch is one CTA
+constexpr int kScatterChunk = 256;    // tokens per CTA of the multi-CTA dispatch
 constexpr int kRouterSmallMaxT = 128;  // up to this many tokens the decode router runs
 constexpr int kStreamRows = 16;        // rows per tile on the streaming path
 
@@ -55,7 +56,7 @@ inline WsLayout ws_layout(const moe_layer& L, int T) {
   w.T = T;
   w.R = int(R);
   w.R_alloc = int(R) + 256;  // row padding: tensor-map boxes of up to 256 rows stay inside the buffers
-  w.n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  w.n_chunks = (T + kScatterChunk - 1) / kScatterChunk;
   w.max_tiles = int(R / 8 + 2 * (E + 1) + 8);  // tiles of >= 8 rows or a group's tail
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };

@@ -15,27 +15,27 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 32;  // warps per dispatch CTA (1024 threads)
-constexpr int kTokensPerWarp = kDispatchChunk / kWarps;
+constexpr int kWarps = 8;  // warps per chunk CTA (256 threads)
+constexpr int kTokensPerWarp = kScatterChunk / kWarps;
 
 
 // Phase 1 (per CTA): per-warp counts of the chunk -> chunk totals [chunk][e].
 // Warps of this CTA that own tokens (the rest skip every per-warp loop).
 __device__ __forceinline__ int active_warps(int T) {
-  const int n = min(T - int(blockIdx.x) * kDispatchChunk, kDispatchChunk);
+  const int n = min(T - int(blockIdx.x) * kScatterChunk, kScatterChunk);
   return min(kWarps, (n + kTokensPerWarp - 1) / kTokensPerWarp);
 }
 
 // The chunk's ids, staged in shared memory with every load issued at once (the walks then
 // read shared memory, not one L2 round trip per step).  Returns the chunk's token count.
 __device__ __forceinline__ int stage_chunk_ids(const int32_t* ids, int T, int k, int* ids_s) {
-  const int c0 = blockIdx.x * kDispatchChunk;
-  const int n = min(T - c0, kDispatchChunk);
+  const int c0 = blockIdx.x * kScatterChunk;
+  const int n = min(T - c0, kScatterChunk);
   for (int i = threadIdx.x; i < n * k; i += blockDim.x) ids_s[i] = __ldcg(ids + size_t(c0) * k + i);
   return n;
 }
 
-// smem: [kWarps][E] per-warp counters, then the chunk's ids [kDispatchChunk][k]
+// smem: [kWarps][E] per-warp counters, then the chunk's ids [kScatterChunk][k]
 __device__ void count_chunk(const int32_t* ids, int T, int E, int k, int* wcnt, int32_t* chunk_row) {
   const int warp = threadIdx.x >> 5;
   const int nw = active_warps(T);
@@ -58,12 +58,12 @@ __device__ void scan_and_tiles(int T, int E, int k, int n_chunks, int rows_per_t
                                int* sm_a, int* warp_tot) {
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 8) {  // eight chunks' loads in flight at once
-      int v[8];
+    for (int c0 = 0; c0 < n_chunks; c0 += 16) {  // sixteen chunks' loads in flight at once
+      int v[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = c0 + j < n_chunks ? o.chunk_base[size_t(c0 + j) * E + e] : 0;
+      for (int j = 0; j < 16; ++j) v[j] = c0 + j < n_chunks ? o.chunk_base[size_t(c0 + j) * E + e] : 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 16; ++j)
         if (c0 + j < n_chunks) {
           o.chunk_base[size_t(c0 + j) * E + e] = run;
           run += v[j];
@@ -113,7 +113,7 @@ __device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt
   const int nw = active_warps(T);
   int* ids_s = wcnt + kWarps * E;
   const int n = stage_chunk_ids(ids, T, k, ids_s);
-  const int cbase = blockIdx.x * kDispatchChunk;  // token index of the chunk's first token
+  const int cbase = blockIdx.x * kScatterChunk;  // token index of the chunk's first token
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   const int t0 = min(n, warp * kTokensPerWarp), t1 = min(n, t0 + kTokensPerWarp);  // chunk-relative
@@ -140,11 +140,11 @@ __device__ void scatter_chunk(const int32_t* ids, int T, int E, int k, int* wcnt
     perm[row] = cbase + t;
     pos[size_t(cbase + t) * k + s] = row;
   });
-  for (int t = blockIdx.x * kDispatchChunk + threadIdx.x; t < min(T, (blockIdx.x + 1) * kDispatchChunk); t += blockDim.x)
+  for (int t = blockIdx.x * kScatterChunk + threadIdx.x; t < min(T, (blockIdx.x + 1) * kScatterChunk); t += blockDim.x)
     perm[size_t(k) * T + t] = t;
 }
 
-__global__ void __launch_bounds__(1024) k_dispatch_count(const int32_t* __restrict__ ids, int T, int E, int k,
+__global__ void __launch_bounds__(kWarps * 32) k_dispatch_count(const int32_t* __restrict__ ids, int T, int E, int k,
                                                          DispatchOut o) {
   pdl_begin();
   extern __shared__ int smem[];
@@ -159,26 +159,10 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(int T, int E, int k, int
   scan_and_tiles(T, E, k, n_chunks, rows_per_tile, o, sm_a, warp_tot);
 }
 
-__global__ void __launch_bounds__(1024) k_dispatch_scatter(const int32_t* __restrict__ ids, int T, int E, int k,
+__global__ void __launch_bounds__(kWarps * 32) k_dispatch_scatter(const int32_t* __restrict__ ids, int T, int E, int k,
                                                            DispatchOut o) {
   pdl_begin();
   extern __shared__ int smem[];
-  scatter_chunk(ids, T, E, k, smem, o);
-}
-
-// T <= one chunk: the three phases in one CTA.
-__global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restrict__ ids, int T, int E, int k,
-                                                         int rows_per_tile, DispatchOut o) {
-  pdl_begin();
-  extern __shared__ int smem[];
-  __shared__ int sm_a[kMaxExperts + 1];
-  __shared__ int warp_tot[33];
-  count_chunk(ids, T, E, k, smem, o.chunk_base);
-  __threadfence_block();
-  __syncthreads();
-  scan_and_tiles(T, E, k, 1, rows_per_tile, o, sm_a, warp_tot);
-  __threadfence_block();
-  __syncthreads();
   scatter_chunk(ids, T, E, k, smem, o);
 }
 
@@ -206,28 +190,24 @@ cudaError_t launch_dispatch(const int32_t* ids, int T, int E, int k, int rows_pe
                             int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos, cudaStream_t s) {
   DispatchOut o;
   dispatch_outputs(ws, base, counts, offsets, perm, pos, &o);
-  const size_t smem = (size_t(kWarps) * E + size_t(kDispatchChunk) * k) * sizeof(int);
-  const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  const size_t smem = (size_t(kWarps) * E + size_t(kScatterChunk) * k) * sizeof(int);
+  const int n_chunks = (T + kScatterChunk - 1) / kScatterChunk;
   // opt in once per process to the largest per-warp counter table (E <= kMaxExperts); later
   // calls (also inside a stream capture) only launch
   static cudaError_t attr = [] {
-    const int most = int((size_t(kWarps) * kMaxExperts + size_t(kDispatchChunk) * kTopK) * sizeof(int));
-    cudaError_t e1 = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    const int most = int((size_t(kWarps) * kMaxExperts + size_t(kScatterChunk) * kTopK) * sizeof(int));
     cudaError_t e2 = cudaFuncSetAttribute(k_dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     cudaError_t e3 = cudaFuncSetAttribute(k_dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    return e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+    return e2 != cudaSuccess ? e2 : e3;
   }();
   if (attr != cudaSuccess) return attr;
-  if (n_chunks == 1 && E < 512) {
+  if (T <= kDispatchChunk && E < 512) {
     const size_t lean = size_t(lean_dispatch_smem_ints(T, E, k)) * sizeof(int);
     return launch_pdl(k_dispatch_lean, dim3(1), dim3(kLeanWarps * 32), lean, s, ids, T, E, k, rows_per_tile, o);
   }
-  if (n_chunks == 1) {
-    return launch_pdl(k_dispatch_small, dim3(1), dim3(1024), smem, s, ids, T, E, k, rows_per_tile, o);
-  }
-  cudaError_t e = launch_pdl(k_dispatch_count, dim3(n_chunks), dim3(1024), smem, s, ids, T, E, k, o);
+  cudaError_t e = launch_pdl(k_dispatch_count, dim3(n_chunks), dim3(kWarps * 32), smem, s, ids, T, E, k, o);
   if (e == cudaSuccess) e = launch_pdl(k_dispatch_scan, dim3(1), dim3(1024), 0, s, T, E, k, n_chunks, rows_per_tile, o);
-  if (e == cudaSuccess) e = launch_pdl(k_dispatch_scatter, dim3(n_chunks), dim3(1024), smem, s, ids, T, E, k, o);
+  if (e == cudaSuccess) e = launch_pdl(k_dispatch_scatter, dim3(n_chunks), dim3(kWarps * 32), smem, s, ids, T, E, k, o);
   return e;
 }
 

@@ -284,6 +284,18 @@ def test_dispatch_exact(moe, shape_layer, T, mode):
         assert np.array_equal(got[key].cpu().numpy().reshape(ref[key].shape), ref[key]), key
 
 
+@pytest.mark.parametrize("T", [1, 700, 5000])
+def test_dispatch_exact_many_experts(moe, T):
+    """E = 1000 (>= 512): the multi-CTA dispatch at every size, bit-exact against the oracle."""
+    E = 1000
+    layer = moe.Layer.from_host(g.make_layer(1, 256, 64, E, fp8=True, bias_var=None))
+    ids = np.argsort(np.random.default_rng(T + 7).random((T, E)), axis=1)[:, :6].astype(np.int32)
+    ref = o.dispatch(ids, E)
+    got = moe.dispatch(torch.from_numpy(ids).cuda(), E, moe.workspace(layer, T))
+    for key in ("counts", "offsets", "perm", "pos"):
+        assert np.array_equal(got[key].cpu().numpy().reshape(ref[key].shape), ref[key]), key
+
+
 # ------------------------------------------------------------------------- layer ---------
 
 def test_tiny_fp32_layer_free_then_forced(moe, tiny):
