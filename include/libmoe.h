@@ -198,7 +198,7 @@ moe_status moe_get_status(void* ws, moe_stream_t stream);
  * serving loop where an allocation, which may synchronise the device, is not allowed).  The
  * pages have no counterpart: this is a deployment variant of the router and selection.
  *   Same arguments and results as moe_route, minus logits_out and the workspace.
- *   Scratch: a fixed 4 MiB + 256 B array inside the library, resident on every GPU that loads
+ *   Scratch: a fixed 4 MiB + 768 B array inside the library, resident on every GPU that loads
  *   it until the process exits; T * n_experts must be <= 1,048,576, else MOE_ERR_WORKSPACE.
  *   The first call on a device looks up the array's device address (once per device, with
  *   that device current); make that first call before any stream capture.

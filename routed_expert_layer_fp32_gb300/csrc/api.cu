@@ -108,7 +108,7 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   bool dispatched = false;  // the decode router also dispatches then
   bool quantised = false;   // the bf16 decode router also quantises the activations (E4M3 layers)
   if (!(forced_ids && forced_w)) {
-    if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
+    if (T <= kRouterDecodeMaxT && L.d % 256 == 0 && L.d <= 2048) {
       selected = !forced_ids;
       // under free routing the router's last selecting CTA also dispatches
       dispatched = selected && L.E < 512;
@@ -225,7 +225,7 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
   const LayerDev L = to_dev(layer);
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + lay.logits);
   DevStatus* st = reinterpret_cast<DevStatus*>(base + lay.status);
-  if (T <= kRouterSmallMaxT && L.d % 256 == 0 && L.d <= 2048) {
+  if (T <= kRouterDecodeMaxT && L.d % 256 == 0 && L.d <= 2048) {
     MOE_TRY(launch_router_decode(x, x_dtype == MOE_BF16, T, L, logits, ids_out, w_out, st, nullptr, 0, nullptr, nullptr, s));
     return MOE_OK;
   } else if (T <= kRouterSmallMaxT && L.d <= 8192)

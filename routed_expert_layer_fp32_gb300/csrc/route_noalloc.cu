@@ -19,10 +19,10 @@
 
 namespace {
 
-constexpr size_t kNoAllocStatusBytes = 256;
+constexpr size_t kNoAllocStatusBytes = sizeof(moe::DevStatus);
 constexpr size_t kNoAllocMaxLogits = size_t(1) << 20;  // limit on T * n_experts
-constexpr size_t kNoAllocBytes = kNoAllocStatusBytes + kNoAllocMaxLogits * sizeof(float);  // 4 MiB + 256 B
-static_assert(sizeof(moe::DevStatus) == kNoAllocStatusBytes, "status record size");
+constexpr size_t kNoAllocBytes = kNoAllocStatusBytes + kNoAllocMaxLogits * sizeof(float);  // 4 MiB + 768 B
+static_assert(kNoAllocStatusBytes % 256 == 0, "the logits start 256-byte aligned");
 
 // The scratch: status record, then T x n_experts fp32 logits.
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];

@@ -270,7 +270,7 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int T, int
 // issued up front; thread = 2 experts x 2 tokens, one sequential fp32 sum over the slice.
 constexpr int kRdLd = kRdK + 4;
 constexpr size_t kRdSmemF32 = size_t(kRdE + kRdT) * kRdLd * 4 + size_t(kRdT) * kRdE * 4 + 16;
-static_assert(size_t(lean_dispatch_smem_ints(kRouterSmallMaxT, 511, kTopK)) * 4 <= size_t(kRdE + kRdT) * kRdLd * 4,
+static_assert(size_t(lean_dispatch_smem_ints(kRouterDecodeMaxT, 511, kTopK)) * 4 <= size_t(kRdE + kRdT) * kRdLd * 4,
               "dispatch scratch");
 __global__ void __launch_bounds__(kRdThreads, 2) k_router_decode_f32(const float* __restrict__ x, int T, int d, int E,
                                                                   const float* __restrict__ Wr,
@@ -361,7 +361,7 @@ constexpr size_t kRmOffPart = kRmOffWpart + size_t(kRdThreads / 32) * kRdT * kRm
 constexpr size_t kRmOffAmax = kRmOffPart + size_t(kRdT) * kRdE * 4;  // [kRdT] partial max |x| (fused quantisation)
 // the dispatching CTA's scratch (T <= 128, E < 512) overlays the Wr and x staging only: the
 // partials after them may still be read by the cluster's other CTAs
-static_assert(size_t(lean_dispatch_smem_ints(kRouterSmallMaxT, 511, kTopK)) * 4 <= kRmOffWpart, "dispatch scratch");
+static_assert(size_t(lean_dispatch_smem_ints(kRouterDecodeMaxT, 511, kTopK)) * 4 <= kRmOffWpart, "dispatch scratch");
 constexpr size_t kRdSmemBf16 = kRmOffAmax + size_t(kRdT) * 4 + 16;
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -619,7 +619,7 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, const LayerD
 cudaError_t launch_router_decode(const void* x, bool x_bf16, int T, const LayerDev& L, float* logits, int32_t* ids,
                                  float* wts, DevStatus* st, const DispatchOut* dsp, int rows_per_tile, uint8_t* xq,
                                  float* sx, cudaStream_t s) {
-  if (T > kRouterSmallMaxT || L.d % kRdK || L.d / kRdK > 8) return cudaErrorInvalidValue;
+  if (T > kRouterDecodeMaxT || L.d % kRdK || L.d / kRdK > 8) return cudaErrorInvalidValue;
   if (xq && (!x_bf16 || !sx)) return cudaErrorInvalidValue;
   const int n_slice = L.d / kRdK;
   static cudaError_t attr = [] {
