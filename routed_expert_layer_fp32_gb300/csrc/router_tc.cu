@@ -31,16 +31,18 @@ constexpr int kRtEpiWarps = 4 * kRtEpiParts;
 constexpr int kRtThreads = (2 + kRtEpiWarps) * 32;
 // partial top-k lists of parts 1..3, merged by part 0: [part-1][token][slot] score, logit, id
 constexpr size_t kRtMergeBytes = size_t(kRtEpiParts - 1) * 128 * kTopK * 12;
+// split mode: rank 1's merged lists for rank 0, [128][kTopK] score, logit, id
+constexpr size_t kRtRecvBytes = size_t(128) * kTopK * 12;
 constexpr int kRtM = 128;
 constexpr int kRtATile = kRtM * 128;
-constexpr size_t kRtSmemBudget = 200 * 1024;
+constexpr size_t kRtSmemBudget = 200 * 1024;  // at most this much for the two rings
 
-// Split layout: block ((kt * 3 + term) * 2 + h) holds term `term` of experts
+// Split layout: block ((kt * 2 + h) * 3 + term) holds term `term` of experts
 // [h n_half, (h + 1) n_half) over k = [64 kt, 64 kt + 64): n_half rows of 128 bytes, the 16-byte
 // chunk c of row r stored at chunk c ^ (r % 8) (the MMA's 128-byte swizzle).  A thread converts
 // one 8-element chunk of one expert row into its three terms.
 __device__ __forceinline__ size_t split_block_offset(int kt, int term, int h, int n_half) {
-  return (size_t(kt * 3 + term) * 2 + h) * size_t(n_half) * 128;
+  return (size_t(kt * 2 + h) * 3 + term) * size_t(n_half) * 128;
 }
 
 __global__ void k_router_split_w(const float* __restrict__ Wr, int E, int d, int n_half, uint8_t* __restrict__ out) {
@@ -80,7 +82,7 @@ __global__ void k_router_split_w(const float* __restrict__ Wr, int E, int d, int
 }
 
 constexpr int kRtC = 2;       // CTAs per cluster sharing the weight stream
-constexpr int kRtMaxStages = 4;
+constexpr int kRtMaxStages = 6;
 
 struct RtCtl {
   uint64_t full_a[kRtMaxStages];
@@ -90,11 +92,13 @@ struct RtCtl {
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_done;
+  uint64_t recv_full;  // split mode, rank 0: rank 1's lists have arrived (one arrival per thread)
   uint32_t tmem_base;
   int abort;
   int epi_ok[2][4][kRtEpiParts];  // per tile parity: each epilogue warp's accumulator wait succeeded
 };
 
+template <bool split>
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_router_tc(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ w_split,
                 const float* __restrict__ bias, const float* __restrict__ sel_bias, int T, int d, int E, int n_half,
@@ -103,12 +107,20 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 int* status_flags) {
   extern __shared__ uint8_t rt_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
+  // split mode (few tiles): both CTAs of the pair take the same token tile, CTA r the experts
+  // [r n_half, (r + 1) n_half): a stage holds only its own half, and rank 1 hands its
+  // selected lists to rank 0.  Otherwise two tiles share the weight stream (multicast).
   const int b_half_bytes = n_half * 128;
-  const int b_stage_bytes = 2 * b_half_bytes;
+  // a weight stage: split mode, the three terms of this CTA's half for one k-slice (one
+  // contiguous 72 KB copy: larger copies stream faster per SM); otherwise both halves of one
+  // (k-slice, term)
+  const int b_stage_bytes = split ? 3 * b_half_bytes : 2 * b_half_bytes;
+  const int b_per_kt = split ? 1 : 3;  // weight stages per k-slice
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + size_t(n_a) * kRtATile;
   RtCtl* ctl = reinterpret_cast<RtCtl*>(ring_b + size_t(n_b) * b_stage_bytes);
   uint8_t* merge = reinterpret_cast<uint8_t*>(ctl) + (sizeof(RtCtl) + 15) / 16 * 16;  // kRtMergeBytes
+  uint8_t* recv = merge + kRtMergeBytes;                                               // kRtRecvBytes (split)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = int(cluster_ctarank());
   const int pair = int(blockIdx.x) / kRtC, n_pairs = int(gridDim.x) / kRtC;
@@ -119,11 +131,12 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
     for (int s = 0; s < n_b; ++s) {
       mbar_init(&ctl->full_b[s], 1);
-      mbar_init(&ctl->empty_b[s], kRtC);
+      mbar_init(&ctl->empty_b[s], split ? 1 : kRtC);
     }
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->acc_empty, kRtEpiWarps);
     mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->recv_full, 4 * 32);  // every thread of rank 1's four part-0 warps
     ctl->abort = 0;
     mbar_fence_init();
   }
@@ -142,9 +155,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   constexpr uint16_t kBoth = (1u << kRtC) - 1u;
   // round j: the pair's tiles are kRtC * (pair + j * n_pairs) + rank; the cluster runs while
   // rank 0's tile exists, rank 1 possibly without a tile of its own ("phantom")
-  auto tile_of = [&](int j, int r) { return kRtC * (pair + j * n_pairs) + r; };
+  auto tile_of = [&](int j, int r) { return split ? pair + j * n_pairs : kRtC * (pair + j * n_pairs) + r; };
   auto sa = [&](int s) { return ring_a + size_t(s) * kRtATile; };
-  auto sb = [&](int s, int h) { return ring_b + size_t(s) * b_stage_bytes + h * b_half_bytes; };
+  // half h of stage s (split mode: the stage is this CTA's half alone)
+  auto sb = [&](int s, int h) { return ring_b + size_t(s) * b_stage_bytes + (split ? 0 : h * b_half_bytes); };
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer: x slice per k-slice (own tile), weight half per (k-slice, term)
@@ -165,16 +179,20 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             tma_load_2d(sa(s), &map_x, kt * 64, item * kRtM, &ctl->full_a[s]);
             ++ia;
           }
-          for (int term = 0; term < 3; ++term, ++ib) {
+          for (int term = 0; term < b_per_kt; ++term, ++ib) {
             const int s = ib % n_b, use = ib / n_b;
             if (!mbar_wait(&ctl->empty_b[s], (use & 1) ^ 1, &ctl->abort)) {
               report_timeout_flag(status_flags, 25);
               stop = true;
               break;
             }
-            mbar_arrive_expect_tx(&ctl->full_b[s], b_stage_bytes);  // both halves land here
-            bulk_g2s_mc(sb(s, rank), w_split + split_block_offset(kt, term, rank, n_half), uint32_t(b_half_bytes),
-                        &ctl->full_b[s], kBoth);
+            mbar_arrive_expect_tx(&ctl->full_b[s], b_stage_bytes);  // both halves land here (split: own half)
+            if (split)
+              bulk_g2s(sb(s, rank), w_split + split_block_offset(kt, 0, rank, n_half), uint32_t(b_stage_bytes),
+                       &ctl->full_b[s]);
+            else
+              bulk_g2s_mc(sb(s, rank), w_split + split_block_offset(kt, term, rank, n_half), uint32_t(b_half_bytes),
+                          &ctl->full_b[s], kBoth);
           }
         }
       }
@@ -208,7 +226,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             stop = true;
             break;
           }
-          for (int term = 0; term < 3; ++term, ++ib) {
+          for (int term = 0; term < b_per_kt; ++term, ++ib) {
             const int s = ib % n_b, use = ib / n_b;
             if (!mbar_wait(&ctl->full_b[s], use & 1, &ctl->abort)) {
               report_timeout_flag(status_flags, 26);
@@ -216,7 +234,17 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               break;
             }
             tc_fence_after();
-            if (real) {
+            if (real && split) {  // this CTA's half only (three terms), into its own columns
+              const uint64_t da = sw128_desc(sa(sa_i));
+              for (int tm = 0; tm < 3; ++tm) {
+                const uint64_t db = sw128_desc(sb(s, rank) + tm * b_half_bytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint32_t acc = (kt > 0 || tm > 0 || kk > 0) ? 1u : 0u;
+                  tc_mma_f16(tmem + uint32_t(rank * n_half), da + 2 * kk, db + 2 * kk, idesc, acc);
+                }
+              }
+            } else if (real) {
               const uint64_t da = sw128_desc(sa(sa_i));
               const uint64_t db0 = sw128_desc(sb(s, 0)), db1 = sw128_desc(sb(s, 1));
 #pragma unroll
@@ -226,7 +254,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 tc_mma_f16(tmem + uint32_t(n_half), da + 2 * kk, db1 + 2 * kk, idesc, acc);
               }
             }
-            tc_commit_mc(&ctl->empty_b[s], kBoth);  // this CTA is done with both halves
+            if (split)
+              tc_commit(&ctl->empty_b[s]);
+            else
+              tc_commit_mc(&ctl->empty_b[s], kBoth);  // this CTA is done with both halves
           }
           if (stop) break;
           if (real) {
@@ -255,8 +286,14 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     float* m_sc = reinterpret_cast<float*>(merge);                       // [3][128][kTopK]
     float* m_lg = m_sc + (kRtEpiParts - 1) * 128 * kTopK;
     int* m_id = reinterpret_cast<int*>(m_lg + (kRtEpiParts - 1) * 128 * kTopK);
-    const int n_chunks = (E + 15) / 16;
-    const int ch_lo = part * n_chunks / kRtEpiParts, ch_hi = (part + 1) * n_chunks / kRtEpiParts;
+    // this CTA's experts in 16-column chunks (split mode: its half), a quarter per part
+    const int n_chunks = split ? n_half / 16 : (E + 15) / 16;
+    const int ch_base = split ? rank * (n_half / 16) : 0;
+    const int ch_lo = ch_base + part * n_chunks / kRtEpiParts, ch_hi = ch_base + (part + 1) * n_chunks / kRtEpiParts;
+    // split mode: rank 1 writes its lists into rank 0's receive buffer [row][slot]
+    float* r_sc = reinterpret_cast<float*>(recv);
+    float* r_lg = r_sc + 128 * kTopK;
+    int* r_id = reinterpret_cast<int*>(r_lg + 128 * kTopK);
     int jt = 0;
     for (int j = 0; tile_of(j, rank) < n_items; ++j, ++jt) {
       const int item = tile_of(j, rank);
@@ -369,7 +406,50 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               }
             }
           }
-          if (t < T) {
+          if (split && rank == 1) {  // hand the list to rank 0, which merges and writes
+            const uint32_t base = mapa_shared(smem_u32(recv), 0);
+#pragma unroll
+            for (int i = 0; i < kTopK; ++i) {
+              const uint32_t o = uint32_t(row * kTopK + i) * 4u;
+              st_cluster_f32(base + o, tv[i]);
+              st_cluster_f32(base + uint32_t(128 * kTopK * 4) + o, tl[i]);
+              st_cluster_f32(base + uint32_t(2 * 128 * kTopK * 4) + o, __int_as_float(ti[i]));
+            }
+            mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->recv_full), 0));  // releases this thread's stores
+          }
+          bool merged = true;
+          if (split && rank == 0) {  // rank 1's list for these tokens, in the same order
+            merged = mbar_wait_cluster(&ctl->recv_full, jt & 1, &ctl->abort);
+            if (!merged && lane == 0) report_timeout_flag(status_flags, 27);
+            bool open = merged;
+#pragma unroll
+            for (int i = 0; i < kTopK; ++i) {
+              const int o = row * kTopK + i;
+              const float s = r_sc[o], lgv = r_lg[o];
+              const int e = r_id[o];
+              open = open && (s > tv[kTopK - 1] || (s == tv[kTopK - 1] && e < ti[kTopK - 1]));
+              if (open) {
+                tv[kTopK - 1] = s;
+                tl[kTopK - 1] = lgv;
+                ti[kTopK - 1] = e;
+#pragma unroll
+                for (int j2 = kTopK - 1; j2 > 0; --j2) {
+                  if (tv[j2] > tv[j2 - 1] || (tv[j2] == tv[j2 - 1] && ti[j2] < ti[j2 - 1])) {
+                    const float fv = tv[j2];
+                    tv[j2] = tv[j2 - 1];
+                    tv[j2 - 1] = fv;
+                    const float fl = tl[j2];
+                    tl[j2] = tl[j2 - 1];
+                    tl[j2 - 1] = fl;
+                    const int fi = ti[j2];
+                    ti[j2] = ti[j2 - 1];
+                    ti[j2 - 1] = fi;
+                  }
+                }
+              }
+            }
+          }
+          if (t < T && merged && !(split && rank == 1)) {
             float m = tl[0];  // the largest selected logit (slot 0 unless the bias reordered them)
 #pragma unroll
             for (int i = 1; i < kTopK; ++i)
@@ -426,21 +506,32 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   cudaError_t e = launch_pdl(k_router_split_w, dim3(int(std::min<long long>((n + 255) / 256, 4096))), dim3(256), 0, s,
                              L.Wr, L.E, L.d, n_half, reinterpret_cast<uint8_t*>(w3));
   if (e != cudaSuccess) return e;
-  const int b_stage_bytes = 2 * n_half * 128;
-  // rings: x slices and weight stages, as many of each as fit (at most kRtMaxStages)
-  int n_b = int(std::min<size_t>(kRtMaxStages, (kRtSmemBudget - 2 * size_t(kRtATile)) / b_stage_bytes));
-  int n_a = int(std::min<size_t>(kRtMaxStages, (kRtSmemBudget - size_t(n_b) * b_stage_bytes) / kRtATile));
+  const int items = (T + kRtM - 1) / kRtM;
+  // few tiles (every tile's CTA pair fits on the GPU at once): split mode, a pair per tile,
+  // each CTA half of the experts; otherwise a pair per two tiles sharing the weight stream
+  const int split = items * kRtC <= rt_sm_count() ? 1 : 0;
+  const int b_stage_bytes = (split ? 3 : 2) * n_half * 128;
+  // rings: weight stages first, then x slices, as many as fit beside the control block and the
+  // merge buffers (at most kRtMaxStages each; at least two x slices)
+  const size_t fixed = 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes + (split ? kRtRecvBytes : 0);
+  const size_t rings = std::min(kRtSmemBudget, 227 * 1024 - fixed);
+  int n_b = int(std::min<size_t>(kRtMaxStages, (rings - 2 * size_t(kRtATile)) / b_stage_bytes));
+  if (n_b < 2) return cudaErrorInvalidValue;
+  int n_a = int(std::min<size_t>(kRtMaxStages, (rings - size_t(n_b) * b_stage_bytes) / kRtATile));
   if (n_b < 1 || n_a < 2) return cudaErrorInvalidValue;
   const int tmem_cols = 2 * n_half <= 256 ? 256 : 512;
   CUtensorMap mx;
   if (!make_map_bytes(&mx, x, uint64_t(T), uint64_t(L.d), kRtM, 2)) return cudaErrorInvalidValue;
-  const size_t smem =
-      size_t(n_a) * kRtATile + size_t(n_b) * b_stage_bytes + 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes;
+  const size_t smem = size_t(n_a) * kRtATile + size_t(n_b) * b_stage_bytes + 1024 + (sizeof(RtCtl) + 15) / 16 * 16 +
+                      kRtMergeBytes + (split ? kRtRecvBytes : 0);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  static cudaError_t attr = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  static cudaError_t attr = [] {
+    const cudaError_t e0 = cudaFuncSetAttribute(k_router_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    const cudaError_t e1 = cudaFuncSetAttribute(k_router_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    return e0 != cudaSuccess ? e0 : e1;
+  }();
   if (attr != cudaSuccess) return attr;
-  const int items = (T + kRtM - 1) / kRtM;
-  const int pairs = std::max(1, std::min((items + kRtC - 1) / kRtC, rt_sm_count() / kRtC));
+  const int pairs = split ? items : std::max(1, std::min((items + kRtC - 1) / kRtC, rt_sm_count() / kRtC));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pairs * kRtC);
   cfg.blockDim = dim3(kRtThreads);
@@ -455,8 +546,12 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_router_tc, mx, static_cast<const uint8_t*>(static_cast<const void*>(w3)), L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half, n_a, n_b,
-                            tmem_cols, logits, ids, wts, L.k, &st->flags);
+  const uint8_t* w_split = static_cast<const uint8_t*>(static_cast<const void*>(w3));
+  if (split)
+    return cudaLaunchKernelEx(&cfg, k_router_tc<true>, mx, w_split, L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half,
+                              n_a, n_b, tmem_cols, logits, ids, wts, L.k, &st->flags);
+  return cudaLaunchKernelEx(&cfg, k_router_tc<false>, mx, w_split, L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half,
+                            n_a, n_b, tmem_cols, logits, ids, wts, L.k, &st->flags);
 }
 
 }  // namespace moe
