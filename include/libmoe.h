@@ -14,8 +14,9 @@
  *                 order;  w[t,i] = p[ids_i] / sum_j p[ids_j]
  *   expert e    = W8A8 SwiGLU: x is quantised per token to E4M3 (scale max|x|/448),
  *                 g = (qx . Wg[e,n]) sx sg[e,n], u likewise, h = silu(g) u, h quantised per
- *                 row the same way, y_e[m] = (qh . Wd[e,m]) sh sd[e,m]
- *   y[t]        = y_shared[t] + sum_{i=0..k-1} w[t,i] y_{ids_i}[t]  (slot order)
+ *                 row the same way, y_e[m] = (qh . Wd[e,m]) sh sd[e,m], stored as a bf16
+ *                 activation (round to nearest even) before the combine
+ *   y[t]        = y_shared[t] + sum_{i=0..k-1} w[t,i] y_{ids_i}[t]  (slot order, fp32)
  * With fp32 weights (MOE_F32) the experts run in fp32 without quantisation.
  *
  * Conventions for every call:
