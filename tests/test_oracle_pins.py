@@ -234,6 +234,62 @@ def test_selection_only_bias_against_float64_definition():
     assert not np.allclose(s_out["w"], out["w"], atol=1e-3)
 
 
+def test_score_mode_bias_against_float64_definition():
+    """Score-mode bias (the routing of every Kolibri-shaped workload: the per-expert bias is
+    added to the router score, "We Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate
+    Said No.", section 1), against float64 numpy: logits = x Wr^T + b; p = softmax over all
+    experts; ids = the six largest p (lowest index first on ties); w = p over those six,
+    renormalised.  A large positive bias on one expert puts it first in every token's set
+    with most of the weight; a large negative one keeps another out of every set.  A slip in
+    the sign or the scale of b moves the logits by |b| (about 0.7 here) and fails the logit
+    check by five orders of magnitude."""
+    w = g.make_layer(55, 256, 128, 384, fp8=True, bias_var=0.5)
+    w.bias[11] = 12.0   # always selected, and dominant in the weights
+    w.bias[3] = -40.0   # never selected
+    x = g.make_x(56, 24, 256, bf16=True)
+    xf = g.bf16_bits_to_f32(x).astype(np.float64)
+    out = o.layer_forward(o.Layer(w), x, want_probs=True)
+    lg = xf @ w.Wr.astype(np.float64).T + w.bias.astype(np.float64)
+    for t in range(x.shape[0]):
+        assert np.max(np.abs(out["logits"][t] - lg[t])) < 1e-5 * np.max(np.abs(lg[t]))
+        e = np.exp(lg[t] - lg[t].max())
+        p = e / e.sum()
+        np.testing.assert_allclose(out["p"][t], p, rtol=1e-5, atol=1e-9)
+        order = np.lexsort((np.arange(384), -p))[:6]
+        assert np.array_equal(out["ids"][t], order)
+        assert out["ids"][t][0] == 11 and 3 not in out["ids"][t]
+        np.testing.assert_allclose(out["w"][t], p[order] / p[order].sum(), rtol=1e-5, atol=1e-7)
+        assert out["w"][t][0] > 0.99
+
+
+def test_stack_is_layers_with_a_bf16_residual_update():
+    """The stack (50 layers in Kolibri-1: "We Ported Aleph Alpha's Kolibri to a MacBook. Our Own
+    Gate Said No.", section "The gate") is, layer after layer, r <- bf16(r + layer(r)): the
+    oracle's stack against three separate layer calls with the residual update done by torch
+    (fp32 add, then torch's round-to-nearest-even conversion to bf16), bit-exact, free routing
+    and forced.  A stack that rounded y alone, skipped the rounding or fed a layer the
+    unrounded sum differs in the bits."""
+    ws = [g.make_layer(57 + l, 128, 64, 16, fp8=True, bias_var=0.5) for l in range(3)]
+    Ls = [o.Layer(w) for w in ws]
+    r0 = g.make_x(60, 20, 128, bf16=True)
+    r = torch.from_numpy(r0.view(np.int16).copy()).view(torch.bfloat16)
+    ids_ref = []
+    for L in Ls:
+        out = o.layer_forward(L, r.view(torch.int16).numpy().view(np.uint16))
+        r = (r.float() + torch.from_numpy(out["y"])).to(torch.bfloat16)
+        ids_ref.append(out["ids"])
+    r_ref = r.view(torch.int16).numpy().view(np.uint16)
+    got, ids = o.stack_forward(Ls, r0)
+    assert np.array_equal(ids, np.stack(ids_ref))
+    assert np.array_equal(got, r_ref)
+    forced, ids_f = o.stack_forward(Ls, r0, forced_ids=ids)
+    assert np.array_equal(ids_f, ids) and np.array_equal(forced, r_ref)
+    # the update is not a no-op and not y alone
+    assert not np.array_equal(got, r0)
+    y_only = torch.from_numpy(o.layer_forward(Ls[0], r0)["y"]).to(torch.bfloat16).view(torch.int16).numpy()
+    assert not np.array_equal(o.stack_forward(Ls[:1], r0)[0], y_only.view(np.uint16))
+
+
 def test_selection_only_bias_with_zero_bias_equals_score_mode():
     w = g.make_layer(53, 256, 128, 384, fp8=True, bias_var=None)
     x = g.make_x(54, 16, 256, bf16=True)
