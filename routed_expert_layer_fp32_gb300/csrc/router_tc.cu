@@ -8,17 +8,22 @@
 // values is exact in fp32, so three accumulating bf16 MMAs with an fp32 accumulator give
 // x . w to fp32 accuracy.
 //
-// Tile: 128 tokens (M) x all experts, the experts split into two MMAs of n_half columns
-// (E = 384: 2 x 192) so one TMEM accumulator row holds a token's full logit row.  The two CTAs
-// of a cluster work on two token tiles in lockstep and share the weight stream: each loads one
-// n_half block of every (k-slice, term) weight stage and multicasts it to both, so each CTA
-// reads half of the 4.7 MB of weight terms per tile pair from L2.  The split kernel writes the
-// terms already in stage order and in the 128-byte-swizzled shared-memory layout, so a block
-// (n_half rows x 128 bytes, 24 KB) is one contiguous bulk copy: on this GPU a row-strided
-// tensor-map box of the same size streams several times slower per SM.  The x k-slice (16 KB) has
-// its own ring and is loaded once for the three terms.  Warp roles as in the expert GEMMs
-// (TMA producer, single-thread MMA issuer, four epilogue warps); bounded waits.  A CTA whose
-// pair partner has a tile but it has none still loads and releases its weight halves.
+// Tile: 128 tokens (M) x all experts, the experts split into two halves of n_half columns
+// (E = 384: 2 x 192) so one TMEM accumulator row holds a token's full logit row.  The split
+// kernel writes the terms already in stage order and in the 128-byte-swizzled shared-memory
+// layout: the three terms of one half for one 64-wide k-slice (n_half rows x 128 bytes each,
+// 72 KB at E = 384) are one contiguous block, so a weight stage is one bulk copy (on this GPU
+// a row-strided tensor-map box of the same size streams several times slower per SM, and
+// larger copies stream faster than smaller ones).  The x k-slice (16 KB) has its own ring and
+// is loaded once for both halves and all three terms.
+//
+// Two ways to spread the tiles.  With many tiles each CTA takes whole tiles (both halves, two
+// weight stages per k-slice) and reads the 4.7 MB of weight terms from L2 for each of them.
+// With few tiles (every tile's CTA pair fits on the GPU at once) each tile gets a CTA pair of a
+// thread-block cluster, each CTA half of the experts (one weight stage per k-slice), and rank 1
+// hands its selected top-k lists to rank 0 through distributed shared memory for the final
+// merge.  Every CTA loads only into its own shared memory.  Warp roles as in the expert GEMMs
+// (TMA producer, single-thread MMA issuer, sixteen epilogue warps); bounded waits.
 #include "common.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -81,14 +86,14 @@ __global__ void k_router_split_w(const float* __restrict__ Wr, int E, int d, int
   }
 }
 
-constexpr int kRtC = 2;       // CTAs per cluster sharing the weight stream
+constexpr int kRtPair = 2;  // CTAs per tile in split mode (one thread-block cluster)
 constexpr int kRtMaxStages = 6;
 
 struct RtCtl {
   uint64_t full_a[kRtMaxStages];
   uint64_t empty_a[kRtMaxStages];
   uint64_t full_b[kRtMaxStages];
-  uint64_t empty_b[kRtMaxStages];  // one arrival per CTA of the cluster
+  uint64_t empty_b[kRtMaxStages];
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_done;
@@ -108,22 +113,23 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   extern __shared__ uint8_t rt_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
   // split mode (few tiles): both CTAs of the pair take the same token tile, CTA r the experts
-  // [r n_half, (r + 1) n_half): a stage holds only its own half, and rank 1 hands its
-  // selected lists to rank 0.  Otherwise two tiles share the weight stream (multicast).
+  // [r n_half, (r + 1) n_half), and rank 1 hands its selected lists to rank 0.  Otherwise a CTA
+  // takes whole tiles, both halves.
   const int b_half_bytes = n_half * 128;
-  // a weight stage: split mode, the three terms of this CTA's half for one k-slice (one
-  // contiguous 72 KB copy: larger copies stream faster per SM); otherwise both halves of one
-  // (k-slice, term)
-  const int b_stage_bytes = split ? 3 * b_half_bytes : 2 * b_half_bytes;
-  const int b_per_kt = split ? 1 : 3;  // weight stages per k-slice
+  // a weight stage: the three terms of one half for one k-slice, one contiguous copy (72 KB at
+  // E = 384); split mode loads its own half's stage per k-slice, otherwise both halves' in turn
+  const int b_stage_bytes = 3 * b_half_bytes;
+  const int b_per_kt = split ? 1 : 2;  // weight stages per k-slice
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + size_t(n_a) * kRtATile;
   RtCtl* ctl = reinterpret_cast<RtCtl*>(ring_b + size_t(n_b) * b_stage_bytes);
   uint8_t* merge = reinterpret_cast<uint8_t*>(ctl) + (sizeof(RtCtl) + 15) / 16 * 16;  // kRtMergeBytes
   uint8_t* recv = merge + kRtMergeBytes;                                               // kRtRecvBytes (split)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = int(cluster_ctarank());
-  const int pair = int(blockIdx.x) / kRtC, n_pairs = int(gridDim.x) / kRtC;
+  const int rank = split ? int(cluster_ctarank()) : 0;
+  // the CTA (split mode: the CTA pair) takes tiles unit, unit + n_units, ...
+  constexpr int kPer = split ? kRtPair : 1;
+  const int unit = int(blockIdx.x) / kPer, n_units = int(gridDim.x) / kPer;
   if (threadIdx.x == 0) {
     for (int s = 0; s < n_a; ++s) {
       mbar_init(&ctl->full_a[s], 1);
@@ -131,7 +137,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
     for (int s = 0; s < n_b; ++s) {
       mbar_init(&ctl->full_b[s], 1);
-      mbar_init(&ctl->empty_b[s], split ? 1 : kRtC);
+      mbar_init(&ctl->empty_b[s], 1);
     }
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->acc_empty, kRtEpiWarps);
@@ -146,29 +152,26 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // the partner's barriers exist before any multicast or remote arrival
+  if (split) cluster_sync_all();  // the partner's receive barrier exists before any remote arrival
   tc_fence_after();
   pdl_begin();
   const uint32_t tmem = ctl->tmem_base;
   const int n_items = (T + kRtM - 1) / kRtM;
   const int KT = d / 64;  // 64 bf16 per 128-byte k-slice
-  constexpr uint16_t kBoth = (1u << kRtC) - 1u;
-  // round j: the pair's tiles are kRtC * (pair + j * n_pairs) + rank; the cluster runs while
-  // rank 0's tile exists, rank 1 possibly without a tile of its own ("phantom")
-  auto tile_of = [&](int j, int r) { return split ? pair + j * n_pairs : kRtC * (pair + j * n_pairs) + r; };
+  auto tile_of = [&](int j) { return unit + j * n_units; };
   auto sa = [&](int s) { return ring_a + size_t(s) * kRtATile; };
-  // half h of stage s (split mode: the stage is this CTA's half alone)
-  auto sb = [&](int s, int h) { return ring_b + size_t(s) * b_stage_bytes + (split ? 0 : h * b_half_bytes); };
+  auto sb = [&](int s) { return ring_b + size_t(s) * b_stage_bytes; };
+  // the expert half stage number hh of a k-slice covers
+  auto half_of = [&](int hh) { return split ? rank : hh; };
 
   if (warp == 0) {
-    if (lane == 0) {  // TMA producer: x slice per k-slice (own tile), weight half per (k-slice, term)
+    if (lane == 0) {  // TMA producer: x slice per k-slice, the weight stages of every k-slice
       int ia = 0, ib = 0;
       bool stop = false;
-      for (int j = 0; tile_of(j, 0) < n_items && !stop; ++j) {
-        const int item = tile_of(j, rank);
-        const bool real = item < n_items;
+      for (int j = 0; tile_of(j) < n_items && !stop; ++j) {
+        const int item = tile_of(j);
         for (int kt = 0; kt < KT && !stop; ++kt) {
-          if (real) {
+          {
             const int s = ia % n_a, use = ia / n_a;
             if (!mbar_wait(&ctl->empty_a[s], (use & 1) ^ 1, &ctl->abort)) {
               report_timeout_flag(status_flags, 21);
@@ -179,20 +182,16 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             tma_load_2d(sa(s), &map_x, kt * 64, item * kRtM, &ctl->full_a[s]);
             ++ia;
           }
-          for (int term = 0; term < b_per_kt; ++term, ++ib) {
+          for (int hh = 0; hh < b_per_kt; ++hh, ++ib) {
             const int s = ib % n_b, use = ib / n_b;
             if (!mbar_wait(&ctl->empty_b[s], (use & 1) ^ 1, &ctl->abort)) {
               report_timeout_flag(status_flags, 25);
               stop = true;
               break;
             }
-            mbar_arrive_expect_tx(&ctl->full_b[s], b_stage_bytes);  // both halves land here (split: own half)
-            if (split)
-              bulk_g2s(sb(s, rank), w_split + split_block_offset(kt, 0, rank, n_half), uint32_t(b_stage_bytes),
-                       &ctl->full_b[s]);
-            else
-              bulk_g2s_mc(sb(s, rank), w_split + split_block_offset(kt, term, rank, n_half), uint32_t(b_half_bytes),
-                          &ctl->full_b[s], kBoth);
+            mbar_arrive_expect_tx(&ctl->full_b[s], b_stage_bytes);
+            bulk_g2s(sb(s), w_split + split_block_offset(kt, 0, half_of(hh), n_half), uint32_t(b_stage_bytes),
+                     &ctl->full_b[s]);
           }
         }
       }
@@ -210,23 +209,20 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       const uint32_t idesc = idesc_bf16(kRtM, n_half);
       int ia = 0, ib = 0, jt = 0;
       bool stop = false;
-      for (int j = 0; tile_of(j, 0) < n_items && !stop; ++j) {
-        const bool real = tile_of(j, rank) < n_items;
-        if (real) {
-          if (!mbar_wait(&ctl->acc_empty, (jt & 1) ^ 1, &ctl->abort)) {
-            report_timeout_flag(status_flags, 22);
-            break;
-          }
-          tc_fence_after();
+      for (int j = 0; tile_of(j) < n_items && !stop; ++j) {
+        if (!mbar_wait(&ctl->acc_empty, (jt & 1) ^ 1, &ctl->abort)) {
+          report_timeout_flag(status_flags, 22);
+          break;
         }
+        tc_fence_after();
         for (int kt = 0; kt < KT && !stop; ++kt) {
           const int sa_i = ia % n_a;
-          if (real && !mbar_wait(&ctl->full_a[sa_i], (ia / n_a) & 1, &ctl->abort)) {
+          if (!mbar_wait(&ctl->full_a[sa_i], (ia / n_a) & 1, &ctl->abort)) {
             report_timeout_flag(status_flags, 23);
             stop = true;
             break;
           }
-          for (int term = 0; term < b_per_kt; ++term, ++ib) {
+          for (int hh = 0; hh < b_per_kt; ++hh, ++ib) {
             const int s = ib % n_b, use = ib / n_b;
             if (!mbar_wait(&ctl->full_b[s], use & 1, &ctl->abort)) {
               report_timeout_flag(status_flags, 26);
@@ -234,38 +230,24 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               break;
             }
             tc_fence_after();
-            if (real && split) {  // this CTA's half only (three terms), into its own columns
-              const uint64_t da = sw128_desc(sa(sa_i));
-              for (int tm = 0; tm < 3; ++tm) {
-                const uint64_t db = sw128_desc(sb(s, rank) + tm * b_half_bytes);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint32_t acc = (kt > 0 || tm > 0 || kk > 0) ? 1u : 0u;
-                  tc_mma_f16(tmem + uint32_t(rank * n_half), da + 2 * kk, db + 2 * kk, idesc, acc);
-                }
-              }
-            } else if (real) {
-              const uint64_t da = sw128_desc(sa(sa_i));
-              const uint64_t db0 = sw128_desc(sb(s, 0)), db1 = sw128_desc(sb(s, 1));
+            // the three terms of one half into that half's accumulator columns
+            const uint64_t da = sw128_desc(sa(sa_i));
+            const uint32_t d_cols = tmem + uint32_t(half_of(hh) * n_half);
+            for (int tm = 0; tm < 3; ++tm) {
+              const uint64_t db = sw128_desc(sb(s) + tm * b_half_bytes);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {  // 16 bf16 (32 bytes) per MMA
-                const uint32_t acc = (kt > 0 || term > 0 || kk > 0) ? 1u : 0u;
-                tc_mma_f16(tmem, da + 2 * kk, db0 + 2 * kk, idesc, acc);
-                tc_mma_f16(tmem + uint32_t(n_half), da + 2 * kk, db1 + 2 * kk, idesc, acc);
+                const uint32_t acc = (kt > 0 || tm > 0 || kk > 0) ? 1u : 0u;
+                tc_mma_f16(d_cols, da + 2 * kk, db + 2 * kk, idesc, acc);
               }
             }
-            if (split)
-              tc_commit(&ctl->empty_b[s]);
-            else
-              tc_commit_mc(&ctl->empty_b[s], kBoth);  // this CTA is done with both halves
+            tc_commit(&ctl->empty_b[s]);
           }
           if (stop) break;
-          if (real) {
-            tc_commit(&ctl->empty_a[sa_i]);
-            ++ia;
-          }
+          tc_commit(&ctl->empty_a[sa_i]);
+          ++ia;
         }
-        if (real && !stop) {
+        if (!stop) {
           tc_commit(&ctl->acc_full);
           ++jt;
         }
@@ -295,8 +277,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     float* r_lg = r_sc + 128 * kTopK;
     int* r_id = reinterpret_cast<int*>(r_lg + 128 * kTopK);
     int jt = 0;
-    for (int j = 0; tile_of(j, rank) < n_items; ++j, ++jt) {
-      const int item = tile_of(j, rank);
+    for (int j = 0; tile_of(j) < n_items; ++j, ++jt) {
+      const int item = tile_of(j);
       // the four warps of a quarter meet at named barriers: they leave on a timeout together
       const bool ok = mbar_wait(&ctl->acc_full, jt & 1, &ctl->abort);
       if (lane == 0) ctl->epi_ok[jt & 1][q][part] = ok ? 1 : 0;
@@ -475,7 +457,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no CTA leaves while its partner may still multicast into it or arrive on it
+  if (split) cluster_sync_all();  // no CTA leaves while its partner may still write its lists into it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);
@@ -493,10 +475,27 @@ int rt_sm_count() {
   return sms;
 }
 
+// Stage counts of the two rings for one mode: weight stages first (three terms of one expert
+// half, 3 n_half 128 bytes each), then x slices, as many as fit beside the control block and
+// the merge buffers (at most kRtMaxStages each).  False unless both rings get two stages.
+bool rt_rings(bool split, int n_half, int* n_a, int* n_b, size_t* smem) {
+  const size_t b_stage = size_t(3) * n_half * 128;
+  const size_t fixed = 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes + (split ? kRtRecvBytes : 0);
+  const size_t rings = std::min(kRtSmemBudget, 227 * 1024 - fixed);
+  if (rings < 2 * b_stage + 2 * size_t(kRtATile)) return false;
+  *n_b = int(std::min<size_t>(kRtMaxStages, (rings - 2 * size_t(kRtATile)) / b_stage));
+  *n_a = int(std::min<size_t>(kRtMaxStages, (rings - size_t(*n_b) * b_stage) / kRtATile));
+  *smem = size_t(*n_a) * kRtATile + size_t(*n_b) * b_stage + fixed;
+  return *smem <= 227 * 1024;
+}
+
 }  // namespace
 
 bool router_tc_supported(const LayerDev& L, bool x_bf16) {
-  return x_bf16 && L.d % 64 == 0 && L.E <= 512 && L.E % 32 == 0 && encode_fn() != nullptr;
+  int n_a = 0, n_b = 0;
+  size_t smem = 0;
+  return x_bf16 && L.d % 64 == 0 && L.E <= 512 && L.E % 32 == 0 && rt_rings(false, L.E / 2, &n_a, &n_b, &smem) &&
+         rt_rings(true, L.E / 2, &n_a, &n_b, &smem) && encode_fn() != nullptr;
 }
 
 cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, int32_t* ids,
@@ -507,33 +506,23 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
                              L.Wr, L.E, L.d, n_half, reinterpret_cast<uint8_t*>(w3));
   if (e != cudaSuccess) return e;
   const int items = (T + kRtM - 1) / kRtM;
-  // few tiles (every tile's CTA pair fits on the GPU at once): split mode, a pair per tile,
-  // each CTA half of the experts; otherwise a pair per two tiles sharing the weight stream
-  const int split = items * kRtC <= rt_sm_count() ? 1 : 0;
-  const int b_stage_bytes = (split ? 3 : 2) * n_half * 128;
-  // rings: weight stages first, then x slices, as many as fit beside the control block and the
-  // merge buffers (at most kRtMaxStages each; at least two x slices)
-  const size_t fixed = 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes + (split ? kRtRecvBytes : 0);
-  const size_t rings = std::min(kRtSmemBudget, 227 * 1024 - fixed);
-  int n_b = int(std::min<size_t>(kRtMaxStages, (rings - 2 * size_t(kRtATile)) / b_stage_bytes));
-  if (n_b < 2) return cudaErrorInvalidValue;
-  int n_a = int(std::min<size_t>(kRtMaxStages, (rings - size_t(n_b) * b_stage_bytes) / kRtATile));
-  if (n_b < 1 || n_a < 2) return cudaErrorInvalidValue;
+  // few tiles (every tile's CTA pair fits on the GPU at once): split mode, a CTA pair per
+  // tile, each CTA half of the experts; otherwise one CTA per tile at a time, both halves
+  const int split = items * kRtPair <= rt_sm_count() ? 1 : 0;
+  int n_a = 0, n_b = 0;
+  size_t smem = 0;
+  if (!rt_rings(split != 0, n_half, &n_a, &n_b, &smem)) return cudaErrorInvalidValue;
   const int tmem_cols = 2 * n_half <= 256 ? 256 : 512;
   CUtensorMap mx;
   if (!make_map_bytes(&mx, x, uint64_t(T), uint64_t(L.d), kRtM, 2)) return cudaErrorInvalidValue;
-  const size_t smem = size_t(n_a) * kRtATile + size_t(n_b) * b_stage_bytes + 1024 + (sizeof(RtCtl) + 15) / 16 * 16 +
-                      kRtMergeBytes + (split ? kRtRecvBytes : 0);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
   static cudaError_t attr = [] {
     const cudaError_t e0 = cudaFuncSetAttribute(k_router_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     const cudaError_t e1 = cudaFuncSetAttribute(k_router_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     return e0 != cudaSuccess ? e0 : e1;
   }();
   if (attr != cudaSuccess) return attr;
-  const int pairs = split ? items : std::max(1, std::min((items + kRtC - 1) / kRtC, rt_sm_count() / kRtC));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pairs * kRtC);
+  cfg.gridDim = dim3(split ? items * kRtPair : std::min(items, rt_sm_count()));
   cfg.blockDim = dim3(kRtThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -541,11 +530,11 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   attrs[1].id = cudaLaunchAttributeClusterDimension;
-  attrs[1].val.clusterDim.x = kRtC;
+  attrs[1].val.clusterDim.x = kRtPair;
   attrs[1].val.clusterDim.y = 1;
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = split ? 2 : 1;
   const uint8_t* w_split = static_cast<const uint8_t*>(static_cast<const void*>(w3));
   if (split)
     return cudaLaunchKernelEx(&cfg, k_router_tc<true>, mx, w_split, L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half,
