@@ -130,7 +130,10 @@ size_t moe_workspace_bytes(const moe_layer* layer, int T);
  * zero-filled memory).  Asynchronous on `stream`. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Router and selection (free routing) for T tokens.
+/* Router and selection (free routing) for T tokens: a float32 router scores every routed
+ * expert and the top k = 6 are kept and weighted (page "We Ported Aleph Alpha's Kolibri to a
+ * MacBook. Our Own Gate Said No.", section "The gate": 384 experts, top 6, a float32 router; the
+ * per-expert bias: section 1).
  *   x           [T, d]  bf16 or fp32 (x_dtype)
  *   k           must equal layer->top_k (6)
  *   ids_out     [T, k] int32: selected experts, descending probability, lowest index on ties
@@ -141,7 +144,10 @@ moe_status moe_route(const void* x, moe_dtype x_dtype, int T, const moe_layer* l
                      int32_t* ids_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes,
                      moe_stream_t stream);
 
-/* Grouping of the T*k routed (token, slot) rows by expert, shared expert last:
+/* Grouping of the T*k routed (token, slot) rows by expert, shared expert last: the sorted
+ * grouping that turns the experts into one grouped GEMM (page "We Ported Aleph Alpha's Kolibri
+ * to a MacBook. Our Own Gate Said No.", section 3, update of 5 October: the sorted path and its
+ * row-count edge cases).
  *   counts  [E + 1]   rows per expert; counts[E] = T (the shared expert's rows)
  *   offsets [E + 2]   exclusive prefix sum of counts; offsets[E] = T*k, offsets[E+1] = T*k + T
  *   perm    [T*k + T] token of each row; tokens ascend within each expert (stable)
@@ -166,7 +172,10 @@ moe_status moe_forward(const void* x, moe_dtype x_dtype, int T, const moe_layer*
                        moe_stream_t stream);
 
 /* L layers on a bf16 residual stream, free routing: for l = 0..L-1,
- * r <- bf16_round_nearest_even(r + layer_l(r)).
+ * r <- bf16_round_nearest_even(r + layer_l(r)).  Kolibri-1 stacks 50 such MoE layers (page "We
+ * Ported Aleph Alpha's Kolibri to a MacBook. Our Own Gate Said No.", section "The gate"); the
+ * bf16 residual with one rounding per layer after an fp32 add is this library's reading of the
+ * pages' bf16 activations.
  *   layers    host array of L layer descriptors (read during the call only)
  *   residual  [T, d] bf16, updated in place
  *   ids_out   [L, T, k] int32 or NULL: the experts each layer selected
@@ -202,8 +211,12 @@ moe_status moe_get_status(void* ws, moe_stream_t stream);
  *   Scratch: a fixed 4 MiB + 768 B array inside the library, resident on every GPU that loads
  *   it until the process exits; T * n_experts must be <= 1,048,576, else MOE_ERR_WORKSPACE.
  *   The first call on a device looks up the array's device address (once per device, with
- *   that device current); make that first call before any stream capture.
+ *   that device current); make that first call before any stream capture.  A device reset or
+ *   another CUDA context on the device moves the array: the first call made under the new
+ *   context looks the address up again.
  *   All calls on a device share the array: calls that overlap on the GPU race; serialise them.
+ *   No device-side error can arise in this call (no forced ids, no device-side waits), so it
+ *   has no status record to read: host-side errors are its return value, as for moe_route.
  *   Allocates nothing (no cudaMalloc, no cudaFree). */
 moe_status moe_route_noalloc(const void* x, moe_dtype x_dtype, int T, const moe_layer* layer, int k,
                              int32_t* ids_out, float* w_out, moe_stream_t stream);

@@ -105,6 +105,12 @@ def test_host_validation_rejects_before_any_launch(lib):
     bad_bias.bias_mode = 2
     assert fwd(p, 1, 4, ctypes.byref(bad_bias), None, None, None, None, p, 0, 0, ws, 1 << 40, None) == -1
     assert lib.moe_route(p, 1, 4, ctypes.byref(bad_bias), 6, p, p, None, ws, 1 << 40, None) == -1
+    # the no-allocation router refuses what moe_route refuses, and sizes beyond its scratch
+    assert lib.moe_route_noalloc(p, 1, 4, ctypes.byref(bad_bias), 6, p, p, None) == -1
+    assert lib.moe_route_noalloc(p, 1, 4, ctypes.byref(good), 5, p, p, None) == -2
+    assert lib.moe_route_noalloc(p, 1, (1 << 20) // 384 + 1, ctypes.byref(good), 6, p, p, None) == -3
+    assert lib.moe_route_noalloc(None, 1, 4, ctypes.byref(good), 6, p, p, None) == -1
+    assert lib.moe_route_noalloc(p, 1, 0, ctypes.byref(good), 6, p, p, None) == 0
     # packing: needs E4M3 rows with d, ffn multiples of 128, and four aligned destinations
     pack = lib.moe_pack_weights
     assert pack(ctypes.byref(_layer(binding, F=576)), p, p, p, p, None) == -2
