@@ -326,8 +326,10 @@ def run_ours(args):
     e2e = {"value": replica_throughput(T, args.steps, world, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2}
 
+    l2_label = f"inputs larger than L2: {len(layers)} weight copies rotated across steps"
     extra = {"layer_hbm_frac": layer_frac, "layer_bytes_per_step": nbytes, "unique_experts": U,
              "stage_ms": stage_ms, "traced_ms_per_step": traced_ms}
+    extra["w8a8_drift_T64"] = w8a8_drift(w, x_host, y, ids, wt)
     if not args.no_extra:
         for Tx in (1, 8):
             extra[f"decode_T{Tx}"] = small_batch(moe, g, layers, Tx, args, hbm_peak, flags)
@@ -349,7 +351,7 @@ def run_ours(args):
         "dtype": "e4m3 weights, bf16 activations, fp32 accumulate (W8A8)", "data": "synthetic (seeded)",
         "config": {"workload": f"kolibri moe layer decode T={T} (d=2048, ffn=640, 384 experts top-6 + 1 shared, "
                                f"E4M3 weights, bias N(0,0.5))", "tokens": T, "layers": 1,
-                   "l2": f"inputs larger than L2: {len(layers)} weight copies rotated across steps",
+                   "l2": l2_label,
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "clocks": clocks, "e2e": e2e,
         "gpu_launches": args.steps * KERNELS_PER_FORWARD, "device_status": status, "extra": extra,
@@ -473,8 +475,63 @@ def small_batch(moe, g, layers, T, args, hbm_peak, flags=0):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / (reps * n)
     nbytes, U = layer_bytes(ids.cpu().numpy(), T)
+    stage_ms, traced_ms = traced_stages(moe, layers, x, ws, y, ids, wt, flags, iters=min(200, args.steps))
     return {"tokens_per_s": T / (ms * 1e-3), "ms_per_layer": ms, "unique_experts": U, "bytes": nbytes,
-            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "timing": f"CUDA graph over {n} layer copies"}
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "timing": f"CUDA graph over {n} layer copies",
+            "stage_ms": stage_ms, "traced_ms_per_layer": traced_ms,
+            "stage_note": "eager launches with an event at every stage boundary (each stage waits for the "
+                          "previous one to finish), so the stages sum to more than the graphed layer time"}
+
+
+def traced_stages(moe, layers, x, ws, y, ids, wt, flags, iters):
+    """Mean duration of each kernel stage: eager forwards over the rotated layer copies with
+    events at the stage boundaries."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.binding.TRACE_POINTS)] for _ in range(iters)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for i in range(iters):
+        moe.forward(x, layers[i % len(layers)], ws, out=y, ids=ids, w=wt, events=evs[i], flags=flags)
+    torch.cuda.synchronize()
+    stage = {nm: statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(iters))
+             for k, nm in enumerate(moe.binding.TRACE_STAGES)}
+    return stage, statistics.mean(evs[i][0].elapsed_time(evs[i][-1]) for i in range(iters))
+
+
+def w8a8_drift(w, x_host, y_dev, ids_dev, w_dev):
+    """Distance of the GPU layer (W8A8: E4M3 weights and per-row E4M3 activations) from a W8A16
+    evaluation of the same layer: dequantised E4M3 weights times their row scales, activations
+    kept in fp32, the GPU's own ids and routing weights, evaluated with torch on the host in
+    float64.  Reported, not gated (the activation quantisation is this library's reading of the
+    pages' FP8 contractions)."""
+    import torch
+    T = x_host.shape[0]
+    x = torch.from_numpy((x_host.astype(np.uint32) << 16).view(np.float32)).double()
+    ids = ids_dev.cpu().numpy()
+    wts = torch.from_numpy(w_dev.cpu().numpy()).double()
+    y_gpu = y_dev.float().cpu().double()
+
+    def deq(codes, scales):
+        return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double() * \
+            torch.from_numpy(np.ascontiguousarray(scales)).double()[:, None]
+
+    def ffn(gu, sgu, dn, sd, xs):
+        g_ = xs @ deq(gu[0], sgu[0]).T
+        u_ = xs @ deq(gu[1], sgu[1]).T
+        return (g_ / (1 + torch.exp(-g_)) * u_) @ deq(dn, sd).T
+
+    y_ref = ffn(w.sh_Wgu, w.sh_sgu, w.sh_Wd, w.sh_sd, x)
+    for e in np.unique(ids):
+        tt, slot = np.nonzero(ids == e)
+        ye = ffn(w.Wgu[e], w.sgu[e], w.Wd[e], w.sd[e], x[tt])
+        y_ref[tt] += wts[tt, slot][:, None] * ye
+    diff = y_gpu - y_ref
+    return {"rel_l2": float(diff.norm() / y_ref.norm()),
+            "max_err_frac": float(diff.abs().max() / y_ref.abs().max()), "tokens": T,
+            "reference": "W8A16 on the host (torch float64, dequantised E4M3 weights, fp32 activations, "
+                         "the GPU's ids and weights)"}
 
 
 def zipf_forced(moe, g, layers, args, hbm_peak, flags=0, T=128):

@@ -54,7 +54,9 @@ typedef enum {
   MOE_ERR_WORKSPACE = -3,     /* ws_bytes < moe_workspace_bytes() */
   MOE_ERR_BAD_FORCED_ID = -4, /* a forced id was out of range or repeated within a token */
   MOE_ERR_TIMEOUT = -5,       /* a device-side wait gave up */
-  MOE_ERR_CUDA = -6           /* a CUDA runtime call failed */
+  MOE_ERR_CUDA = -6,          /* a CUDA runtime call failed */
+  MOE_ERR_INDEX = -7          /* MOE_DEBUG builds only: a kernel's index check failed (an internal
+                                 error of the library; the access was kept inside its buffer) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;

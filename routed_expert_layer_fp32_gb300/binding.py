@@ -20,7 +20,7 @@ LAYOUT_ROWS, LAYOUT_TILED = 0, 1
 BIAS_SCORE, BIAS_SELECT = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC = 0, 1, 2
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
-          -4: "MOE_ERR_BAD_FORCED_ID", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_CUDA"}
+          -4: "MOE_ERR_BAD_FORCED_ID", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_CUDA", -7: "MOE_ERR_INDEX"}
 
 # every entry point include/libmoe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward",
@@ -55,32 +55,46 @@ def lib():
     """The loaded libmoe.so.  Raises if it has not been built (no CPU fallback exists)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise ImportError(f"libmoe.so not built ({LIB_PATH}); run __graft_entry__.build()")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, i32, i64, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint
-        L.moe_workspace_bytes.argtypes = [vp, i32]
-        L.moe_workspace_bytes.restype = sz
-        L.moe_workspace_init.argtypes = [vp, sz, vp]
-        L.moe_route.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
-        L.moe_dispatch.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
-        L.moe_forward.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, u32, vp, sz, vp]
-        L.moe_forward_stack.argtypes = [vp, i32, vp, i32, vp, u32, vp, sz, vp]
-        L.moe_forward_traced.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, u32, vp, sz, vp, vp]
-        L.moe_forward_stack_traced.argtypes = [vp, i32, vp, i32, vp, u32, vp, sz, vp, vp]
-        L.moe_get_status.argtypes = [vp, vp]
-        L.moe_status_string.argtypes = [i32]
-        L.moe_status_string.restype = ctypes.c_char_p
-        L.moe_e4m3_encode.argtypes = [vp, vp, i64, vp]
-        L.moe_route_noalloc.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
-        L.moe_selftest_wait_timeout.argtypes = [vp, sz, u32, vp]
-        L.moe_pack_weights.argtypes = [vp, vp, vp, vp, vp, vp]
-        for f in ("moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward", "moe_forward_stack",
-                  "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status", "moe_e4m3_encode",
-                  "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_pack_weights"):
-            getattr(L, f).restype = i32
-        _lib = L
+        _lib = load(LIB_PATH)
     return _lib
+
+
+def use_library(path: Optional[str]):
+    """Route every call of this module through the libmoe build at `path` (e.g. the MOE_DEBUG
+    build); None goes back to libmoe.so.  Returns the library in use before."""
+    global _lib
+    before = _lib
+    _lib = load(path) if path else None
+    return before
+
+
+def load(path: str):
+    """A libmoe build at `path` with every entry point's argument and result types set."""
+    if not os.path.exists(path):
+        raise ImportError(f"libmoe not built ({path}); run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint
+    L.moe_workspace_bytes.argtypes = [vp, i32]
+    L.moe_workspace_bytes.restype = sz
+    L.moe_workspace_init.argtypes = [vp, sz, vp]
+    L.moe_route.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
+    L.moe_dispatch.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_forward.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, u32, vp, sz, vp]
+    L.moe_forward_stack.argtypes = [vp, i32, vp, i32, vp, u32, vp, sz, vp]
+    L.moe_forward_traced.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, u32, vp, sz, vp, vp]
+    L.moe_forward_stack_traced.argtypes = [vp, i32, vp, i32, vp, u32, vp, sz, vp, vp]
+    L.moe_get_status.argtypes = [vp, vp]
+    L.moe_status_string.argtypes = [i32]
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_e4m3_encode.argtypes = [vp, vp, i64, vp]
+    L.moe_route_noalloc.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
+    L.moe_selftest_wait_timeout.argtypes = [vp, sz, u32, vp]
+    L.moe_pack_weights.argtypes = [vp, vp, vp, vp, vp, vp]
+    for f in ("moe_workspace_init", "moe_route", "moe_dispatch", "moe_forward", "moe_forward_stack",
+              "moe_forward_traced", "moe_forward_stack_traced", "moe_get_status", "moe_e4m3_encode",
+              "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_pack_weights"):
+        getattr(L, f).restype = i32
+    return L
 
 
 def status_string(status: int) -> str:

@@ -142,7 +142,7 @@ moe_status run_layer(const void* x, moe_dtype x_dtype, int T, const moe_layer* L
   MOE_TRY(mark(6));
   MOE_TRY(use_tc ? launch_down_tc(L, T, lay, base, s) : launch_down_stream(L, T, lay, base, s));
   MOE_TRY(mark(7));
-  MOE_TRY(launch_combine(base + lay.y_rows, pos, w, T, L, y, y_dtype, residual_add, s));
+  MOE_TRY(launch_combine(base + lay.y_rows, pos, w, T, L, y, y_dtype, residual_add, &st->flags, s));
   MOE_TRY(mark(8));
   return MOE_OK;
 }
@@ -320,6 +320,7 @@ moe_status moe_get_status(void* ws, moe_stream_t stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(ws, 0, sizeof(DevStatus)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h.flags & kFlagIndex) return MOE_ERR_INDEX;
   if (h.flags & kFlagBadForced) return MOE_ERR_BAD_FORCED_ID;
   if (h.flags & kFlagTimeout) return MOE_ERR_TIMEOUT;
   return MOE_OK;
@@ -334,6 +335,7 @@ const char* moe_status_string(moe_status status) {
     case MOE_ERR_BAD_FORCED_ID: return "a forced expert id was out of range or repeated within a token";
     case MOE_ERR_TIMEOUT: return "a device-side wait timed out";
     case MOE_ERR_CUDA: return "a CUDA runtime call failed";
+    case MOE_ERR_INDEX: return "an index check of a MOE_DEBUG build failed (an internal error)";
   }
   return "unknown status";
 }

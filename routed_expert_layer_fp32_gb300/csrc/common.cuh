@@ -173,6 +173,53 @@ __device__ __forceinline__ void pdl_trigger_then_wait() {
 
 __device__ __forceinline__ void set_status(DevStatus* st, int flag) { atomicOr(&st->flags, flag); }
 
+// ---- MOE_DEBUG builds: index checks -------------------------------------------------------
+// Compiled with -DMOE_DEBUG, the kernels check every data-dependent index they read (tile
+// descriptors, tokens in perm, rows in pos) against the buffers it addresses.  A failed check
+// records kFlagIndex and the site in the status record (moe_get_status returns
+// MOE_ERR_INDEX) and the access is redirected to an index inside the buffer, so the kernel
+// finishes without touching memory outside its buffers; nothing traps.  Release builds
+// compile the checks away.
+constexpr int kFlagIndex = 4;
+#ifdef MOE_DEBUG
+constexpr bool kDebugIndexChecks = true;
+#else
+constexpr bool kDebugIndexChecks = false;
+#endif
+
+__device__ __forceinline__ void report_index(int* status_flags, int site) {
+  atomicOr(status_flags, kFlagIndex);
+  atomicCAS(status_flags + 2, 0, 1000 + site);
+}
+
+// Tile i of a tile list as an expert kernel reads it.  Debug builds check the group (<= E, the
+// shared expert being group E), the rows (inside [0, R)) and the height (1 .. max_rows), and
+// replace a bad tile by a clamped one; every role of a kernel reads its tiles through this, so
+// the roles stay in step whatever they read.
+__device__ __forceinline__ Tile checked_tile(const Tile* tiles, int i, int E, int R, int max_rows, int* status_flags,
+                                             int site) {
+  Tile t = tiles[i];
+  if (kDebugIndexChecks) {
+    const int hmax = min(max_rows, R);
+    if (!(t.group >= 0 && t.group <= E && t.nrows >= 1 && t.nrows <= hmax && t.row0 >= 0 && t.row0 <= R - t.nrows)) {
+      report_index(status_flags, site);
+      t.group = min(max(t.group, 0), E);
+      t.nrows = min(max(t.nrows, 1), hmax);
+      t.row0 = min(max(t.row0, 0), R - t.nrows);
+    }
+  }
+  return t;
+}
+
+// A token index read from perm: debug builds check 0 <= t < T (token 0 replaces a bad one).
+__device__ __forceinline__ int checked_token(int t, int T, int* status_flags, int site) {
+  if (kDebugIndexChecks && (t < 0 || t >= T)) {
+    report_index(status_flags, site);
+    return 0;
+  }
+  return t;
+}
+
 // Record a device-side timeout: flags |= kFlagTimeout, and the first site that gave up.
 __device__ __forceinline__ void report_timeout_flag(int* status_flags, int site) {
   atomicOr(status_flags, kFlagTimeout);
@@ -263,6 +310,6 @@ cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char*
 cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s);
 cudaError_t launch_combine(const void* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L,
-                           void* y, moe_dtype y_dtype, bool residual_add, cudaStream_t s);
+                           void* y, moe_dtype y_dtype, bool residual_add, int* status_flags, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
 }  // namespace moe

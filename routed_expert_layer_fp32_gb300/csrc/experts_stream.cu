@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) k_act_quant(const XT* __restrict__ x, int
 
 // ------------------------------------------------------------ gate/up, FP8 -----------------
 struct ExpertArgs {
-  int d, F, E;
+  int d, F, E, T, R;  // R = T (k + 1) rows
   const uint8_t* wgu;
   const float* sgu;
   const uint8_t* wd;
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
         if (lane == 0) report_timeout(status_flags, 1);
         break;
       }
-      const Tile tl = a.tiles[item / nblk];
+      const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kStreamRows, status_flags, 11);
       const int n0 = (item % nblk) * 16;
       const uint8_t* Wg = tl.group == a.E ? a.sh_wgu : a.wgu + size_t(tl.group) * 2 * a.F * a.d;
       uint8_t* st = gu_smem + s * stage_bytes;
@@ -192,7 +192,8 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
       const uint8_t* src = Wg + (lane < 16 ? size_t(n0 + lane) : size_t(a.F + n0 + lane - 16)) * a.d;
       bulk_g2s_stream(st + lane * rs, src, a.d, &ctl->full[s], pol);
       if (lane < tl.nrows)
-        bulk_g2s(st + (32 + lane) * rs, a.xq + size_t(a.perm[tl.row0 + lane]) * a.d, a.d, &ctl->full[s]);
+        bulk_g2s(st + (32 + lane) * rs, a.xq + size_t(checked_token(a.perm[tl.row0 + lane], a.T, status_flags, 12)) * a.d,
+                 a.d, &ctl->full[s]);
     }
     pipe_drain(ctl, kGuStages, j);
     return;
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
       if (lane == 0) report_timeout(status_flags, 2);
       break;
     }
-    const Tile tl = a.tiles[item / nblk];
+    const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kStreamRows, status_flags, 13);
     const int n0 = (item % nblk) * 16;
     const int ntg = (tl.nrows + 7) >> 3;
     const uint8_t* st = gu_smem + s * stage_bytes;
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_gateup_fp8(ExpertArgs a, int
         const int n = n0 + gq + ((c & 2) ? 8 : 0);
         if (r < tl.nrows) {
           const int row = tl.row0 + r;
-          const float sx = a.sx[a.perm[row]];
+          const float sx = a.sx[checked_token(a.perm[row], a.T, status_flags, 14)];
           const float gv = gsum * sx * sg[n];
           const float uv = usum * sx * su[n];
           a.h[size_t(row) * a.F + n] = silu(gv) * uv;
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_down_fp8(ExpertArgs a, int* 
         if (lane == 0) report_timeout(status_flags, 3);
         break;
       }
-      const Tile tl = a.tiles[item / nblk];
+      const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kStreamRows, status_flags, 15);
       const int m0 = (item % nblk) * 64;
       const uint8_t* W = tl.group == a.E ? a.sh_wd : a.wd + size_t(tl.group) * a.d * a.F;
       uint8_t* st = dn_smem + s * stage_bytes;
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_down_fp8(ExpertArgs a, int* 
       if (lane == 0) report_timeout(status_flags, 4);
       break;
     }
-    const Tile tl = a.tiles[item / nblk];
+    const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kStreamRows, status_flags, 16);
     const int mw = warp * 16;  // this warp's columns within the item
     const int m0 = (item % nblk) * 64 + mw;
     const int ntg = (tl.nrows + 7) >> 3;
@@ -490,7 +491,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // extra CTA hides more latency; 3 otherwise, without the spills the 64-register cap costs)
 template <typename OT, bool kResidual, typename YT, int kMinCtas>
 __global__ void __launch_bounds__(256, kMinCtas) k_combine(const YT* __restrict__ y_rows, const int32_t* __restrict__ pos,
-                                                 const float* __restrict__ w, int T, int d, int k, OT* __restrict__ out) {
+                                                 const float* __restrict__ w, int T, int d, int k, OT* __restrict__ out,
+                                                 int* status_flags) {
   // A few CTAs per SM walk the tokens; a token's slots (rows and weights) are loaded while the
   // previous token's rows are in flight.  The first token's slots come from the dispatch,
   // which completed before the kernel this launch overlaps started: read before the wait.
@@ -501,6 +503,10 @@ __global__ void __launch_bounds__(256, kMinCtas) k_combine(const YT* __restrict_
     for (int i = 0; i < kTopK; ++i) {
       const bool ok = t < T && i < k;
       r[i] = ok ? pos[size_t(t) * k + i] : -1;
+      if (kDebugIndexChecks && r[i] >= k * T) {  // a routed row lies in [0, kT); -1 marks a dropped slot
+        report_index(status_flags, 17);
+        r[i] = -1;
+      }
       ww[i] = ok ? w[size_t(t) * k + i] : 0.0f;
     }
   };
@@ -583,6 +589,8 @@ ExpertArgs expert_args(const LayerDev& L, const WsLayout& ws, char* base) {
   a.d = L.d;
   a.F = L.F;
   a.E = L.E;
+  a.T = ws.T;
+  a.R = ws.R;
   a.wgu = L.wgu;
   a.sgu = L.sgu;
   a.wd = L.wd;
@@ -660,31 +668,32 @@ cudaError_t launch_down_stream(const LayerDev& L, int T, const WsLayout& ws, cha
 
 template <typename YT, int kMinCtas>
 cudaError_t launch_combine_k(const YT* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
-                             moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+                             moe_dtype y_dtype, bool residual_add, int* status_flags, cudaStream_t s) {
   const dim3 grid(std::max(1, std::min(T, num_sms() * kMinCtas)));
   if (y_dtype == MOE_F32)
     return launch_pdl(k_combine<float, false, YT, kMinCtas>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
-                      (float*)y);
+                      (float*)y, status_flags);
   if (residual_add)
     return launch_pdl(k_combine<__nv_bfloat16, true, YT, kMinCtas>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d,
-                      L.k, (__nv_bfloat16*)y);
+                      L.k, (__nv_bfloat16*)y, status_flags);
   return launch_pdl(k_combine<__nv_bfloat16, false, YT, kMinCtas>, grid, dim3(256), 0, s, y_rows, pos, w, T, L.d, L.k,
-                    (__nv_bfloat16*)y);
+                    (__nv_bfloat16*)y, status_flags);
 }
 
 template <typename YT>
 cudaError_t launch_combine_t(const YT* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
-                             moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+                             moe_dtype y_dtype, bool residual_add, int* status_flags, cudaStream_t s) {
   if (T > num_sms() * 8)  // CTAs walk several tokens each
-    return launch_combine_k<YT, 4>(y_rows, pos, w, T, L, y, y_dtype, residual_add, s);
-  return launch_combine_k<YT, 3>(y_rows, pos, w, T, L, y, y_dtype, residual_add, s);
+    return launch_combine_k<YT, 4>(y_rows, pos, w, T, L, y, y_dtype, residual_add, status_flags, s);
+  return launch_combine_k<YT, 3>(y_rows, pos, w, T, L, y, y_dtype, residual_add, status_flags, s);
 }
 
 cudaError_t launch_combine(const void* y_rows, const int32_t* pos, const float* w, int T, const LayerDev& L, void* y,
-                           moe_dtype y_dtype, bool residual_add, cudaStream_t s) {
+                           moe_dtype y_dtype, bool residual_add, int* status_flags, cudaStream_t s) {
   if (L.fp8)
-    return launch_combine_t(static_cast<const __nv_bfloat16*>(y_rows), pos, w, T, L, y, y_dtype, residual_add, s);
-  return launch_combine_t(static_cast<const float*>(y_rows), pos, w, T, L, y, y_dtype, residual_add, s);
+    return launch_combine_t(static_cast<const __nv_bfloat16*>(y_rows), pos, w, T, L, y, y_dtype, residual_add,
+                            status_flags, s);
+  return launch_combine_t(static_cast<const float*>(y_rows), pos, w, T, L, y, y_dtype, residual_add, status_flags, s);
 }
 
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s) {

@@ -55,7 +55,7 @@ constexpr int kSplitMaxT = 16;  // gate/up k-steps split over a CTA pair up to t
 constexpr int kGateUpPairChunkMaxN = 32;  // gate/up stages of two k-chunks up to this tile width
 
 struct TcArgs {
-  int d, F, E, T;
+  int d, F, E, T, R;  // R = T (k + 1) rows
   const uint8_t* w;    // tiled weights of the routed experts (gate/up or down)
   const uint8_t* wsh;  // the shared expert's, same layout
   const Tile* tiles;
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int budget = kPrefetchBytes;
       const int known = kGateUp ? ((a.T + kN - 1) / kN) * nblk : *a.n_tiles * nblk;
       for (int item = unit; item < known && budget > 0; item += n_units) {
-        const Tile tl = kGateUp ? Tile{a.E, 0, 0, 0} : a.tiles[item / nblk];
+        const Tile tl = kGateUp ? Tile{a.E, 0, 0, 0} : checked_tile(a.tiles, item / nblk, a.E, a.R, kN, a.status_flags, 1);
         for (int ks = ks_lo; ks < ks_hi && budget > 0; ++ks, budget -= kCopies * int(kCopyBytes))
           for (int ai = 0; ai < kCopies; ++ai) prefetch_l2_bulk(w_src(tl, item % nblk, ai, ks * kC), kCopyBytes);
       }
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int it = 0;
     bool stop = false;
     for (int item = unit; item < total && !stop; item += n_units) {
-      const Tile tl = a.tiles[item / nblk];
+      const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kN, a.status_flags, 2);
       const int nb = item % nblk;
       // the tokens of this lane's rows: gather4 lanes own rows 4l..4l+3; cp.async lanes own
       // 16-byte column l % 8 of rows l / 8 + 4j
@@ -220,11 +220,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int i = 0; i < kG; ++i) g[i] = 0;
       if (kGateUp) {
-        const int first = a.perm[tl.row0];
+        const int first = checked_token(a.perm[tl.row0], a.T, a.status_flags, 3);
 #pragma unroll
         for (int i = 0; i < kG; ++i) {
           const int r = C::kLdgsts ? (lane >> 3) + 4 * i : 4 * lane + i;
-          g[i] = (r < tl.nrows && (C::kLdgsts || 4 * lane < kN)) ? a.perm[tl.row0 + r] : first;
+          g[i] = (r < tl.nrows && (C::kLdgsts || 4 * lane < kN)) ? checked_token(a.perm[tl.row0 + r], a.T, a.status_flags, 3)
+                                                                 : first;
         }
       }
       for (int ks = ks_lo; ks < ks_hi; ++ks, ++it) {
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const Tile tl = a.tiles[item / nblk];
+      const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kN, a.status_flags, 4);
       const int nb = item % nblk;
       const bool shared = tl.group == a.E;
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(b * C::kColsPerAcc);
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           load_acc(0, c0, gv);
           load_acc(1, c0, uv);
           // lane i < 16 fetches the scale of token c0 + i; shuffles hand it to every lane
-          const float sx_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sx[a.perm[tl.row0 + c0 + lane]] : 0.0f;
+          const float sx_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sx[checked_token(a.perm[tl.row0 + c0 + lane], a.T, a.status_flags, 5)] : 0.0f;
           float* hp = a.h + size_t(tl.row0 + c0) * a.F + n;
           if (c0 + 16 <= tl.nrows) {
 #pragma unroll
@@ -526,6 +527,7 @@ cudaError_t launch_down_n(int kN, int kA, int kC, const CUtensorMap& mx, const T
 TcArgs tc_args(const LayerDev& L, int T, const WsLayout& ws, char* base) {
   TcArgs a;
   a.T = T;
+  a.R = T * (L.k + 1);
   a.d = L.d;
   a.F = L.F;
   a.E = L.E;

@@ -399,6 +399,73 @@ def test_large_prefill_sampled_rows(moe, kolibri, T):
     assert moe.get_status(ws) == 0
 
 
+def _edge_ids(counts, T, E=384, first_filler=100):
+    """Forced ids for T tokens in which edge expert j (ids 10 + j) holds exactly counts[j] rows
+    (tokens 0 .. counts[j] - 1); each token's remaining slots take filler experts
+    first_filler, first_filler + 1, ... in turn (never an edge expert)."""
+    ids = np.zeros((T, 6), np.int32)
+    nxt = 0
+    n_fill = E - first_filler
+    for t in range(T):
+        row = [10 + j for j, c in enumerate(counts) if t < c]
+        while len(row) < 6:
+            row.append(first_filler + nxt % n_fill)
+            nxt += 1
+        ids[t] = row
+    return ids
+
+
+def _check_sampled_forced(w, x, fid, y, ids, extra_rows, where, n=40):
+    """Forced ids bit-exact; outputs of a seeded row sample plus the given rows against the
+    oracle (every token is independent, so a row sample is exact for those rows)."""
+    assert np.array_equal(ids.cpu().numpy(), fid), f"{where}: forced ids not bit-exact"
+    T = x.shape[0]
+    rows = np.unique(np.concatenate([np.random.default_rng(T).choice(T, n, replace=False),
+                                     np.array([r for r in extra_rows if 0 <= r < T], np.int64)]))
+    ref = o.layer_forward(o.Layer(w), x[rows], forced_ids=fid[rows], nthreads=o.default_threads())
+    ok, msg = parity.outputs_ok(y.float().cpu().numpy()[rows], ref["y"])
+    assert ok, f"{where}: {msg}"
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_one_expert_set_holds_every_row(moe, kolibri, path):
+    """The pages' first wave, 8 x 1,099 x 6 = 52,752 routed rows ("We Ported Aleph Alpha's
+    Kolibri to a MacBook. Our Own Gate Said No.", section 3, update of 5 October), all on one
+    set of six experts: 8,792 tokens forced to the same experts, so six groups of 8,792 rows and
+    the shared expert's 8,792 (long runs of full tiles of one expert; 8,792 is not a multiple of
+    the tile height)."""
+    w, L = kolibri.w, kolibri.for_path(path)
+    T = 8 * 1099
+    fid = np.tile(np.array([[200, 3, 377, 41, 96, 250]], np.int32), (T, 1))
+    assert fid.size == 52752
+    x = g.make_x(401, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, _ = moe.forward(to_dev_x(x), L, ws, forced_ids=torch.from_numpy(fid).cuda(), flags=PATHS[path])
+    _check_sampled_forced(w, x, fid, y, ids, [0, 127, 128, T - 1], f"52,752 rows, {path}")
+    assert moe.get_status(ws) == 0
+
+
+def test_grouped_gemm_row_count_edges(moe, kolibri):
+    """Groups of exactly 32,767, 32,768, 32,769, 32,832, 33,000 and 34,000 rows in one call: the
+    row counts around 2^15 at which the pages' sorted grouped GEMM went wrong (32,769, 33,000,
+    34,000) or stayed right (32,768, 32,832) ("We Ported Aleph Alpha's Kolibri to a MacBook. Our
+    Own Gate Said No.", section 3, update of 5 October), 34,000 tokens forced so that six experts
+    hold those counts, on the tcgen05 grouped GEMMs.  Rows at every group boundary are among the
+    sampled rows."""
+    w, L = kolibri.w, kolibri.tiled
+    counts = [32767, 32768, 32769, 32832, 33000, 34000]
+    T = max(counts)
+    fid = _edge_ids(counts, T)
+    per_expert = np.bincount(fid.ravel(), minlength=384)
+    assert [int(per_expert[10 + j]) for j in range(6)] == counts
+    x = g.make_x(402, T, w.d, bf16=True)
+    ws = moe.workspace(L, T)
+    y, ids, _ = moe.forward(to_dev_x(x), L, ws, forced_ids=torch.from_numpy(fid).cuda(), flags=PATHS["tc"])
+    edges = [c + dd for c in counts for dd in (-1, 0)]
+    _check_sampled_forced(w, x, fid, y, ids, edges, "row-count edges")
+    assert moe.get_status(ws) == 0
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_batched_decode_zipf_forced(moe, kolibri, path):
     w, L = kolibri.w, kolibri.for_path(path)
