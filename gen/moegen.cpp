@@ -15,6 +15,7 @@
 // Weight quantisation recipe (input preparation, the "converted checkpoint"): each output
 // row r of a weight matrix is stored as E4M3 codes of w/s_r with s_r = max|w_r| / 448
 // (s_r = 1 for an all-zero row), rounded to nearest, ties to even code, saturating at 448.
+// The 4-bit checkpoint stores E2M1 codes of w/s_r with s_r = max|w_r| / 6 the same way.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -104,6 +105,26 @@ inline uint8_t quant_e4m3(float v) {
   return sign | uint8_t(code);
 }
 
+// Nearest E2M1 code of v (OCP Microscaling v1.0, 4-bit element format E2M1: magnitudes 0,
+// 0.5, 1, 1.5, 2, 3, 4, 6 in code order 0..7, sign in bit 3), ties to the code with mantissa
+// bit 0, saturating at +-6: brute force over the eight magnitudes in double.
+inline uint8_t quant_e2m1(float v) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const uint8_t sign = std::signbit(v) ? 8 : 0;
+  const double a = std::fabs(double(v));
+  if (!(a == a)) return 0;
+  int best = 0;
+  double bestd = a;
+  for (int c = 1; c < 8; ++c) {
+    const double dd = std::fabs(a - mag[c]);
+    if (dd < bestd || (dd == bestd && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      bestd = dd;
+    }
+  }
+  return uint8_t(sign | best);
+}
+
 inline uint16_t bf16_bits(float f) {
   uint32_t u;
   std::memcpy(&u, &f, 4);
@@ -169,6 +190,34 @@ void moegen_normal_e4m3_rows(uint64_t seed, uint32_t layer, uint32_t tensor, int
       for (int64_t i = 0; i < cols; ++i) dst[i] = quant_e4m3(buf[size_t(i)] / s);
     }
   });
+}
+
+// The 4-bit checkpoint: rows [row0, row0 + rows) of the same Gaussian matrix, each row stored
+// as E2M1 codes of w/s with s = rowabsmax / 6 (1 for an all-zero row), two codes per byte
+// (element 2i in the low nibble of byte i).  codes: [rows, cols / 2], scales: [rows].
+void moegen_normal_e2m1_rows(uint64_t seed, uint32_t layer, uint32_t tensor, int64_t row0, int64_t rows,
+                             int64_t cols, double var, uint8_t* codes, float* scales, int nthreads) {
+  uint64_t st = stream_state(seed, layer, tensor);
+  float sd = float(std::sqrt(var));
+  parallel_rows(rows, nthreads, [&](int64_t a, int64_t b) {
+    std::vector<float> buf(static_cast<size_t>(cols));
+    for (int64_t r = a; r < b; ++r) {
+      uint64_t base = uint64_t(row0 + r) * uint64_t(cols);
+      float amax = 0.0f;
+      for (int64_t c = 0; c < cols; ++c) buf[size_t(c)] = sd * normal_at(st, base + uint64_t(c));
+      for (int64_t i = 0; i < cols; ++i) amax = std::max(amax, std::fabs(buf[size_t(i)]));
+      float s = amax > 0.0f ? amax / 6.0f : 1.0f;
+      scales[r] = s;
+      uint8_t* dst = codes + r * (cols / 2);
+      for (int64_t i = 0; i < cols; i += 2)
+        dst[i / 2] = uint8_t(quant_e2m1(buf[size_t(i)] / s) | (quant_e2m1(buf[size_t(i + 1)] / s) << 4));
+    }
+  });
+}
+
+// Codes of single values (for the generator's own tests).
+void moegen_quant_e2m1_n(const float* v, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = quant_e2m1(v[i]);
 }
 
 // Quantise caller-supplied fp32 rows with the same recipe (used for hand-built weights).

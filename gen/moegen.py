@@ -56,11 +56,13 @@ def lib():
         L.moegen_normal_bf16.argtypes = [u64, u32, u32, u64, i64, dbl, vp, i32]
         L.moegen_normal_e4m3_rows.argtypes = [u64, u32, u32, i64, i64, i64, dbl, vp, vp, i32]
         L.moegen_quant_rows_e4m3.argtypes = [vp, i64, i64, vp, vp]
+        L.moegen_normal_e2m1_rows.argtypes = [u64, u32, u32, i64, i64, i64, dbl, vp, vp, i32]
+        L.moegen_quant_e2m1_n.argtypes = [vp, i64, vp]
         L.moegen_zipf_ids.argtypes = [u64, u32, u32, i32, i32, i32, dbl, vp]
         L.moegen_dirichlet_w.argtypes = [u64, u32, u32, i32, i32, vp]
         L.moegen_uniform_int.argtypes = [u64, u32, u32, i64, i64, vp]
         for f in ("moegen_normal_f32", "moegen_normal_bf16", "moegen_normal_e4m3_rows",
-                  "moegen_quant_rows_e4m3", "moegen_zipf_ids", "moegen_dirichlet_w", "moegen_uniform_int"):
+                  "moegen_quant_rows_e4m3", "moegen_normal_e2m1_rows", "moegen_quant_e2m1_n", "moegen_zipf_ids", "moegen_dirichlet_w", "moegen_uniform_int"):
             getattr(L, f).restype = None
         _lib = L
     return _lib
@@ -102,6 +104,25 @@ def normal_e4m3_rows(seed, layer, tensor, row0, rows, cols, var, codes=None, sca
     return codes, scales
 
 
+def normal_e2m1_rows(seed, layer, tensor, row0, rows, cols, var, codes=None, scales=None, nthreads=None):
+    """The 4-bit checkpoint of rows [row0, row0 + rows): packed E2M1 codes [rows, cols / 2]
+    (element 2i in the low nibble of byte i) and scales rowabsmax / 6."""
+    if codes is None:
+        codes = np.empty((rows, cols // 2), np.uint8)
+    if scales is None:
+        scales = np.empty((rows,), np.float32)
+    lib().moegen_normal_e2m1_rows(seed, layer, tensor, row0, rows, cols, var, _ptr(codes), _ptr(scales),
+                                  nthreads or default_threads())
+    return codes, scales
+
+
+def quant_e2m1(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().moegen_quant_e2m1_n(_ptr(v), v.size, _ptr(out))
+    return out
+
+
 def quant_rows_e4m3(w: np.ndarray):
     w = np.ascontiguousarray(w, np.float32)
     rows, cols = int(np.prod(w.shape[:-1])), w.shape[-1]
@@ -131,7 +152,8 @@ def uniform_int(seed, count, n, tensor=T_SAMPLE, layer=0):
 
 @dataclass
 class LayerWeights:
-    """Host arrays of one layer.  fp8=True: E4M3 codes + fp32 per-row scales; else fp32."""
+    """Host arrays of one layer.  fp8=True: E4M3 codes + fp32 per-row scales; fp4=True: packed
+    E2M1 codes (two per byte, the last dimension halved) + fp32 per-row scales; else fp32."""
     d: int
     ffn: int
     E: int
@@ -147,19 +169,38 @@ class LayerWeights:
     sh_sgu: Optional[np.ndarray] = None  # [2, ffn]
     sh_sd: Optional[np.ndarray] = None   # [d]
     meta: dict = field(default_factory=dict)
+    fp4: bool = False
 
 
 def make_layer(seed: int, d: int, ffn: int, E: int, fp8: bool, bias_var: Optional[float],
                layer: int = 0, nthreads: Optional[int] = None, out: Optional[dict] = None,
-               down_var: Optional[float] = None) -> LayerWeights:
+               down_var: Optional[float] = None, fp4: bool = False) -> LayerWeights:
     """One layer's weights from the recipe above.  `out` may supply preallocated arrays
     (e.g. pinned host buffers) keyed like the LayerWeights fields.  `down_var` replaces the
-    down-projection variance 1/ffn (used by the stack, see stack_layer)."""
+    down-projection variance 1/ffn (used by the stack, see stack_layer).  fp4=True: the 4-bit
+    checkpoint of the same Gaussian weights (E2M1 codes, scale rowabsmax / 6)."""
     nt = nthreads or default_threads()
     dv = down_var if down_var is not None else 1.0 / ffn
     o = out or {}
     Wr = normal_f32(seed, layer, T_WR, (E, d), 1.0 / d, out=o.get("Wr"), nthreads=nt)
     bias = normal_f32(seed, layer, T_BIAS, (E,), bias_var, out=o.get("bias"), nthreads=nt) if bias_var else None
+    if fp4:
+        Wgu = np.empty((E, 2, ffn, d // 2), np.uint8)
+        sgu = np.empty((E, 2, ffn), np.float32)
+        normal_e2m1_rows(seed, layer, T_WGU, 0, E * 2 * ffn, d, 1.0 / d, Wgu.reshape(E * 2 * ffn, d // 2),
+                         sgu.reshape(-1), nthreads=nt)
+        Wd = np.empty((E, d, ffn // 2), np.uint8)
+        sd = np.empty((E, d), np.float32)
+        normal_e2m1_rows(seed, layer, T_WD, 0, E * d, ffn, dv, Wd.reshape(E * d, ffn // 2), sd.reshape(-1),
+                         nthreads=nt)
+        sh_Wgu = np.empty((2, ffn, d // 2), np.uint8)
+        sh_sgu = np.empty((2, ffn), np.float32)
+        normal_e2m1_rows(seed, layer, T_SH_WGU, 0, 2 * ffn, d, 1.0 / d, sh_Wgu.reshape(2 * ffn, d // 2),
+                         sh_sgu.reshape(-1), nthreads=nt)
+        sh_Wd = np.empty((d, ffn // 2), np.uint8)
+        sh_sd = np.empty((d,), np.float32)
+        normal_e2m1_rows(seed, layer, T_SH_WD, 0, d, ffn, dv, sh_Wd, sh_sd, nthreads=nt)
+        return LayerWeights(d, ffn, E, False, Wr, bias, Wgu, Wd, sh_Wgu, sh_Wd, sgu, sd, sh_sgu, sh_sd, fp4=True)
     if fp8:
         Wgu = o.get("Wgu", np.empty((E, 2, ffn, d), np.uint8))
         sgu = o.get("sgu", np.empty((E, 2, ffn), np.float32))
@@ -211,9 +252,9 @@ def tiny_layer():
     return make_layer(SEED_TINY, TINY["d"], TINY["ffn"], TINY["E"], fp8=False, bias_var=None)
 
 
-def kolibri_layer(seed: int, layer: int = 0, out=None, nthreads=None, down_var=None):
-    return make_layer(seed, KOLIBRI["d"], KOLIBRI["ffn"], KOLIBRI["E"], fp8=True, bias_var=0.5,
-                      layer=layer, out=out, nthreads=nthreads, down_var=down_var)
+def kolibri_layer(seed: int, layer: int = 0, out=None, nthreads=None, down_var=None, fp4: bool = False):
+    return make_layer(seed, KOLIBRI["d"], KOLIBRI["ffn"], KOLIBRI["E"], fp8=not fp4, bias_var=0.5,
+                      layer=layer, out=out, nthreads=nthreads, down_var=down_var, fp4=fp4)
 
 
 # The 50-layer stack applies r <- r + moe(r) with no normalisation; with the single-layer

@@ -28,6 +28,9 @@
 //  - SwiGLU: y = Wd (silu(Wg x) * (Wu x)), silu(z) = z / (1 + exp(-z)), no biases;
 //  - FP8 = OCP E4M3FN (bias 7, max 448, no infinities, NaN 0x7F/0xFF, subnormals kept),
 //    one fp32 scale per output row;
+//  - 4-bit weights (the K4 builds of "We Stopped the Kolibri Benchmark Before Scoring One
+//    Answer", section "What this means if you want Kolibri on a Mac"; the pages give no
+//    format): OCP E2M1 codes with one fp32 scale per output row, activations as for FP8;
 //  - W8A8: activations entering each FP8 contraction are quantised per token (per row)
 //    to E4M3 with scale rowabsmax / 448, round to nearest even, saturating;
 //  - shared expert: weight 1, same shape and format as a routed expert;
@@ -54,6 +57,17 @@ float e4m3_value(uint8_t c) {
   if (e == 15 && m == 7) return std::nanf("");
   if (e == 0) mag = (float(m) / 8.0f) * std::ldexp(1.0f, -6);
   else mag = (1.0f + float(m) / 8.0f) * std::ldexp(1.0f, e - 7);
+  return s ? -mag : mag;
+}
+
+// E2M1 (the 4-bit element format of the OCP Microscaling specification, v1.0, section
+// 5.3.3) decode by the format's definition: s ee m, exponent bias 1, no infinities or NaN.
+//   e == 0:   (-1)^s * m/2                 (subnormal: 0 or 0.5)
+//   e  > 0:   (-1)^s * (1 + m/2) * 2^(e-1)
+// The magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+float e2m1_value(uint8_t c) {
+  int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  float mag = (e == 0) ? float(m) * 0.5f : (1.0f + float(m) * 0.5f) * std::ldexp(1.0f, e - 1);
   return s ? -mag : mag;
 }
 
@@ -128,7 +142,9 @@ enum { OR_ACT_W8A8 = 0, OR_ACT_W8A16 = 1 };
 
 typedef struct {
   int d, ffn, E, k;        // d_model, expert hidden width, routed experts, experts per token
-  int w_fp8;               // 1: E4M3 codes + per-row fp32 scales; 0: fp32 weights
+  int w_fp8;               // 1: E4M3 codes + per-row fp32 scales; 0: fp32 weights;
+                           // 2: E2M1 codes + per-row fp32 scales, two codes per byte (element
+                           //    2i in the low nibble of byte i), so a row of K weights is K/2 bytes
   int act_mode;            // OR_ACT_W8A8 (default) or OR_ACT_W8A16 (fp32 activations)
   int mutant;              // OR_MUT_*
   const float* Wr;         // [E, d]
@@ -145,6 +161,7 @@ typedef struct {
 } oracle_layer;
 
 float oracle_e4m3_decode(uint8_t c) { return kDec.v[c]; }
+float oracle_e2m1_decode(uint8_t c) { return e2m1_value(uint8_t(c & 15)); }
 uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }
 uint16_t oracle_bf16_rne(float f) { return f32_to_bf16(f); }
 void oracle_e4m3_encode_n(const float* v, int64_t n, uint8_t* out) {
@@ -242,9 +259,18 @@ void oracle_expert(const oracle_layer* L, int e, const float* xf, float* ye) {
     }
     return;
   }
-  const uint8_t* Wg = shared ? (const uint8_t*)L->sh_Wgu : (const uint8_t*)L->Wgu + size_t(e) * 2 * F * d;
-  const uint8_t* Wu = Wg + size_t(F) * d;
-  const uint8_t* Wd = shared ? (const uint8_t*)L->sh_Wd : (const uint8_t*)L->Wd + size_t(e) * d * F;
+  // quantised weights: E4M3 (one byte per weight) or E2M1 (two weights per byte); a matrix of
+  // rows of K weights, the value of weight (row, k) before its row scale
+  const bool w4 = (L->w_fp8 == 2);
+  auto wval = [&](const uint8_t* W, int row, int k, int K) -> float {
+    if (!w4) return kDec.v[W[size_t(row) * K + k]];
+    const uint8_t b = W[size_t(row) * (K / 2) + k / 2];
+    return e2m1_value(uint8_t((k & 1) ? (b >> 4) : (b & 15)));
+  };
+  const size_t wdiv = w4 ? 2 : 1;  // weights per byte
+  const uint8_t* Wg = shared ? (const uint8_t*)L->sh_Wgu : (const uint8_t*)L->Wgu + size_t(e) * 2 * F * d / wdiv;
+  const uint8_t* Wu = Wg + size_t(F) * d / wdiv;
+  const uint8_t* Wd = shared ? (const uint8_t*)L->sh_Wd : (const uint8_t*)L->Wd + size_t(e) * d * F / wdiv;
   const float* sg = shared ? L->sh_sgu : L->sgu + size_t(e) * 2 * F;
   const float* su = sg + F;
   const float* sdn = shared ? L->sh_sd : L->sd + size_t(e) * d;
@@ -264,8 +290,8 @@ void oracle_expert(const oracle_layer* L, int e, const float* xf, float* ye) {
   }
   for (int n = 0; n < F; ++n) {
     float ag = 0.0f, au = 0.0f;
-    for (int k = 0; k < d; ++k) ag += xa[size_t(k)] * kDec.v[Wg[size_t(n) * d + k]];
-    for (int k = 0; k < d; ++k) au += xa[size_t(k)] * kDec.v[Wu[size_t(n) * d + k]];
+    for (int k = 0; k < d; ++k) ag += xa[size_t(k)] * wval(Wg, n, k, d);
+    for (int k = 0; k < d; ++k) au += xa[size_t(k)] * wval(Wu, n, k, d);
     g[size_t(n)] = ag * sx * row_scale(sg, n, F);
     u[size_t(n)] = au * sx * row_scale(su, n, F);
   }
@@ -284,7 +310,7 @@ void oracle_expert(const oracle_layer* L, int e, const float* xf, float* ye) {
   }
   for (int m = 0; m < d; ++m) {
     float acc = 0.0f;
-    for (int n = 0; n < F; ++n) acc += ha[size_t(n)] * kDec.v[Wd[size_t(m) * F + n]];
+    for (int n = 0; n < F; ++n) acc += ha[size_t(n)] * wval(Wd, m, n, F);
     ye[m] = acc * sh * row_scale(sdn, m, d);
   }
 }

@@ -60,6 +60,8 @@ def lib():
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3_decode.restype = ctypes.c_float
+        L.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e2m1_decode.restype = ctypes.c_float
         L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         L.oracle_e4m3_encode.restype = ctypes.c_uint8
         L.oracle_bf16_rne.argtypes = [ctypes.c_float]
@@ -99,7 +101,8 @@ class Layer:
                  bias_mode: int = BIAS_SCORE):
         self.w = w
         self.k = k
-        self.s = OracleLayer(w.d, w.ffn, w.E, k, 1 if w.fp8 else 0, act_mode, mutant,
+        wfmt = 2 if getattr(w, "fp4", False) else (1 if w.fp8 else 0)  # E2M1, E4M3 or fp32 weights
+        self.s = OracleLayer(w.d, w.ffn, w.E, k, wfmt, act_mode, mutant,
                              _p(w.Wr), _p(w.bias), _p(w.Wgu), _p(w.sgu), _p(w.Wd), _p(w.sd),
                              _p(w.sh_Wgu), _p(w.sh_sgu), _p(w.sh_Wd), _p(w.sh_sd), bias_mode)
 
@@ -203,6 +206,12 @@ def dispatch(ids: np.ndarray, E: int, mutant: int = MUT_NONE):
 def e4m3_decode_all() -> np.ndarray:
     L = lib()
     return np.array([L.oracle_e4m3_decode(c) for c in range(256)], np.float32)
+
+
+def e2m1_decode_all() -> np.ndarray:
+    """The values of the 16 E2M1 codes."""
+    L = lib()
+    return np.array([L.oracle_e2m1_decode(c) for c in range(16)], np.float32)
 
 
 def e4m3_encode(v: np.ndarray) -> np.ndarray:

@@ -74,6 +74,108 @@ def test_e4m3_encode_matches_torch_in_range_and_saturates():
     assert np.all(o.e4m3_encode(-big) == 0xFE)
 
 
+# The OCP Microscaling Formats specification v1.0 (section 5.3.3) lists the E2M1 element
+# format by its representable values: sign bit 3; magnitudes 0 and 0.5 (subnormal), 1, 1.5,
+# 2, 3, 4, 6 (max normal 6.0, min normal 1.0, min subnormal 0.5); no infinities or NaN.
+E2M1_SPEC = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float64)
+
+
+def test_e2m1_decode_matches_the_format():
+    dec = o.e2m1_decode_all().astype(np.float64)
+    assert np.array_equal(dec[:8], E2M1_SPEC)
+    assert np.array_equal(dec[8:], -E2M1_SPEC) and np.signbit(dec[8])
+
+
+def test_generator_e2m1_quantiser_rounds_to_nearest_even():
+    """The 4-bit checkpoint's encoder (the generator's, input preparation): every midpoint
+    goes to the even code, its neighbours to the nearest, beyond 6 saturates."""
+    mids = (E2M1_SPEC[:-1] + E2M1_SPEC[1:]) / 2
+    v = np.concatenate([mids, np.nextafter(mids.astype(np.float32), np.float32(9)),
+                        np.nextafter(mids.astype(np.float32), np.float32(-1)), E2M1_SPEC, [7.0, 1e9]]).astype(np.float32)
+    got = g.quant_e2m1(v)
+    want = []
+    for x in v.astype(np.float64):
+        dist = np.abs(E2M1_SPEC - x)
+        best = np.flatnonzero(dist == dist.min())
+        want.append(best[0] if len(best) == 1 else best[best % 2 == 0][0])
+    assert np.array_equal(got, np.array(want, np.uint8))
+    assert np.array_equal(g.quant_e2m1(-v), np.array(want, np.uint8) | 8)
+
+
+def _dec4(packed):
+    """Packed E2M1 rows (two codes per byte, element 2i in the low nibble) as float64 values,
+    decoded with the specification's table."""
+    codes = np.stack([packed & 15, packed >> 4], axis=-1).reshape(*packed.shape[:-1], -1)
+    return np.where(codes & 8, -1.0, 1.0) * E2M1_SPEC[codes & 7]
+
+
+def test_w4a8_expert_matches_float64_with_torch_quantiser():
+    """The expert with 4-bit weights: E2M1 codes times their row scales, per-row E4M3
+    activations (torch's conversion), float64 products, as the W8A8 pin above."""
+    w = g.make_layer(17, 256, 128, 8, fp8=False, bias_var=0.5, fp4=True)
+    x = g.make_x(18, 64, w.d, bf16=True)
+    xf = g.bf16_bits_to_f32(x)
+    L = o.Layer(w)
+
+    def q(v):
+        s = np.float32(np.max(np.abs(v)) / np.float32(448.0))
+        codes = torch.from_numpy((v / s).astype(np.float32)).to(torch.float8_e4m3fn)
+        return codes.double().numpy(), float(s)
+
+    errs = []
+    for t in range(64):
+        e = t % 8
+        qx, sx = q(xf[t])
+        gg = (_dec4(w.Wgu[e, 0]) @ qx) * sx * w.sgu[e, 0].astype(np.float64)
+        uu = (_dec4(w.Wgu[e, 1]) @ qx) * sx * w.sgu[e, 1].astype(np.float64)
+        h = (gg / (1 + np.exp(-gg)) * uu).astype(np.float32)
+        qh, sh = q(h)
+        y = (_dec4(w.Wd[e]) @ qh) * sh * w.sd[e].astype(np.float64)
+        errs.append(parity.rel_l2(o.expert(L, e, xf[t]), y))
+    errs = np.array(errs)
+    assert np.mean(errs < 1e-5) >= 0.9, errs
+    assert errs.max() < 1e-3, errs
+
+
+def test_one_hot_route_is_the_dense_ffn_w4a16():
+    """4-bit weights, forced_w = (1,0,0,0,0,0), shared expert zeroed: y = the dense FFN of that
+    expert on fp32 activations and the spec-decoded weights (float64)."""
+    w = g.make_layer(19, 128, 128, 16, fp8=False, bias_var=0.5, fp4=True)
+    w.sh_sgu[:] = 0
+    w.sh_sd[:] = 0
+    x = g.make_x(20, 6, w.d, bf16=True)
+    xf = g.bf16_bits_to_f32(x).astype(np.float64)
+    L = o.Layer(w, act_mode=o.ACT_W8A16)
+    ids = np.array([[e, (e + 3) % 16, (e + 5) % 16, (e + 7) % 16, (e + 9) % 16, (e + 11) % 16] for e in range(6)],
+                   np.int32)
+    fw = np.zeros((6, 6), np.float32)
+    fw[:, 0] = 1
+    out = o.layer_forward(L, x, forced_ids=ids, forced_w=fw)
+    for t in range(6):
+        e = ids[t, 0]
+        Wg = _dec4(w.Wgu[e, 0]) * w.sgu[e, 0][:, None]
+        Wu = _dec4(w.Wgu[e, 1]) * w.sgu[e, 1][:, None]
+        Wd = _dec4(w.Wd[e]) * w.sd[e][:, None]
+        gg, uu = Wg @ xf[t], Wu @ xf[t]
+        y = Wd @ (gg / (1 + np.exp(-gg)) * uu)
+        assert parity.rel_l2(out["y"][t], y) < 2e-6
+
+
+def test_4bit_checkpoint_is_a_coarser_copy_of_the_same_weights():
+    """The 4-bit and the FP8 checkpoints of one seed decode to the same Gaussian weights within
+    each format's rounding (E2M1 keeps one mantissa bit), so their layers agree loosely."""
+    w8 = g.make_layer(21, 256, 128, 8, fp8=True, bias_var=0.5)
+    w4 = g.make_layer(21, 256, 128, 8, fp8=False, bias_var=0.5, fp4=True)
+    a = _dec4(w4.Wgu) * w4.sgu[..., None]
+    b = _dec(w8.Wgu) * w8.sgu[..., None]
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 0.05 < rel < 0.2, rel
+    x = g.make_x(22, 16, 256, bf16=True)
+    y8 = o.layer_forward(o.Layer(w8), x)
+    y4 = o.layer_forward(o.Layer(w4), x, forced_ids=y8["ids"])
+    assert 0.03 < parity.rel_l2(y4["y"], y8["y"]) < 0.3
+
+
 def test_bf16_rne_matches_definition_and_torch():
     rng = np.random.default_rng(1)
     bits = rng.integers(0, 2 ** 32, size=2_000_000, dtype=np.uint64).astype(np.uint32)
