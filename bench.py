@@ -35,6 +35,7 @@ D, FFN, E, K = 2048, 640, 384, 6
 EXPERT_BYTES = 3 * D * FFN + (2 * FFN + D) * 4          # E4M3 codes + fp32 row scales
 ROUTER_BYTES = E * D * 4 + E * 4                         # fp32 router weights + bias
 GATEUP_EXPERT_BYTES = 2 * FFN * D + 2 * FFN * 4
+EXPERT_BYTES_W4 = 3 * D * FFN // 2 + (2 * FFN + D) * 4  # E2M1 codes (two per byte) + fp32 row scales
 N_COPIES = 8
 HEADLINE_T = 64
 KERNELS_PER_FORWARD = 5  # router (quantises x, selects, then dispatches in its last CTA), gate_up, h_quant, down, combine (free routing, T <= 128)
@@ -54,6 +55,7 @@ def parse_args():
     ap.add_argument("--path", choices=sorted(PATH_FLAGS), default="auto", help="expert kernels")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill extras")
     ap.add_argument("--no-stack", action="store_true", help="skip the 50-layer stack extras")
+    ap.add_argument("--no-w4", action="store_true", help="skip the 4-bit weight extras")
     return ap.parse_args()
 
 
@@ -338,6 +340,8 @@ def run_ours(args):
         for Tx in (2048, 16384):
             extra[f"prefill_T{Tx}"] = prefill(moe, g, layers[0], Tx, flags)
         extra["prefill_T2048_as_4x512_forced"] = prefill_forced_chunks(moe, g, layers[0], flags)
+    if not args.no_w4 and args.path != "stream":
+        extra.update(w4_bench(moe, g, args, hbm_peak, n_copies=len(layers), prefill_too=not args.no_prefill))
     if not args.no_stack:
         del layers[1:]
         torch.cuda.empty_cache()
@@ -532,6 +536,59 @@ def w8a8_drift(w, x_host, y_dev, ids_dev, w_dev):
             "max_err_frac": float(diff.abs().max() / y_ref.abs().max()), "tokens": T,
             "reference": "W8A16 on the host (torch float64, dequantised E4M3 weights, fp32 activations, "
                          "the GPU's ids and weights)"}
+
+
+def w4_bench(moe, g, args, hbm_peak, n_copies, prefill_too):
+    """The same Kolibri-shaped layer with 4-bit expert weights (E2M1 codes + fp32 row scales,
+    W4A8): decode at batch 1, 8 and 64 (CUDA graph over rotated weight copies, as small_batch)
+    with the HBM fraction over the 4-bit bytes of the selected experts, and the 16k prefill."""
+    import torch
+    w = g.kolibri_layer(g.SEED_DECODE, fp4=True)
+    base = moe.Layer.from_host(w)
+    layers = [base] + [base.clone() for _ in range(n_copies - 1)]
+    out = {}
+    for T in (1, 8, 64):
+        x = torch.from_numpy(g.make_x(g.SEED_DECODE, T, D, bf16=True).view(np.int16).copy()).cuda().view(torch.bfloat16)
+        ws = moe.workspace(base, T)
+        y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+        ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        wt = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        for lay in layers:
+            moe.forward(x, lay, ws, out=y, ids=ids, w=wt)
+        torch.cuda.synchronize()
+        st = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(graph, stream=st):
+                for lay in layers:
+                    moe.forward(x, lay, ws, out=y, ids=ids, w=wt)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, args.steps // len(layers))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * len(layers))
+        U = len(np.unique(ids.cpu().numpy()))
+        nbytes = (U + 1) * EXPERT_BYTES_W4 + ROUTER_BYTES + 4 * T * D
+        stage_ms, traced = traced_stages(moe, layers, x, ws, y, ids, wt, 0, iters=min(200, args.steps))
+        out[f"w4_decode_T{T}"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_layer": ms, "unique_experts": U,
+                                  "bytes": nbytes, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                                  "weights": "E2M1 + fp32 row scales", "stage_ms": stage_ms,
+                                  "timing": f"CUDA graph over {len(layers)} layer copies"}
+        if T == 64:  # the gate/up kernel alone, over its algorithmic bytes
+            gu_bytes = (U + 1) * (FFN * D + 2 * FFN * 4) + T * D + (K + 1) * T * FFN * 4
+            out["w4_decode_T64"]["gate_up_hbm_frac"] = gu_bytes / (stage_ms["gate_up"] * 1e-3) / 1e9 / hbm_peak
+    del layers
+    if prefill_too:
+        out["w4_prefill_T16384"] = prefill(moe, g, base, 16384, 0)
+    torch.cuda.empty_cache()
+    return out
 
 
 def zipf_forced(moe, g, layers, args, hbm_peak, flags=0, T=128):

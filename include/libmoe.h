@@ -28,7 +28,8 @@
  *  - T == 0 is a no-op returning MOE_OK.
  *  - Alignment: x, y, weights, scales and the workspace 16-byte aligned.
  *  - Shapes: top_k == 6 (else MOE_ERR_UNSUPPORTED), n_experts <= 1024, T <= 2^20;
- *    E4M3 weights in the tiled layout: d_model % 128 == 0 and ffn % 128 == 0; E4M3 weights
+ *    E4M3 or E2M1 weights in the tiled layout: d_model % 128 == 0 and ffn % 128 == 0 (E2M1
+ *    weights only in the tiled layout); E4M3 weights
  *    in the row layout: d_model % 256 == 0, d_model <= 2048, ffn % 64 == 0, ffn <= 640;
  *    fp32 weights: d_model % 128 == 0 and ffn % 32 == 0.
  *  - Layout: row-major, last index contiguous.
@@ -59,7 +60,13 @@ typedef enum {
                                  error of the library; the access was kept inside its buffer) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+/* MOE_E2M1: 4-bit weights (OCP E2M1 codes: sign bit 3, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4,
+ * 6), two per byte, element 2i in the low nibble of byte i, with one fp32 scale per output row
+ * like MOE_E4M3 (this library's reading of the 4-bit "K4" builds of page "We Stopped the
+ * Kolibri Benchmark Before Scoring One Answer", section "What this means if you want Kolibri
+ * on a Mac"; the pages give no format).  Weight matrices keep their row count and halve their
+ * bytes per row; activations enter the contractions as E4M3 as for MOE_E4M3 (W4A8). */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_E2M1 = 3 } moe_dtype;
 
 /* Byte order of the E4M3 expert weight tensors (w_gate_up, w_down, sh_gate_up, sh_down).
  *   MOE_LAYOUT_ROWS   the shapes below, row-major (a checkpoint's order).
@@ -73,9 +80,14 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
  *                       = rows 128 m .. +127 of expert e's [d, F] matrix, k = 128 j .. +127
  *                     inside a tile, byte (r, c) sits at r*128 + 16*((c/16) ^ (r%8)) + c%16.
  *                     The shared expert's tensors are tiled the same way (as expert 0).
- *                     Requires E4M3, d_model % 128 == 0 and ffn % 128 == 0.
+ *                     Requires E4M3 or E2M1, d_model % 128 == 0 and ffn % 128 == 0.
+ *                     E2M1 weights use the same tile order with 8 KB tiles (tile index
+ *                     x 8192 in place of x 16384): 128 rows of 64 bytes (128 codes of k)
+ *                     each, rows in order and unswizzled (the tensor cores' swizzle is
+ *                     applied when a tile is copied to shared memory).
  * The tensor-core expert kernels read the tiled layout (each pipeline stage is then one
- * contiguous copy of 32-80 KB); the weight-streaming kernels read the row layout. */
+ * contiguous copy of 32-80 KB); the weight-streaming kernels read the row layout.  E2M1
+ * layers run only on the tensor-core kernels, so moe_forward takes them tiled. */
 typedef enum { MOE_LAYOUT_ROWS = 0, MOE_LAYOUT_TILED = 1 } moe_layout;
 
 /* How router_bias enters the routing (page "We Ported Aleph Alpha's Kolibri to a MacBook.
@@ -88,11 +100,13 @@ typedef enum { MOE_BIAS_SCORE = 0, MOE_BIAS_SELECT = 1 } moe_bias_mode;
 /* One layer: borrowed device pointers.  Shapes with d = d_model, F = ffn, E = n_experts.
  *   w_router     [E, d]  fp32            router_bias [E] fp32 or NULL
  *   w_gate_up    [E, 2, F, d]            gate rows (index 0) then up rows (index 1)
+ *                (E2M1: the last dimension of each weight tensor holds two codes per byte)
  *   s_gate_up    [E, 2, F] fp32          per-output-row scales (E4M3 only, else NULL)
  *   w_down       [E, d, F]               s_down [E, d] fp32 (E4M3 only)
  *   sh_gate_up   [2, F, d]               sh_s_gate_up [2, F] (E4M3 only)
  *   sh_down      [d, F]                  sh_s_down [d] (E4M3 only)
- * Weights are E4M3 codes (w_dtype = MOE_E4M3, one byte each) or fp32 (MOE_F32). */
+ * Weights are E4M3 codes (w_dtype = MOE_E4M3, one byte each), E2M1 codes (MOE_E2M1, two
+ * per byte) or fp32 (MOE_F32). */
 typedef struct {
   int d_model, ffn, n_experts, top_k;
   moe_dtype w_dtype;
@@ -116,12 +130,13 @@ typedef struct {
 #define MOE_PATH_STREAM 1u /* weight-streaming kernels (row layout; any T) */
 #define MOE_PATH_TC 2u     /* tcgen05 grouped GEMMs (tiled layout; any T) */
 
-/* Writes the tiled layout (MOE_LAYOUT_TILED above) of src's four E4M3 weight tensors, which
- * must be in the row layout, into gate_up [E*2*F*d], down [E*d*F], sh_gate_up [2*F*d] and
- * sh_down [d*F] bytes of caller-owned device memory (16-byte aligned, not overlapping the
- * sources).  The scales and the router are unchanged; a moe_layer with the four pointers
+/* Writes the tiled layout (MOE_LAYOUT_TILED above) of src's four E4M3 (or E2M1) weight
+ * tensors, which must be in the row layout, into gate_up [E*2*F*d], down [E*d*F], sh_gate_up
+ * [2*F*d] and sh_down [d*F] bytes (half as many for E2M1) of caller-owned device memory
+ * (16-byte aligned, not overlapping the sources).  The scales and the router are unchanged; a moe_layer with the four pointers
  * replaced and w_layout = MOE_LAYOUT_TILED then describes the same layer.  Asynchronous on
- * `stream`.  MOE_ERR_UNSUPPORTED unless E4M3 with d_model % 128 == 0 and ffn % 128 == 0. */
+ * `stream`.  MOE_ERR_UNSUPPORTED unless E4M3 or E2M1 with d_model % 128 == 0 and
+ * ffn % 128 == 0. */
 moe_status moe_pack_weights(const moe_layer* src, void* gate_up, void* down, void* sh_gate_up, void* sh_down,
                             moe_stream_t stream);
 

@@ -15,7 +15,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
-MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1 = 0, 1, 2, 3
 LAYOUT_ROWS, LAYOUT_TILED = 0, 1
 BIAS_SCORE, BIAS_SELECT = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC = 0, 1, 2
@@ -142,16 +142,20 @@ class Layer:
 
     def __init__(self, w_router, router_bias, w_gate_up, w_down, sh_gate_up, sh_down,
                  s_gate_up=None, s_down=None, sh_s_gate_up=None, sh_s_down=None, top_k: int = 6,
-                 layout: int = LAYOUT_ROWS, bias_mode: int = BIAS_SCORE):
+                 layout: int = LAYOUT_ROWS, bias_mode: int = BIAS_SCORE, w_dtype: Optional[int] = None):
         self.tensors = dict(w_router=w_router, router_bias=router_bias, w_gate_up=w_gate_up, w_down=w_down,
                             sh_gate_up=sh_gate_up, sh_down=sh_down, s_gate_up=s_gate_up, s_down=s_down,
                             sh_s_gate_up=sh_s_gate_up, sh_s_down=sh_s_down)
         E, two, F, d = w_gate_up.shape
         assert two == 2
-        fp8 = w_gate_up.dtype in (torch.uint8, torch.float8_e4m3fn)
+        if w_dtype is None:  # uint8 / float8 codes are E4M3; E2M1 codes must be named
+            w_dtype = MOE_E4M3 if w_gate_up.dtype in (torch.uint8, torch.float8_e4m3fn) else MOE_F32
+        if w_dtype == MOE_E2M1:
+            d *= 2  # two codes per byte
+        fp8 = w_dtype in (MOE_E4M3, MOE_E2M1)
         self.d, self.F, self.E, self.k, self.fp8, self.layout = d, F, E, top_k, fp8, layout
-        self.bias_mode = bias_mode
-        self.c = MoeLayerC(d, F, E, top_k, MOE_E4M3 if fp8 else MOE_F32,
+        self.bias_mode, self.w_dtype = bias_mode, w_dtype
+        self.c = MoeLayerC(d, F, E, top_k, w_dtype,
                            _ptr(w_router), _ptr(router_bias), _ptr(w_gate_up), _ptr(s_gate_up), _ptr(w_down),
                            _ptr(s_down), _ptr(sh_gate_up), _ptr(sh_s_gate_up), _ptr(sh_down), _ptr(sh_s_down),
                            layout, bias_mode)
@@ -163,12 +167,13 @@ class Layer:
         out = {k: torch.empty_like(t[k]) for k in ("w_gate_up", "w_down", "sh_gate_up", "sh_down")}
         _check(lib().moe_pack_weights(self.ref, _ptr(out["w_gate_up"]), _ptr(out["w_down"]), _ptr(out["sh_gate_up"]),
                                       _ptr(out["sh_down"]), _stream()), "moe_pack_weights")
-        return Layer(**{**t, **out}, top_k=self.k, layout=LAYOUT_TILED, bias_mode=self.bias_mode)
+        return Layer(**{**t, **out}, top_k=self.k, layout=LAYOUT_TILED, bias_mode=self.bias_mode,
+                     w_dtype=self.w_dtype)
 
     def clone(self) -> "Layer":
         """A copy at other device addresses (same values, layout and bias mode)."""
         return Layer(**{k: (v.clone() if v is not None else None) for k, v in self.tensors.items()}, top_k=self.k,
-                     layout=self.layout, bias_mode=self.bias_mode)
+                     layout=self.layout, bias_mode=self.bias_mode, w_dtype=self.w_dtype)
 
     @classmethod
     def from_host(cls, w, device="cuda", top_k: int = 6, tiled: Optional[bool] = None, bias_mode: int = BIAS_SCORE):
@@ -177,10 +182,12 @@ class Layer:
         multiples of 128; the row layout (weight-streaming kernels) otherwise."""
         def dev(a):
             return None if a is None else torch.from_numpy(a).to(device)
+        fp4 = getattr(w, "fp4", False)
         rows = cls(dev(w.Wr), dev(w.bias), dev(w.Wgu), dev(w.Wd), dev(w.sh_Wgu), dev(w.sh_Wd),
-                   dev(w.sgu), dev(w.sd), dev(w.sh_sgu), dev(w.sh_sd), top_k=top_k, bias_mode=bias_mode)
-        if tiled is None:
-            tiled = rows.fp8 and rows.d % 128 == 0 and rows.F % 128 == 0
+                   dev(w.sgu), dev(w.sd), dev(w.sh_sgu), dev(w.sh_sd), top_k=top_k, bias_mode=bias_mode,
+                   w_dtype=MOE_E2M1 if fp4 else None)
+        if tiled is None or fp4:  # 4-bit weights run tiled only
+            tiled = fp4 or (rows.fp8 and rows.d % 128 == 0 and rows.F % 128 == 0)
         if not tiled:
             return rows
         packed = rows.tiled()

@@ -36,6 +36,10 @@ moe_status check_layer(const moe_layer* L) {
     if (!L->s_gate_up || !L->s_down || !L->sh_s_gate_up || !L->sh_s_down) return MOE_ERR_INVALID_ARG;
     if (L->w_layout == MOE_LAYOUT_TILED ? !(L->d_model % 128 == 0 && L->ffn % 128 == 0) : !stream_ok(*L))
       return MOE_ERR_UNSUPPORTED;
+  } else if (L->w_dtype == MOE_E2M1) {
+    // 4-bit weights run on the tensor-core kernels only
+    if (!L->s_gate_up || !L->s_down || !L->sh_s_gate_up || !L->sh_s_down) return MOE_ERR_INVALID_ARG;
+    if (L->w_layout != MOE_LAYOUT_TILED || L->d_model % 128 != 0 || L->ffn % 128 != 0) return MOE_ERR_UNSUPPORTED;
   } else if (L->w_dtype == MOE_F32) {
     if (L->w_layout != MOE_LAYOUT_ROWS) return MOE_ERR_INVALID_ARG;
     if (L->d_model % 128 != 0 || L->ffn % 32 != 0) return MOE_ERR_UNSUPPORTED;
@@ -51,7 +55,9 @@ LayerDev to_dev(const moe_layer* L) {
   d.F = L->ffn;
   d.E = L->n_experts;
   d.k = L->top_k;
-  d.fp8 = L->w_dtype == MOE_E4M3;
+  // quantised weights (E4M3 or E2M1) take the W8A8 / W4A8 path: E4M3 activations, bf16 rows
+  d.fp8 = L->w_dtype == MOE_E4M3 || L->w_dtype == MOE_E2M1;
+  d.w4 = L->w_dtype == MOE_E2M1;
   d.tiled = L->w_layout == MOE_LAYOUT_TILED;
   d.bias_sel = L->bias_mode == MOE_BIAS_SELECT && L->router_bias != nullptr;
   d.Wr = L->w_router;
@@ -195,7 +201,8 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
 moe_status moe_pack_weights(const moe_layer* src, void* gate_up, void* down, void* sh_gate_up, void* sh_down,
                             moe_stream_t stream) {
   // only the four weight tensors are read: no check of the shapes the other kernels need
-  if (!src || src->w_dtype != MOE_E4M3 || src->w_layout != MOE_LAYOUT_ROWS) return MOE_ERR_INVALID_ARG;
+  if (!src || (src->w_dtype != MOE_E4M3 && src->w_dtype != MOE_E2M1) || src->w_layout != MOE_LAYOUT_ROWS)
+    return MOE_ERR_INVALID_ARG;
   if (src->n_experts < 1 || src->n_experts > kMaxExperts || src->d_model <= 0 || src->ffn <= 0)
     return MOE_ERR_INVALID_ARG;
   if (!src->w_gate_up || !src->w_down || !src->sh_gate_up || !src->sh_down || !aligned16(src->w_gate_up) ||

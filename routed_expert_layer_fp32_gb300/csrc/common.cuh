@@ -248,7 +248,8 @@ inline cudaError_t launch_pdl(void (*kernel)(ExpTypes...), dim3 grid, dim3 block
 namespace moe {
 struct LayerDev {
   int d, F, E, k;
-  bool fp8;
+  bool fp8;       // quantised weights (E4M3, or E2M1 with w4): E4M3 activations, bf16 expert rows
+  bool w4;        // E2M1 weights (4-bit codes, two per byte)
   bool tiled;     // E4M3 weights in the tiled layout (MOE_LAYOUT_TILED)
   bool bias_sel;  // MOE_BIAS_SELECT: the bias ranks the experts but stays out of the logits
   // the bias added to the logits the routers write, and the one the selection adds on top

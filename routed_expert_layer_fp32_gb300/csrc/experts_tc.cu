@@ -118,9 +118,10 @@ struct TcCfg {
       size_t(kStages) * kStageBytes + kRecvBytes + 1024 /* alignment slack */ + sizeof(TcCtl);
 };
 
-template <int kN, bool kGateUp, int kA, int kSplit, int kC>
+template <int kN, bool kGateUp, int kA, int kSplit, int kC, bool kW4>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_expert_tc(const __grid_constant__ CUtensorMap map_x, TcArgs a) {
+    k_expert_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                const __grid_constant__ CUtensorMap map_wsh, TcArgs a) {
   using C = TcCfg<kN, kGateUp, kA, kSplit, kC>;
   static_assert(!kGateUp || kA == 2, "gate/up stages hold the gate and the up rows");
   static_assert(kSplit == 1 || kSplit == 2, "items are split over one or two CTAs");
@@ -176,15 +177,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto a_tile = [&](int s, int ai, int c) {
     return stage_a(s) + (kGateUp ? (c * 2 + ai) : (ai * kC + c)) * kATileBytes;
   };
-  // tiled-layout source of an item's block ai (down) or of its gate/up pairs, first chunk j
-  auto w_src = [&](const Tile& tl, int nb, int ai, int j) {
-    const bool shared = tl.group == a.E;
-    const size_t e = shared ? 0 : size_t(tl.group);
-    const uint8_t* base = shared ? a.wsh : a.w;
-    if (kGateUp) return base + ((e * nb_rows + nb) * KT + j) * 2 * size_t(kATileBytes);
-    return base + ((e * nb_rows + size_t(nb) * kA + ai) * KT + j) * size_t(kATileBytes);
+  // tiled-layout index of the first tile of an item's block ai (down) or of its gate/up pairs,
+  // chunk j; the copy's tiles follow it
+  auto w_tile = [&](const Tile& tl, int nb, int ai, int j) -> size_t {
+    const size_t e = tl.group == a.E ? 0 : size_t(tl.group);
+    if (kGateUp) return ((e * nb_rows + nb) * KT + j) * 2;
+    return (e * nb_rows + size_t(nb) * kA + ai) * KT + j;
   };
-  constexpr uint32_t kCopyBytes = kGateUp ? 2 * kC * kATileBytes : kC * kATileBytes;  // per weight copy
+  // E4M3 tiles are 16 KB in memory and in shared memory; E2M1 tiles 8 KB in memory, unpacked
+  // to the 16 KB operand layout by the copy (tensor map type 16U4_ALIGN16B)
+  constexpr uint32_t kTileMem = kW4 ? kATileBytes / 2 : kATileBytes;
+  auto w_src = [&](const Tile& tl, int nb, int ai, int j) {
+    return (tl.group == a.E ? a.wsh : a.w) + w_tile(tl, nb, ai, j) * kTileMem;
+  };
+  constexpr uint32_t kCopyTiles = kGateUp ? 2 * kC : kC;  // tiles per weight copy
+  constexpr uint32_t kCopyBytes = kCopyTiles * kATileBytes;  // shared-memory bytes per weight copy
   constexpr int kCopies = kGateUp ? 1 : kA;
 
   if (warp == 0) {  // -------------------------------------------------- TMA producer warp
@@ -198,7 +205,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int item = unit; item < known && budget > 0; item += n_units) {
         const Tile tl = kGateUp ? Tile{a.E, 0, 0, 0} : checked_tile(a.tiles, item / nblk, a.E, a.R, kN, a.status_flags, 1);
         for (int ks = ks_lo; ks < ks_hi && budget > 0; ++ks, budget -= kCopies * int(kCopyBytes))
-          for (int ai = 0; ai < kCopies; ++ai) prefetch_l2_bulk(w_src(tl, item % nblk, ai, ks * kC), kCopyBytes);
+          for (int ai = 0; ai < kCopies; ++ai)
+            prefetch_l2_bulk(w_src(tl, item % nblk, ai, ks * kC), kCopyTiles * kTileMem);
       }
     }
     pdl_begin();
@@ -239,10 +247,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->full[s], C::kLdgsts ? C::kABytes : C::kStageBytes);
+          // the weights' bytes in memory (E2M1: half their shared-memory bytes), then the
+          // activations' unless cp.async brings them
+          mbar_arrive_expect_tx(&ctl->full[s], (kW4 ? C::kABytes / 2 : C::kABytes) + (C::kLdgsts ? 0 : C::kBBytes));
 #pragma unroll
-          for (int ai = 0; ai < kCopies; ++ai)
-            bulk_g2s_stream(stage_a(s) + ai * kCopyBytes, w_src(tl, nb, ai, ks * kC), kCopyBytes, &ctl->full[s], pol);
+          for (int ai = 0; ai < kCopies; ++ai) {
+            if (kW4) {  // one tensor-map box per tile, rows of the [tiles x 128, 128] code matrix
+              const CUtensorMap* mw = tl.group == a.E ? &map_wsh : &map_w;
+              const int y0 = int(w_tile(tl, nb, ai, ks * kC) * kTileM);
+              for (int t = 0; t < int(kCopyTiles); ++t)
+                tma_load_2d(stage_a(s) + ai * kCopyBytes + t * kATileBytes, mw, 0, y0 + t * kTileM, &ctl->full[s]);
+            } else {
+              bulk_g2s_stream(stage_a(s) + ai * kCopyBytes, w_src(tl, nb, ai, ks * kC), kCopyBytes, &ctl->full[s], pol);
+            }
+          }
           if (!kGateUp) tma_load_3d(stage_b(s), &map_x, 0, tl.row0, ks * kC, &ctl->full[s]);
         }
         if (C::kLdgsts) {
@@ -284,7 +302,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_begin();
     total = *a.n_tiles * nblk;
     if (lane == 0) {  // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_e4m3(kTileM, kN);
+      constexpr uint32_t idesc = kW4 ? idesc_f8f6f4(kTileM, kN, kFmtE2M1, kFmtE4M3) : idesc_e4m3(kTileM, kN);
       int it = 0, jt = 0;
       bool stop = false;
       for (int item = unit; item < total && !stop; item += n_units, ++jt) {
@@ -469,10 +487,11 @@ int sm_count() {
   return sms;
 }
 
-template <int kN, bool kGateUp, int kA, int kSplit, int kC>
-cudaError_t launch_tc(const CUtensorMap& mx, const TcArgs& a, long long max_items, cudaStream_t s) {
+template <int kN, bool kGateUp, int kA, int kSplit, int kC, bool kW4 = false>
+cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mwsh, const TcArgs& a,
+                      long long max_items, cudaStream_t s) {
   using C = TcCfg<kN, kGateUp, kA, kSplit, kC>;
-  static cudaError_t attr = cudaFuncSetAttribute(k_expert_tc<kN, kGateUp, kA, kSplit, kC>,
+  static cudaError_t attr = cudaFuncSetAttribute(k_expert_tc<kN, kGateUp, kA, kSplit, kC, kW4>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
   if (attr != cudaSuccess) return attr;
   // one CTA (or one CTA pair) per SM
@@ -491,36 +510,57 @@ cudaError_t launch_tc(const CUtensorMap& mx, const TcArgs& a, long long max_item
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = kSplit == 2 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_expert_tc<kN, kGateUp, kA, kSplit, kC>, mx, a);
+  return cudaLaunchKernelEx(&cfg, k_expert_tc<kN, kGateUp, kA, kSplit, kC, kW4>, mx, mw, mwsh, a);
+}
+
+template <int kN, int kC, bool kSplit2>
+cudaError_t launch_gateup_w(bool w4, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mwsh,
+                            const TcArgs& a, long long items, cudaStream_t s) {
+  constexpr int kS = kSplit2 ? 2 : 1;
+  return w4 ? launch_tc<kN, true, 2, kS, kC, true>(mx, mw, mwsh, a, items, s)
+            : launch_tc<kN, true, 2, kS, kC, false>(mx, mw, mwsh, a, items, s);
 }
 
 // Gate/up: decode tiles (16 or 32 token rows) take two k-chunks per stage (64 KB of weights in
-// one copy); wider tiles one chunk (their activation boxes are larger).
-cudaError_t launch_gateup_n(int kN, int kC, bool split, const CUtensorMap& mx, const TcArgs& a, long long items,
-                            cudaStream_t s) {
-  if (kN == 16 && kC == 2) return split ? launch_tc<16, true, 2, 2, 2>(mx, a, items, s)
-                                        : launch_tc<16, true, 2, 1, 2>(mx, a, items, s);
-  if (kN == 16) return split ? launch_tc<16, true, 2, 2, 1>(mx, a, items, s) : launch_tc<16, true, 2, 1, 1>(mx, a, items, s);
-  if (kN == 32 && kC == 2) return launch_tc<32, true, 2, 1, 2>(mx, a, items, s);
-  if (kN == 32) return launch_tc<32, true, 2, 1, 1>(mx, a, items, s);
-  if (kN == 64) return kC == 2 ? launch_tc<64, true, 2, 1, 2>(mx, a, items, s) : launch_tc<64, true, 2, 1, 1>(mx, a, items, s);
-  if (kN == 128) return kC == 2 ? launch_tc<128, true, 2, 1, 2>(mx, a, items, s) : launch_tc<128, true, 2, 1, 1>(mx, a, items, s);
+// one copy); wider tiles one chunk (their activation boxes are larger).  E2M1 weights (w4)
+// load through the tensor maps mw / mwsh.
+cudaError_t launch_gateup_n(int kN, int kC, bool split, bool w4, const CUtensorMap& mx, const CUtensorMap& mw,
+                            const CUtensorMap& mwsh, const TcArgs& a, long long items, cudaStream_t s) {
+  if (kN == 16 && kC == 2) return split ? launch_gateup_w<16, 2, true>(w4, mx, mw, mwsh, a, items, s)
+                                        : launch_gateup_w<16, 2, false>(w4, mx, mw, mwsh, a, items, s);
+  if (kN == 16) return split ? launch_gateup_w<16, 1, true>(w4, mx, mw, mwsh, a, items, s)
+                             : launch_gateup_w<16, 1, false>(w4, mx, mw, mwsh, a, items, s);
+  if (kN == 32) return kC == 2 ? launch_gateup_w<32, 2, false>(w4, mx, mw, mwsh, a, items, s)
+                               : launch_gateup_w<32, 1, false>(w4, mx, mw, mwsh, a, items, s);
+  if (kN == 64) return kC == 2 ? launch_gateup_w<64, 2, false>(w4, mx, mw, mwsh, a, items, s)
+                               : launch_gateup_w<64, 1, false>(w4, mx, mw, mwsh, a, items, s);
+  if (kN == 128) return kC == 2 ? launch_gateup_w<128, 2, false>(w4, mx, mw, mwsh, a, items, s)
+                                : launch_gateup_w<128, 1, false>(w4, mx, mw, mwsh, a, items, s);
   return cudaErrorInvalidValue;
 }
 
 // Down: decode tiles take an item's whole k range (ffn = 640: five chunks, 80 KB in one
 // copy) per stage; wider tiles pair two 128-row blocks per stage, one chunk at a time.
-cudaError_t launch_down_n(int kN, int kA, int kC, const CUtensorMap& mx, const TcArgs& a, long long items,
-                          cudaStream_t s) {
+template <int kN, int kA, int kC>
+cudaError_t launch_down_w(bool w4, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mwsh,
+                          const TcArgs& a, long long items, cudaStream_t s) {
+  return w4 ? launch_tc<kN, false, kA, 1, kC, true>(mx, mw, mwsh, a, items, s)
+            : launch_tc<kN, false, kA, 1, kC, false>(mx, mw, mwsh, a, items, s);
+}
+
+cudaError_t launch_down_n(int kN, int kA, int kC, bool w4, const CUtensorMap& mx, const CUtensorMap& mw,
+                          const CUtensorMap& mwsh, const TcArgs& a, long long items, cudaStream_t s) {
   if (kA == 2) {
-    if (kN == 64) return launch_tc<64, false, 2, 1, 1>(mx, a, items, s);
-    if (kN == 128) return launch_tc<128, false, 2, 1, 1>(mx, a, items, s);
+    if (kN == 64) return launch_down_w<64, 2, 1>(w4, mx, mw, mwsh, a, items, s);
+    if (kN == 128) return launch_down_w<128, 2, 1>(w4, mx, mw, mwsh, a, items, s);
     return cudaErrorInvalidValue;
   }
-  if (kN == 16) return kC == 5 ? launch_tc<16, false, 1, 1, 5>(mx, a, items, s) : launch_tc<16, false, 1, 1, 1>(mx, a, items, s);
-  if (kN == 32) return kC == 5 ? launch_tc<32, false, 1, 1, 5>(mx, a, items, s) : launch_tc<32, false, 1, 1, 1>(mx, a, items, s);
-  if (kN == 64) return launch_tc<64, false, 1, 1, 1>(mx, a, items, s);
-  if (kN == 128) return launch_tc<128, false, 1, 1, 1>(mx, a, items, s);
+  if (kN == 16) return kC == 5 ? launch_down_w<16, 1, 5>(w4, mx, mw, mwsh, a, items, s)
+                               : launch_down_w<16, 1, 1>(w4, mx, mw, mwsh, a, items, s);
+  if (kN == 32) return kC == 5 ? launch_down_w<32, 1, 5>(w4, mx, mw, mwsh, a, items, s)
+                               : launch_down_w<32, 1, 1>(w4, mx, mw, mwsh, a, items, s);
+  if (kN == 64) return launch_down_w<64, 1, 1>(w4, mx, mw, mwsh, a, items, s);
+  if (kN == 128) return launch_down_w<128, 1, 1>(w4, mx, mw, mwsh, a, items, s);
   return cudaErrorInvalidValue;
 }
 
@@ -575,11 +615,18 @@ cudaError_t launch_gateup_tc(const LayerDev& L, int T, const WsLayout& ws, char*
   TcArgs a = tc_args(L, T, ws, base);
   a.w = L.wgu;
   a.wsh = L.sh_wgu;
+  CUtensorMap mw = mx, mwsh = mx;  // E2M1 weights: [tiles x 128, 128] code matrices, one tile per box
+  if (L.w4) {
+    const uint64_t tiles_e = uint64_t(L.F / kTileM) * (L.d / kKTile) * 2;
+    if (!make_map_e2m1(&mw, L.wgu, uint64_t(L.E) * tiles_e * kTileM, kTileM) ||
+        !make_map_e2m1(&mwsh, L.sh_wgu, tiles_e * kTileM, kTileM))
+      return cudaErrorInvalidValue;
+  }
   const long long items = max_tc_tiles(L, T, kN) * (L.F / kTileM);
   // a handful of tokens touch few experts: fewer items than SMs, so the k-steps of each item
   // are split over a CTA pair
   const bool split = T <= kSplitMaxT;
-  return launch_gateup_n(kN, kC, split, mx, a, items, s);
+  return launch_gateup_n(kN, kC, split, L.w4, mx, mw, mwsh, a, items, s);
 }
 
 cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* base, cudaStream_t s) {
@@ -595,8 +642,15 @@ cudaError_t launch_down_tc(const LayerDev& L, int T, const WsLayout& ws, char* b
   TcArgs a = tc_args(L, T, ws, base);
   a.w = L.wd;
   a.wsh = L.sh_wd;
+  CUtensorMap mw = mx, mwsh = mx;  // E2M1 weights: [tiles x 128, 128] code matrices, one tile per box
+  if (L.w4) {
+    const uint64_t tiles_e = uint64_t(L.d / kTileM) * KT;
+    if (!make_map_e2m1(&mw, L.wd, uint64_t(L.E) * tiles_e * kTileM, kTileM) ||
+        !make_map_e2m1(&mwsh, L.sh_wd, tiles_e * kTileM, kTileM))
+      return cudaErrorInvalidValue;
+  }
   const long long items = max_tc_tiles(L, T, kN) * (L.d / (kA * kTileM));
-  return launch_down_n(kN, kA, kC, mx, a, items, s);
+  return launch_down_n(kN, kA, kC, L.w4, mx, mw, mwsh, a, items, s);
 }
 
 }  // namespace moe

@@ -128,7 +128,8 @@ extern "C" moe_status moe_route_noalloc(const void* x, moe_dtype x_dtype, int T,
   L.F = layer->ffn;
   L.E = layer->n_experts;
   L.k = layer->top_k;
-  L.fp8 = layer->w_dtype == MOE_E4M3;
+  L.fp8 = layer->w_dtype == MOE_E4M3 || layer->w_dtype == MOE_E2M1;
+  L.w4 = layer->w_dtype == MOE_E2M1;
   L.Wr = layer->w_router;
   L.bias = layer->router_bias;
   L.bias_sel = layer->bias_mode == MOE_BIAS_SELECT && layer->router_bias != nullptr;

@@ -129,12 +129,15 @@ __device__ __forceinline__ uint64_t sw128_desc(const void* smem_tile) {
   return d;
 }
 
-// Instruction descriptor of kind::f8f6f4: fp32 accumulator (bits 4-5 = 1), A and B E4M3
-// (format 0 in bits 7-9 and 10-12), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22,
-// M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
-  return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+// Instruction descriptor of kind::f8f6f4: fp32 accumulator (bits 4-5 = 1), the A and B
+// element formats in bits 7-9 and 10-12 (E4M3 = 0, E2M1 = 5; a layer's A and B may differ in
+// this kind), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kFmtE4M3 = 0, kFmtE2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(int M, int N, uint32_t a_fmt, uint32_t b_fmt) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) { return idesc_f8f6f4(M, N, kFmtE4M3, kFmtE4M3); }
+
 
 
 // Instruction descriptor of kind::f16 with bf16 A and B (format 1 in bits 7-9 and 10-12),
@@ -201,6 +204,22 @@ inline bool make_map_chunks(CUtensorMap* map, const void* base, uint64_t rows, u
 
 inline bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   return make_map_bytes(map, base, rows, cols, box_rows, 1);
+}
+
+// E2M1 codes of a tiled weight tensor as a [rows, 128] matrix of 64-byte rows (8 KB per
+// 128-row tile), boxes of box_rows rows, copied to shared memory in the 16-byte-per-16-codes
+// operand layout of kind::f8f6f4 (type 16U4_ALIGN16B: each 8 bytes of codes, then 8 bytes the
+// MMA ignores) with the 128-byte swizzle.  A box's transaction count is its bytes in memory.
+inline bool make_map_e2m1(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace moe
