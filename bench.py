@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill extras")
     ap.add_argument("--no-stack", action="store_true", help="skip the 50-layer stack extras")
     ap.add_argument("--no-w4", action="store_true", help="skip the 4-bit weight extras")
+    ap.add_argument("--weights", choices=["e4m3", "e2m1"], default="e4m3",
+                    help="expert weight format of the timed layer (e2m1: the 4-bit checkpoint)")
     return ap.parse_args()
 
 
@@ -77,15 +79,15 @@ def profiled_traffic(kernel_key: str):
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch (\S+) decode_T64: (\d+)", text)
+    m = re.search(r"traffic_bytes_per_launch " + re.escape(kernel_key) + r" decode_T64: (\d+)", text)
     sh = re.search(r"source_sha256: ([0-9a-f]+)", text)
-    if not m or not sh or m.group(1) != kernel_key:
+    if not m or not sh:
         return None
     h = hashlib.sha256()
     for f in ("experts_tc.cu", "tcgen05.cuh", "tma.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "routed_expert_layer_fp32_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    return int(m.group(2)) if h.hexdigest() == sh.group(1) else None
+    return int(m.group(1)) if h.hexdigest() == sh.group(1) else None
 
 
 def fp8_peak():
@@ -175,19 +177,20 @@ def replica_throughput(units_per_rank: int, steps: int, world: int, elapsed_ms_m
     return world * units_per_rank * steps / (elapsed_ms_max / 1e3)
 
 
-def layer_bytes(ids: np.ndarray, T: int):
+def layer_bytes(ids: np.ndarray, T: int, w4: bool = False):
     """Algorithmic HBM bytes of one forward: the used experts (and the shared one) once, the
     router once, x read and y written in bf16."""
     U = len(np.unique(ids[ids >= 0]))
-    return (U + 1) * EXPERT_BYTES + ROUTER_BYTES + 4 * T * D, U
+    return (U + 1) * (EXPERT_BYTES_W4 if w4 else EXPERT_BYTES) + ROUTER_BYTES + 4 * T * D, U
 
 
-def gateup_bytes(U: int, T: int):
+def gateup_bytes(U: int, T: int, w4: bool = False):
     """Algorithmic bytes of one gate/up launch: the used experts' gate/up codes and scales,
     each token's E4M3 activation row once (the kernel gathers a token's routed copies by
     token), h written once in fp32 for every (token, slot) and shared row."""
     R = (K + 1) * T
-    return (U + 1) * GATEUP_EXPERT_BYTES + T * D + R * FFN * 4
+    per_expert = (FFN * D + 2 * FFN * 4) if w4 else GATEUP_EXPERT_BYTES
+    return (U + 1) * per_expert + T * D + R * FFN * 4
 
 
 # ------------------------------------------------------------------------------ ours ------
@@ -208,7 +211,8 @@ def run_ours(args):
     from gen import moegen as g
 
     hbm_peak, peak_kind = peaks()
-    w = g.kolibri_layer(g.SEED_DECODE)
+    w4 = args.weights == "e2m1"
+    w = g.kolibri_layer(g.SEED_DECODE, fp4=w4)
     base = moe.Layer.from_host(w, tiled=(args.path != "stream"))
     layers = [base]
     for _ in range(args.copies - 1):  # copies at other addresses: same values, no L2 reuse between steps
@@ -262,12 +266,13 @@ def run_ours(args):
         stage_ms[name] = statistics.mean(evs[i][si].elapsed_time(evs[i][si + 1]) for i in range(n_trace))
     traced_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][-1]) for i in range(n_trace))
     ids_h = ids.cpu().numpy()
-    nbytes, U = layer_bytes(ids_h, T)
-    gu_bytes = gateup_bytes(U, T)
+    nbytes, U = layer_bytes(ids_h, T, w4)
+    gu_bytes = gateup_bytes(U, T, w4)
     ms_step = elapsed_ms / args.steps
     value = replica_throughput(T, args.steps, world, elapsed_ms)
     gu_ms = stage_ms["gate_up"]
-    gu_kernel = "k_gateup_fp8" if args.path == "stream" else "k_expert_tc<16,gate_up>"
+    gu_kernel = "k_gateup_fp8" if args.path == "stream" else (
+        "k_expert_tc<16,gate_up,e2m1>" if w4 else "k_expert_tc<16,gate_up>")
     traffic = profiled_traffic(gu_kernel) if (args.path != "stream" and T == HEADLINE_T) else None
     roof = {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_bytes / (gu_ms * 1e-3) / 1e9,
             "peak": hbm_peak, "unit": "GB/s", "peak_kind": peak_kind,
@@ -331,7 +336,8 @@ def run_ours(args):
     l2_label = f"inputs larger than L2: {len(layers)} weight copies rotated across steps"
     extra = {"layer_hbm_frac": layer_frac, "layer_bytes_per_step": nbytes, "unique_experts": U,
              "stage_ms": stage_ms, "traced_ms_per_step": traced_ms}
-    extra["w8a8_drift_T64"] = w8a8_drift(w, x_host, y, ids, wt)
+    if not w4:
+        extra["w8a8_drift_T64"] = w8a8_drift(w, x_host, y, ids, wt)
     if not args.no_extra:
         for Tx in (1, 8):
             extra[f"decode_T{Tx}"] = small_batch(moe, g, layers, Tx, args, hbm_peak, flags)
@@ -352,9 +358,10 @@ def run_ours(args):
         "metric": "MoE-layer tokens/s (decode, batch 64); % of HBM roofline",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 weights, bf16 activations, fp32 accumulate (W8A8)", "data": "synthetic (seeded)",
+        "dtype": ("e2m1 weights, bf16 activations, fp32 accumulate (W4A8)" if w4 else
+                  "e4m3 weights, bf16 activations, fp32 accumulate (W8A8)"), "data": "synthetic (seeded)",
         "config": {"workload": f"kolibri moe layer decode T={T} (d=2048, ffn=640, 384 experts top-6 + 1 shared, "
-                               f"E4M3 weights, bias N(0,0.5))", "tokens": T, "layers": 1,
+                               f"{'E2M1' if w4 else 'E4M3'} weights, bias N(0,0.5))", "tokens": T, "layers": 1,
                    "l2": l2_label,
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "clocks": clocks, "e2e": e2e,
