@@ -97,7 +97,12 @@ def fp8_peak():
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return 2.0 * float(p["bf16_tflops"]), "measured bf16 x 2 (nominal fp8/bf16)"
+        kind = "measured bf16 x 2 (nominal fp8/bf16)"
+        clk = p.get("clocks_under_load", {})
+        if clk.get("sm_mhz_median"):  # the bf16 GEMM was measured at this clock, under the power cap
+            kind += (f"; the bf16 GEMM ran at a median SM clock of {clk['sm_mhz_median']:.0f} MHz "
+                     f"(max {clk.get('sm_max_mhz', 0):.0f}) at up to {clk.get('power_w_max', 0):.0f} W")
+        return 2.0 * float(p["bf16_tflops"]), kind
     return 2.0 * 1900.0, "fallback bf16 x 2"
 
 
