@@ -73,6 +73,19 @@ struct TcArgs {
   int* status_flags;
 };
 
+// MMA width for a tile of `nrows` token rows: the rows rounded up to the 16 columns an M = 128
+// MMA steps in, at most the tile width.  Columns past it are neither loaded nor computed (the
+// padding of an expert's last tile would otherwise cost up to a whole tile of MMA work).
+template <int kN>
+__device__ __forceinline__ int mma_cols(int nrows) {
+  return kN <= 16 ? kN : min(kN, max(16, (nrows + 15) & ~15));
+}
+
+// An instruction descriptor with its N field (bits 17-22, N / 8) replaced.
+__device__ __forceinline__ uint32_t with_n(uint32_t idesc, int n) {
+  return (idesc & ~(0x3Fu << 17)) | (uint32_t(n >> 3) << 17);
+}
+
 struct TcCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
@@ -81,6 +94,7 @@ struct TcCtl {
   uint64_t mma_done;
   uint64_t recv_full;  // split-K, rank 0: the partner's partial accumulators have arrived
   uint64_t recv_free;  // split-K, rank 1: rank 0 has consumed the receive buffer
+  int stage_n[kMaxStages];  // MMA width (token columns) of the item a stage belongs to
   uint32_t tmem_base;
   int abort;
 };
@@ -221,6 +235,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int item = unit; item < total && !stop; item += n_units) {
       const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kN, a.status_flags, 2);
       const int nb = item % nblk;
+      const int n_mma = mma_cols<kN>(tl.nrows);
       // the tokens of this lane's rows: gather4 lanes own rows 4l..4l+3; cp.async lanes own
       // 16-byte column l % 8 of rows l / 8 + 4j
       constexpr int kG = C::kLdgsts ? kN / 4 : 4;
@@ -247,6 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         if (lane == 0) {
+          ctl->stage_n[s] = n_mma;  // published to the MMA issuer by the arrive below
           // the weights' bytes in memory (E2M1: half their shared-memory bytes), then the
           // activations' unless cp.async brings them
           mbar_arrive_expect_tx(&ctl->full[s], (kW4 ? C::kABytes / 2 : C::kABytes) + (C::kLdgsts ? 0 : C::kBBytes));
@@ -274,7 +290,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < kG; ++i) {
               const int r = (lane >> 3) + 4 * i;
-              cp_async16(dst + r * kKTile + ((cc ^ (r & 7)) << 4), a.xq + size_t(g[i]) * a.d + col);
+              if (r < n_mma)  // rows past the MMA's width are never read
+                cp_async16(dst + r * kKTile + ((cc ^ (r & 7)) << 4), a.xq + size_t(g[i]) * a.d + col);
             }
           }
           cp_async_arrive_noinc(&ctl->full[s]);
@@ -302,7 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_begin();
     total = *a.n_tiles * nblk;
     if (lane == 0) {  // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = kW4 ? idesc_f8f6f4(kTileM, kN, kFmtE2M1, kFmtE4M3) : idesc_e4m3(kTileM, kN);
+      constexpr uint32_t idesc0 = kW4 ? idesc_f8f6f4(kTileM, kN, kFmtE2M1, kFmtE4M3) : idesc_e4m3(kTileM, kN);
       int it = 0, jt = 0;
       bool stop = false;
       for (int item = unit; item < total && !stop; item += n_units, ++jt) {
@@ -322,6 +339,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           if (C::kLdgsts) fence_proxy_async_smem();  // the activation rows were written by cp.async
+          const uint32_t idesc = kN > 16 ? with_n(idesc0, ctl->stage_n[s]) : idesc0;
 #pragma unroll
           for (int c = 0; c < kC; ++c) {
             const uint64_t db = sw128_desc(stage_b(s) + c * kN * kKTile);
