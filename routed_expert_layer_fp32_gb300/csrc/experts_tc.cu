@@ -380,16 +380,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t peer_recv_full = kSplit == 2 ? mapa_shared(smem_u32(&ctl->recv_full), 0) : 0;
     const uint32_t peer_recv_free = kSplit == 2 ? mapa_shared(smem_u32(&ctl->recv_free), 1) : 0;
     int jt = 0;
+    constexpr int kGroups = kHalf / 16;  // 16-column groups of this warp's columns
     for (int item = unit; item < total; item += n_units, ++jt) {
       const int b = jt % C::kBufs, ub = jt / C::kBufs;
+      // The item's tile, its row scales and its token columns' scales do not depend on the
+      // accumulators: load them before the wait, so their latency (a tile -> perm -> scale
+      // chain through L2) overlaps the item's MMAs instead of following them.
+      const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kN, a.status_flags, 4);
+      const int nb = item % nblk;
+      const bool shared = tl.group == a.E;
+      const int cols = min(cend, tl.nrows);  // this warp's columns of the item end here
+      float colscale[kGroups];               // lane i < 16: the scale of column cbeg + 16 g + i
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        const int c = cbeg + 16 * g + lane;
+        colscale[g] = 0.0f;
+        if (lane < 16 && c < cols)
+          colscale[g] = kGateUp ? a.sx[checked_token(a.perm[tl.row0 + c], a.T, a.status_flags, 5)] : a.sh[tl.row0 + c];
+      }
+      float rowscale[kA];  // gate/up: the gate and up scales of this lane's output; down: per block
+#pragma unroll
+      for (int ai = 0; ai < kA; ++ai) {
+        if (kGateUp) {
+          const float* sgp = shared ? a.sh_sgu : a.sgu + size_t(tl.group) * 2 * a.F;
+          rowscale[ai] = sgp[ai * a.F + nb * kTileM + rloc];
+        } else {
+          const int m = (nb * kA + ai) * kTileM + rloc;
+          rowscale[ai] = shared ? a.sh_sd[m] : a.sd[size_t(tl.group) * a.d + m];
+        }
+      }
       if (!mbar_wait(&ctl->acc_full[b], ub & 1, &ctl->abort)) {
         if (lane == 0) report_timeout_flag(a.status_flags, 14);
         break;
       }
       tc_fence_after();
-      const Tile tl = checked_tile(a.tiles, item / nblk, a.E, a.R, kN, a.status_flags, 4);
-      const int nb = item % nblk;
-      const bool shared = tl.group == a.E;
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(b * C::kColsPerAcc);
       if (kSplit == 2 && rank == 1) {  // hand the partial accumulators to rank 0
         if (!mbar_wait_cluster(&ctl->recv_free, (jt & 1) ^ 1, &ctl->abort)) {
@@ -425,14 +449,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       if (kGateUp) {
         const int n = nb * kTileM + rloc;
-        const float* sgp = shared ? a.sh_sgu : a.sgu + size_t(tl.group) * 2 * a.F;
-        const float sg = sgp[n], su = sgp[a.F + n];
-        for (int c0 = cbeg; c0 < cend && c0 < tl.nrows; c0 += 16) {
+        const float sg = rowscale[0], su = rowscale[1];
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+          const int c0 = cbeg + 16 * gi;
+          if (c0 >= cols) break;
           float gv[16], uv[16];
           load_acc(0, c0, gv);
           load_acc(1, c0, uv);
-          // lane i < 16 fetches the scale of token c0 + i; shuffles hand it to every lane
-          const float sx_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sx[checked_token(a.perm[tl.row0 + c0 + lane], a.T, a.status_flags, 5)] : 0.0f;
+          const float sx_l = colscale[gi];  // shuffles hand lane i's token scale to every lane
           float* hp = a.h + size_t(tl.row0 + c0) * a.F + n;
           if (c0 + 16 <= tl.nrows) {
 #pragma unroll
@@ -458,11 +483,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
        for (int ai = 0; ai < kA; ++ai) {  // row block ai of the item: accumulator columns ai * kN
         const int m = (nb * kA + ai) * kTileM + rloc;
-        const float sdm = shared ? a.sh_sd[m] : a.sd[size_t(tl.group) * a.d + m];
-        for (int c0 = cbeg; c0 < cend && c0 < tl.nrows; c0 += 16) {
+        const float sdm = rowscale[ai];
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+          const int c0 = cbeg + 16 * gi;
+          if (c0 >= cols) break;
           float yv[16];
           load_acc(ai, c0, yv);
-          const float sh_l = (lane < 16 && c0 + lane < tl.nrows) ? a.sh[tl.row0 + c0 + lane] : 0.0f;
+          const float sh_l = colscale[gi];
           __nv_bfloat16* yp = a.y_rows + size_t(tl.row0 + c0) * a.d + m;
           if (c0 + 16 <= tl.nrows) {
 #pragma unroll
