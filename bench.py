@@ -412,7 +412,9 @@ def prefill(moe, g, layer, T, flags, warmup=3, iters=10):
 def stack_bench(moe, g, hbm_peak, flags):
     """The 50-layer stack (r <- bf16(r + moe(r)), free routing, ~76 GB of E4M3 weights
     resident): decode with 32 tokens and a 16,384-token prefill, each one moe_forward_stack
-    call per step, timed with CUDA events (the residual is reset from the input every step)."""
+    call per step, timed with CUDA events (the residual is reset from the input every step).
+    The decode step is replayed as one CUDA graph (GraphedStack: the input copy and the 50
+    layers' launches), as a serving loop would run it; the prefill step is called directly."""
     import torch
     t0 = time.time()
     layers = [moe.Layer.from_host(g.stack_layer(l)) for l in range(g.STACK_LAYERS)]
@@ -425,15 +427,20 @@ def stack_bench(moe, g, hbm_peak, flags):
         r = x.clone()
         ws = moe.workspace(layers[0], T)
         ids = torch.empty((len(layers), T, K), dtype=torch.int32, device="cuda")
+        if T == 32:
+            graphed = moe.GraphedStack(layers, r, ws, x=x, ids_out=ids, flags=flags, layer_arr=arr)
+            step = graphed.replay
+        else:
+            def step():
+                r.copy_(x)
+                moe.forward_stack(layers, r, ws, ids_out=ids, flags=flags, layer_arr=arr)
         for _ in range(2):
-            r.copy_(x)
-            moe.forward_stack(layers, r, ws, ids_out=ids, flags=flags, layer_arr=arr)
+            step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(iters):
-            r.copy_(x)
-            moe.forward_stack(layers, r, ws, ids_out=ids, flags=flags, layer_arr=arr)
+            step()
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / iters
@@ -444,7 +451,8 @@ def stack_bench(moe, g, hbm_peak, flags):
             out["stack_decode_T32"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_stack": ms,
                                        "ms_per_layer": ms / len(layers), "bytes": nbytes,
                                        "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
-                                       "unique_experts_mean": float(np.mean(us)), "layers": len(layers)}
+                                       "unique_experts_mean": float(np.mean(us)), "layers": len(layers),
+                                       "step": "one CUDA graph (GraphedStack)"}
         else:
             flops = len(layers) * 7 * T * 3 * 2 * D * FFN
             out["stack_prefill_T16384"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_stack": ms,

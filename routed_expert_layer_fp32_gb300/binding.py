@@ -329,6 +329,36 @@ def forward_stack(layers: Sequence[Layer], residual: torch.Tensor, ws: torch.Ten
     return residual
 
 
+class GraphedStack:
+    """One step of the layer stack on fixed buffers, captured once as a CUDA graph and replayed
+    with one launch: optionally the copy of the step's input `x` into the residual, then the L
+    layers of moe_forward_stack.  At small batches a layer's kernels take a few microseconds
+    each, and issuing the L x 5 launches one by one from the host shows between them.  The
+    constructor runs the step once before capturing it (one-time attribute setup), so the
+    residual holds one step's result afterwards."""
+
+    def __init__(self, layers: Sequence[Layer], residual: torch.Tensor, ws: torch.Tensor,
+                 x: Optional[torch.Tensor] = None, ids_out=None, flags: int = PATH_AUTO, layer_arr=None):
+        arr = layer_arr if layer_arr is not None else layer_array(layers)
+        self.buffers = (layers, residual, ws, x, ids_out, arr)  # kept alive with the graph
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            if x is not None:
+                residual.copy_(x)
+            forward_stack(layers, residual, ws, ids_out=ids_out, flags=flags, layer_arr=arr)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            if x is not None:
+                residual.copy_(x, non_blocking=True)
+            forward_stack(layers, residual, ws, ids_out=ids_out, flags=flags, layer_arr=arr)
+
+    def replay(self):
+        self.graph.replay()
+
+
 def get_status(ws: torch.Tensor) -> int:
     """Synchronises the current stream; returns (and clears) the device-side status code."""
     return int(lib().moe_get_status(_ptr(ws), _stream()))

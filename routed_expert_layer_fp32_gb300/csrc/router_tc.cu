@@ -8,21 +8,22 @@
 // values is exact in fp32, so three accumulating bf16 MMAs with an fp32 accumulator give
 // x . w to fp32 accuracy.
 //
-// Tile: 128 tokens (M) x all experts, the experts split into two halves of n_half columns
-// (E = 384: 2 x 192) so one TMEM accumulator row holds a token's full logit row.  The split
-// kernel writes the terms already in stage order and in the 128-byte-swizzled shared-memory
-// layout: the three terms of one half for one 64-wide k-slice (n_half rows x 128 bytes each,
-// 72 KB at E = 384) are one contiguous block, so a weight stage is one bulk copy (on this GPU
-// a row-strided tensor-map box of the same size streams several times slower per SM, and
-// larger copies stream faster than smaller ones).  The x k-slice (16 KB) has its own ring and
-// is loaded once for both halves and all three terms.
+// Tile: 128 tokens (M) x all experts, the experts split into P parts of n_part columns (E =
+// 384: P = 2 halves of 192, or 4 x 96) so one TMEM accumulator row holds a token's
+// full logit row.  The split kernel writes the terms already in stage order and in the
+// 128-byte-swizzled shared-memory layout: the three terms of one part for one 64-wide k-slice
+// (n_part rows x 128 bytes each, 72 KB for a half at E = 384) are one contiguous block, so a
+// weight stage is one bulk copy (on this GPU a row-strided tensor-map box of the same size
+// streams several times slower per SM, and larger copies stream faster than smaller ones).
+// The x k-slice (16 KB) has its own ring and is loaded once for all parts and all three terms.
 //
 // Two ways to spread the tiles.  With many tiles each CTA takes whole tiles (both halves, two
 // weight stages per k-slice) and reads the 4.7 MB of weight terms from L2 for each of them.
-// With few tiles (every tile's CTA pair fits on the GPU at once) each tile gets a CTA pair of a
-// thread-block cluster, each CTA half of the experts (one weight stage per k-slice), and rank 1
-// hands its selected top-k lists to rank 0 through distributed shared memory for the final
-// merge.  Every CTA loads only into its own shared memory.  Warp roles as in the expert GEMMs
+// With few tiles each tile gets a thread-block cluster of P = 2 or 4 CTAs (the largest P for
+// which every tile's cluster fits on the GPU at once), each CTA one part of the experts
+// (one weight stage per k-slice), and ranks 1 .. P-1 hand their selected top-k lists to rank
+// 0 through distributed shared memory for the final merge.  Every CTA loads only into its own
+// shared memory.  Warp roles as in the expert GEMMs
 // (TMA producer, single-thread MMA issuer, sixteen epilogue warps); bounded waits.
 #include "common.cuh"
 #include "tcgen05.cuh"
@@ -36,27 +37,32 @@ constexpr int kRtEpiWarps = 4 * kRtEpiParts;
 constexpr int kRtThreads = (2 + kRtEpiWarps) * 32;
 // partial top-k lists of parts 1..3, merged by part 0: [part-1][token][slot] score, logit, id
 constexpr size_t kRtMergeBytes = size_t(kRtEpiParts - 1) * 128 * kTopK * 12;
-// split mode: rank 1's merged lists for rank 0, [128][kTopK] score, logit, id
+// split mode: each of ranks 1 .. P-1 hands rank 0 its merged lists, [128][kTopK] score, logit, id
 constexpr size_t kRtRecvBytes = size_t(128) * kTopK * 12;
+// CTAs per cluster in split mode.  Measured (moe_route, 600-8192 tokens): 4 is 3 us faster
+// than 2 up to 2048 tokens; 8 is no faster anywhere and at 2048 tokens its sixteen 8-CTA
+// clusters of ~213 KB CTAs do not all fit at once (111 us against 56).
+constexpr int kRtMaxParts = 4;
 constexpr int kRtM = 128;
 constexpr int kRtATile = kRtM * 128;
 constexpr size_t kRtSmemBudget = 200 * 1024;  // at most this much for the two rings
 
-// Split layout: block ((kt * 2 + h) * 3 + term) holds term `term` of experts
-// [h n_half, (h + 1) n_half) over k = [64 kt, 64 kt + 64): n_half rows of 128 bytes, the 16-byte
-// chunk c of row r stored at chunk c ^ (r % 8) (the MMA's 128-byte swizzle).  A thread converts
-// one 8-element chunk of one expert row into its three terms.
-__device__ __forceinline__ size_t split_block_offset(int kt, int term, int h, int n_half) {
-  return (size_t(kt * 2 + h) * 3 + term) * size_t(n_half) * 128;
+// Split layout for P parts: block ((kt * P + h) * 3 + term) holds term `term` of experts
+// [h n_part, (h + 1) n_part) over k = [64 kt, 64 kt + 64): n_part rows of 128 bytes, the
+// 16-byte chunk c of row r stored at chunk c ^ (r % 8) (the MMA's 128-byte swizzle).  A thread
+// converts one 8-element chunk of one expert row into its three terms.
+__device__ __forceinline__ size_t split_block_offset(int kt, int term, int h, int n_part, int P) {
+  return (size_t(kt * P + h) * 3 + term) * size_t(n_part) * 128;
 }
 
-__global__ void k_router_split_w(const float* __restrict__ Wr, int E, int d, int n_half, uint8_t* __restrict__ out) {
+__global__ void k_router_split_w(const float* __restrict__ Wr, int E, int d, int n_half, int P,
+                                 uint8_t* __restrict__ out) {
   pdl_begin();
   const int chunks = d / 8;  // 16-byte chunks of bf16 per expert row
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)E * chunks;
        i += (long long)gridDim.x * blockDim.x) {
     const int e = int(i / chunks), q = int(i % chunks);
-    const int kt = q >> 3, c = q & 7, h = e / n_half, r = e % n_half;
+    const int kt = q >> 3, c = q & 7, h = e / n_half, r = e % n_half;  // n_half: the part height
     const float4 a = *reinterpret_cast<const float4*>(Wr + size_t(e) * d + q * 8);
     const float4 b = *reinterpret_cast<const float4*>(Wr + size_t(e) * d + q * 8 + 4);
     const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -81,12 +87,11 @@ __global__ void k_router_split_w(const float* __restrict__ Wr, int E, int d, int
     const size_t in_block = size_t(r) * 128 + size_t((c ^ (r & 7)) * 16);
 #pragma unroll
     for (int term = 0; term < 3; ++term)
-      *reinterpret_cast<uint4*>(out + split_block_offset(kt, term, h, n_half) + in_block) =
+      *reinterpret_cast<uint4*>(out + split_block_offset(kt, term, h, n_half, P) + in_block) =
           make_uint4(t3[term][0], t3[term][1], t3[term][2], t3[term][3]);
   }
 }
 
-constexpr int kRtPair = 2;  // CTAs per tile in split mode (one thread-block cluster)
 constexpr int kRtMaxStages = 6;
 
 struct RtCtl {
@@ -97,7 +102,7 @@ struct RtCtl {
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_done;
-  uint64_t recv_full;  // split mode, rank 0: rank 1's lists have arrived (one arrival per thread)
+  uint64_t recv_full;  // split mode, rank 0: ranks 1 .. P-1's lists have arrived (one arrival per thread)
   uint32_t tmem_base;
   int abort;
   int epi_ok[2][4][kRtEpiParts];  // per tile parity: each epilogue warp's accumulator wait succeeded
@@ -107,29 +112,29 @@ template <bool split>
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_router_tc(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ w_split,
                 const float* __restrict__ bias, const float* __restrict__ sel_bias, int T, int d, int E, int n_half,
-                int n_a, int n_b, int tmem_cols,
+                int P, int n_a, int n_b, int tmem_cols,
                 float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int k,
                 int* status_flags) {
   extern __shared__ uint8_t rt_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
-  // split mode (few tiles): both CTAs of the pair take the same token tile, CTA r the experts
-  // [r n_half, (r + 1) n_half), and rank 1 hands its selected lists to rank 0.  Otherwise a CTA
-  // takes whole tiles, both halves.
+  // split mode (few tiles): the P CTAs of a cluster take the same token tile, CTA r the experts
+  // [r n_half, (r + 1) n_half) (n_half = E / P: the part height), and ranks 1 .. P-1 hand their
+  // selected lists to rank 0.  Otherwise a CTA takes whole tiles, both halves (P = 2).
   const int b_half_bytes = n_half * 128;
   // a weight stage: the three terms of one half for one k-slice, one contiguous copy (72 KB at
   // E = 384); split mode loads its own half's stage per k-slice, otherwise both halves' in turn
   const int b_stage_bytes = 3 * b_half_bytes;
-  const int b_per_kt = split ? 1 : 2;  // weight stages per k-slice
+  const int b_per_kt = split ? 1 : P;  // weight stages per k-slice
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + size_t(n_a) * kRtATile;
   RtCtl* ctl = reinterpret_cast<RtCtl*>(ring_b + size_t(n_b) * b_stage_bytes);
   uint8_t* merge = reinterpret_cast<uint8_t*>(ctl) + (sizeof(RtCtl) + 15) / 16 * 16;  // kRtMergeBytes
-  uint8_t* recv = merge + kRtMergeBytes;                                               // kRtRecvBytes (split)
+  uint8_t* recv = merge + kRtMergeBytes;                                               // (P-1) kRtRecvBytes (split)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = split ? int(cluster_ctarank()) : 0;
-  // the CTA (split mode: the CTA pair) takes tiles unit, unit + n_units, ...
-  constexpr int kPer = split ? kRtPair : 1;
-  const int unit = int(blockIdx.x) / kPer, n_units = int(gridDim.x) / kPer;
+  // the CTA (split mode: the cluster) takes tiles unit, unit + n_units, ...
+  const int per = split ? P : 1;
+  const int unit = int(blockIdx.x) / per, n_units = int(gridDim.x) / per;
   if (threadIdx.x == 0) {
     for (int s = 0; s < n_a; ++s) {
       mbar_init(&ctl->full_a[s], 1);
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->acc_empty, kRtEpiWarps);
     mbar_init(&ctl->mma_done, 1);
-    mbar_init(&ctl->recv_full, 4 * 32);  // every thread of rank 1's four part-0 warps
+    mbar_init(&ctl->recv_full, (split ? P - 1 : 1) * 4 * 32);  // every thread of the senders' part-0 warps
     ctl->abort = 0;
     mbar_fence_init();
   }
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&ctl->full_b[s], b_stage_bytes);
-            bulk_g2s(sb(s), w_split + split_block_offset(kt, 0, half_of(hh), n_half), uint32_t(b_stage_bytes),
+            bulk_g2s(sb(s), w_split + split_block_offset(kt, 0, half_of(hh), n_half, P), uint32_t(b_stage_bytes),
                      &ctl->full_b[s]);
           }
         }
@@ -272,10 +277,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const int n_chunks = split ? n_half / 16 : (E + 15) / 16;
     const int ch_base = split ? rank * (n_half / 16) : 0;
     const int ch_lo = ch_base + part * n_chunks / kRtEpiParts, ch_hi = ch_base + (part + 1) * n_chunks / kRtEpiParts;
-    // split mode: rank 1 writes its lists into rank 0's receive buffer [row][slot]
-    float* r_sc = reinterpret_cast<float*>(recv);
-    float* r_lg = r_sc + 128 * kTopK;
-    int* r_id = reinterpret_cast<int*>(r_lg + 128 * kTopK);
+    // split mode: rank r >= 1 writes its lists into block r - 1 of rank 0's receive buffer,
+    // [block][score, logit, id][row][slot]
     int jt = 0;
     for (int j = 0; tile_of(j) < n_items; ++j, ++jt) {
       const int item = tile_of(j);
@@ -388,8 +391,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               }
             }
           }
-          if (split && rank == 1) {  // hand the list to rank 0, which merges and writes
-            const uint32_t base = mapa_shared(smem_u32(recv), 0);
+          if (split && rank >= 1) {  // hand the list to rank 0, which merges and writes
+            const uint32_t base = mapa_shared(smem_u32(recv), 0) + uint32_t(rank - 1) * uint32_t(kRtRecvBytes);
 #pragma unroll
             for (int i = 0; i < kTopK; ++i) {
               const uint32_t o = uint32_t(row * kTopK + i) * 4u;
@@ -400,38 +403,43 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->recv_full), 0));  // releases this thread's stores
           }
           bool merged = true;
-          if (split && rank == 0) {  // rank 1's list for these tokens, in the same order
+          if (split && rank == 0) {  // ranks 1 .. P-1's lists for these tokens, in rank order
             merged = mbar_wait_cluster(&ctl->recv_full, jt & 1, &ctl->abort);
             if (!merged && lane == 0) report_timeout_flag(status_flags, 27);
-            bool open = merged;
+            for (int src = 0; merged && src < P - 1; ++src) {
+              const float* r_sc = reinterpret_cast<const float*>(recv + size_t(src) * kRtRecvBytes);
+              const float* r_lg = r_sc + 128 * kTopK;
+              const int* r_id = reinterpret_cast<const int*>(r_lg + 128 * kTopK);
+              bool open = true;  // a list is sorted: once one candidate stays out, the rest do
 #pragma unroll
-            for (int i = 0; i < kTopK; ++i) {
-              const int o = row * kTopK + i;
-              const float s = r_sc[o], lgv = r_lg[o];
-              const int e = r_id[o];
-              open = open && (s > tv[kTopK - 1] || (s == tv[kTopK - 1] && e < ti[kTopK - 1]));
-              if (open) {
-                tv[kTopK - 1] = s;
-                tl[kTopK - 1] = lgv;
-                ti[kTopK - 1] = e;
+              for (int i = 0; i < kTopK; ++i) {
+                const int o = row * kTopK + i;
+                const float s = r_sc[o], lgv = r_lg[o];
+                const int e = r_id[o];
+                open = open && (s > tv[kTopK - 1] || (s == tv[kTopK - 1] && e < ti[kTopK - 1]));
+                if (open) {
+                  tv[kTopK - 1] = s;
+                  tl[kTopK - 1] = lgv;
+                  ti[kTopK - 1] = e;
 #pragma unroll
-                for (int j2 = kTopK - 1; j2 > 0; --j2) {
-                  if (tv[j2] > tv[j2 - 1] || (tv[j2] == tv[j2 - 1] && ti[j2] < ti[j2 - 1])) {
-                    const float fv = tv[j2];
-                    tv[j2] = tv[j2 - 1];
-                    tv[j2 - 1] = fv;
-                    const float fl = tl[j2];
-                    tl[j2] = tl[j2 - 1];
-                    tl[j2 - 1] = fl;
-                    const int fi = ti[j2];
-                    ti[j2] = ti[j2 - 1];
-                    ti[j2 - 1] = fi;
+                  for (int j2 = kTopK - 1; j2 > 0; --j2) {
+                    if (tv[j2] > tv[j2 - 1] || (tv[j2] == tv[j2 - 1] && ti[j2] < ti[j2 - 1])) {
+                      const float fv = tv[j2];
+                      tv[j2] = tv[j2 - 1];
+                      tv[j2 - 1] = fv;
+                      const float fl = tl[j2];
+                      tl[j2] = tl[j2 - 1];
+                      tl[j2 - 1] = fl;
+                      const int fi = ti[j2];
+                      ti[j2] = ti[j2 - 1];
+                      ti[j2 - 1] = fi;
+                    }
                   }
                 }
               }
             }
           }
-          if (t < T && merged && !(split && rank == 1)) {
+          if (t < T && merged && !(split && rank >= 1)) {
             float m = tl[0];  // the largest selected logit (slot 0 unless the bias reordered them)
 #pragma unroll
             for (int i = 1; i < kTopK; ++i)
@@ -476,15 +484,19 @@ int rt_sm_count() {
 }
 
 // Stage counts of the two rings for one mode: weight stages first (three terms of one expert
-// half, 3 n_half 128 bytes each), then x slices, as many as fit beside the control block and
+// part, 3 n_part 128 bytes each), then x slices, as many as fit beside the control block and
 // the merge buffers (at most kRtMaxStages each).  False unless both rings get two stages.
-bool rt_rings(bool split, int n_half, int* n_a, int* n_b, size_t* smem) {
-  const size_t b_stage = size_t(3) * n_half * 128;
-  const size_t fixed = 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes + (split ? kRtRecvBytes : 0);
+bool rt_rings(bool split, int n_part, int P, int* n_a, int* n_b, size_t* smem) {
+  const size_t b_stage = size_t(3) * n_part * 128;
+  const size_t fixed = 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes + (split ? size_t(P - 1) * kRtRecvBytes : 0);
   const size_t rings = std::min(kRtSmemBudget, 227 * 1024 - fixed);
   if (rings < 2 * b_stage + 2 * size_t(kRtATile)) return false;
-  *n_b = int(std::min<size_t>(kRtMaxStages, (rings - 2 * size_t(kRtATile)) / b_stage));
-  *n_a = int(std::min<size_t>(kRtMaxStages, (rings - size_t(*n_b) * b_stage) / kRtATile));
+  if (split && P >= 4) {  // one weight stage per x slice: rings of equal depth
+    *n_a = *n_b = int(std::min<size_t>(kRtMaxStages, rings / (b_stage + size_t(kRtATile))));
+  } else {
+    *n_b = int(std::min<size_t>(kRtMaxStages, (rings - 2 * size_t(kRtATile)) / b_stage));
+    *n_a = int(std::min<size_t>(kRtMaxStages, (rings - size_t(*n_b) * b_stage) / kRtATile));
+  }
   *smem = size_t(*n_a) * kRtATile + size_t(*n_b) * b_stage + fixed;
   return *smem <= 227 * 1024;
 }
@@ -494,25 +506,30 @@ bool rt_rings(bool split, int n_half, int* n_a, int* n_b, size_t* smem) {
 bool router_tc_supported(const LayerDev& L, bool x_bf16) {
   int n_a = 0, n_b = 0;
   size_t smem = 0;
-  return x_bf16 && L.d % 64 == 0 && L.E <= 512 && L.E % 32 == 0 && rt_rings(false, L.E / 2, &n_a, &n_b, &smem) &&
-         rt_rings(true, L.E / 2, &n_a, &n_b, &smem) && encode_fn() != nullptr;
+  return x_bf16 && L.d % 64 == 0 && L.E <= 512 && L.E % 32 == 0 && rt_rings(false, L.E / 2, 2, &n_a, &n_b, &smem) &&
+         rt_rings(true, L.E / 2, 2, &n_a, &n_b, &smem) && encode_fn() != nullptr;
 }
 
 cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloat16* w3, float* logits, int32_t* ids,
                              float* wts, DevStatus* st, cudaStream_t s) {
-  const int n_half = L.E / 2;  // E % 32 == 0: two halves of a multiple of 16 experts
+  const int items = (T + kRtM - 1) / kRtM;
+  // few tiles: split mode, a cluster of P CTAs per tile, each CTA E / P experts, with the
+  // largest P (4 or 2) for which every tile's cluster fits on the GPU at once and the parts
+  // are whole 16-column chunks; otherwise one CTA per tile at a time, both halves (P = 2)
+  int split = 0, P = 2, n_a = 0, n_b = 0;
+  size_t smem = 0;
+  for (int p = kRtMaxParts; p >= 2 && !split; p /= 2)
+    if (L.E % (16 * p) == 0 && items * p <= rt_sm_count() && rt_rings(true, L.E / p, p, &n_a, &n_b, &smem)) {
+      split = 1;
+      P = p;
+    }
+  if (!split && !rt_rings(false, L.E / 2, 2, &n_a, &n_b, &smem)) return cudaErrorInvalidValue;
+  const int n_half = L.E / P;  // the part height (E % 32 == 0: P = 2 gives whole 16-column chunks)
   const long long n = (long long)L.E * (L.d / 8);
   cudaError_t e = launch_pdl(k_router_split_w, dim3(int(std::min<long long>((n + 255) / 256, 4096))), dim3(256), 0, s,
-                             L.Wr, L.E, L.d, n_half, reinterpret_cast<uint8_t*>(w3));
+                             L.Wr, L.E, L.d, n_half, P, reinterpret_cast<uint8_t*>(w3));
   if (e != cudaSuccess) return e;
-  const int items = (T + kRtM - 1) / kRtM;
-  // few tiles (every tile's CTA pair fits on the GPU at once): split mode, a CTA pair per
-  // tile, each CTA half of the experts; otherwise one CTA per tile at a time, both halves
-  const int split = items * kRtPair <= rt_sm_count() ? 1 : 0;
-  int n_a = 0, n_b = 0;
-  size_t smem = 0;
-  if (!rt_rings(split != 0, n_half, &n_a, &n_b, &smem)) return cudaErrorInvalidValue;
-  const int tmem_cols = 2 * n_half <= 256 ? 256 : 512;
+  const int tmem_cols = L.E <= 256 ? 256 : 512;
   CUtensorMap mx;
   if (!make_map_bytes(&mx, x, uint64_t(T), uint64_t(L.d), kRtM, 2)) return cudaErrorInvalidValue;
   static cudaError_t attr = [] {
@@ -522,7 +539,7 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   }();
   if (attr != cudaSuccess) return attr;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(split ? items * kRtPair : std::min(items, rt_sm_count()));
+  cfg.gridDim = dim3(split ? items * P : std::min(items, rt_sm_count()));
   cfg.blockDim = dim3(kRtThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -530,7 +547,7 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   attrs[1].id = cudaLaunchAttributeClusterDimension;
-  attrs[1].val.clusterDim.x = kRtPair;
+  attrs[1].val.clusterDim.x = P;
   attrs[1].val.clusterDim.y = 1;
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
@@ -538,9 +555,9 @@ cudaError_t launch_router_tc(const void* x, int T, const LayerDev& L, __nv_bfloa
   const uint8_t* w_split = static_cast<const uint8_t*>(static_cast<const void*>(w3));
   if (split)
     return cudaLaunchKernelEx(&cfg, k_router_tc<true>, mx, w_split, L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half,
-                              n_a, n_b, tmem_cols, logits, ids, wts, L.k, &st->flags);
+                              P, n_a, n_b, tmem_cols, logits, ids, wts, L.k, &st->flags);
   return cudaLaunchKernelEx(&cfg, k_router_tc<false>, mx, w_split, L.logit_bias(), L.sel_bias(), T, L.d, L.E, n_half,
-                            n_a, n_b, tmem_cols, logits, ids, wts, L.k, &st->flags);
+                            P, n_a, n_b, tmem_cols, logits, ids, wts, L.k, &st->flags);
 }
 
 }  // namespace moe

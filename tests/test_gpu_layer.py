@@ -148,6 +148,36 @@ def test_router_logits_ids_weights(moe, kolibri, T):
     assert moe.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("d,E,T", [(2048, 384, 600), (2048, 384, 2048), (2048, 384, 4096), (2048, 384, 9000),
+                                   (2048, 384, 12000), (1024, 512, 1024), (1024, 480, 1024), (1024, 256, 1024),
+                                   (1024, 224, 1024)])
+def test_prefill_router_cluster_sizes(moe, d, E, T):
+    """The tensor-core prefill router at every way it spreads the tiles: a cluster of P = 4 or
+    2 CTAs per 128-token tile, each CTA E / P experts (600, 2048 and 4096 tokens: P = 4; 9000:
+    P = 2; 12,000: one CTA per tile, all experts), 256 experts split 4 x 64 and 224 experts
+    only 2 x 112 (224 is not a multiple of 4 x 16), and 480 and 512 experts at d = 1024, where
+    two halves' weight stages do not fit in shared memory and the SIMT router with the
+    selection kernel runs instead.  Logits, ids and weights against
+    the oracle on every token up to 2048 and on 256 sampled tokens above (each token's routing
+    is independent of the others)."""
+    w = g.make_layer(61 + E, d, 64, E, fp8=True, bias_var=0.5)
+    L = moe.Layer.from_host(w)
+    x = g.make_x(62 + T, T, d, bf16=True)
+    ws = moe.workspace(L, T)
+    ids, wt, lg = moe.route(to_dev_x(x), L, ws, logits=True)
+    rows = np.arange(T) if T <= 2048 else np.sort(np.random.default_rng(T).choice(T, 256, replace=False))
+    ref = oracle_route(w, x[rows])
+    lg = lg.cpu().numpy()[rows]
+    err = np.max(np.abs(lg - ref["logits"]), axis=1) / np.max(np.abs(ref["logits"]), axis=1)
+    assert err.max() < 3e-5, err.max()
+    ids_h, wt_h = ids.cpu().numpy()[rows], wt.cpu().numpy()[rows]
+    ok, bad, _ = parity.ids_ok(ids_h, ref["ids"], ref["p"], E)
+    assert ok, bad
+    same = np.all(ids_h == ref["ids"], axis=1)
+    assert np.max(np.abs(wt_h[same] - ref["w"][same])) < 1e-5
+    assert moe.get_status(ws) == 0
+
+
 @pytest.mark.parametrize("d,E,T,bf16", [(256, 200, 128, True), (512, 200, 65, True), (768, 384, 17, False),
                                         (1280, 100, 128, True), (2048, 384, 100, False), (512, 512, 64, True),
                                         (256, 1000, 40, True), (512, 1000, 300, True), (512, 480, 200, True)])
@@ -380,6 +410,32 @@ def test_graphed_forward_matches_the_call(moe, kolibri, T):
         y_ref, ids_ref, w_ref = moe.forward(to_dev_x(x), L, moe.workspace(L, T), y_dtype=torch.bfloat16)
         assert torch.equal(ids, ids_ref) and torch.equal(wt, w_ref)
         assert torch.equal(y_pin.view(torch.int16), y_ref.cpu().view(torch.int16))
+    assert moe.get_status(ws) == 0
+
+
+@pytest.mark.parametrize("T", [1, 32])
+def test_graphed_stack_matches_the_call(moe, T):
+    """GraphedStack replays (input -> residual, a four-layer stack) and gives what the plain
+    moe_forward_stack call gives, bit for bit (residual and every layer's ids), for new inputs
+    written between replays."""
+    layers_w = [g.make_layer(700 + l, 512, 128, 64, fp8=True, bias_var=0.5) for l in range(4)]
+    layers = [moe.Layer.from_host(lw) for lw in layers_w]
+    ws = moe.workspace(layers[0], T)
+    x = torch.empty((T, 512), dtype=torch.bfloat16, device="cuda")
+    r = torch.empty_like(x)
+    ids = torch.empty((4, T, 6), dtype=torch.int32, device="cuda")
+    step = moe.GraphedStack(layers, r, ws, x=x, ids_out=ids)
+    for seed in (711, 712):
+        xh = to_dev_x(g.make_x(seed, T, 512, bf16=True))
+        x.copy_(xh)
+        step.replay()
+        torch.cuda.synchronize()
+        r_ref = xh.clone()
+        ids_ref = torch.empty_like(ids)
+        moe.forward_stack(layers, r_ref, moe.workspace(layers[0], T), ids_out=ids_ref)
+        torch.cuda.synchronize()
+        assert torch.equal(ids, ids_ref)
+        assert torch.equal(r.view(torch.int16), r_ref.view(torch.int16))
     assert moe.get_status(ws) == 0
 
 
