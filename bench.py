@@ -380,17 +380,31 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def prefill(moe, g, layer, T, flags, warmup=3, iters=10):
-    """One prefill-sized layer call (free routing), eager launches, per-stage events.  The
-    expert FLOPs are 7T x 3 x 2 x d x ffn (six routed rows and one shared row per token)."""
+def prefill(moe, g, layer, T, flags, warmup=3, iters=10, expert_bytes=None):
+    """One prefill-sized layer call (free routing): `ms_per_layer` over back-to-back calls
+    (events around the loop), `traced_ms_per_layer` and `stage_ms` with an event at every stage
+    boundary (which also stops the next kernel from starting early).  Two rooflines: the
+    expert FLOPs 7T x 3 x 2 x d x ffn (six routed rows and one shared row per token) against
+    the FP8 peak, and the bytes of the experts the call touches (at a few thousand tokens
+    nearly all of them) against HBM."""
     import torch
     peak, kind = fp8_peak()
+    hbm_peak, _ = peaks()
     x = torch.from_numpy(g.make_x(g.SEED_PREFILL, T, D, bf16=True).view(np.int16).copy()).cuda().view(torch.bfloat16)
     ws = moe.workspace(layer, T)
     y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
     for _ in range(warmup):
-        moe.forward(x, layer, ws, out=y, flags=flags)
+        _, ids, _ = moe.forward(x, layer, ws, out=y, flags=flags)
     torch.cuda.synchronize()
+    unique = len(np.unique(ids.cpu().numpy()))
+    nbytes = (unique + 1) * (expert_bytes or EXPERT_BYTES) + ROUTER_BYTES + 2 * T * D
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        moe.forward(x, layer, ws, out=y, flags=flags)
+    e1.record()
+    torch.cuda.synchronize()
+    plain = e0.elapsed_time(e1) / iters
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.binding.TRACE_POINTS)] for _ in range(iters)]
     for row in evs:
         for e in row:
@@ -404,9 +418,11 @@ def prefill(moe, g, layer, T, flags, warmup=3, iters=10):
              for k, n in enumerate(moe.binding.TRACE_STAGES)}
     flops = 7 * T * 3 * 2 * D * FFN
     gemm_ms = stage["gate_up"] + stage["down"]
-    return {"tokens_per_s": T / (total * 1e-3), "ms_per_layer": total, "expert_tflops": flops / (total * 1e-3) / 1e12,
-            "fp8_frac": flops / (total * 1e-3) / 1e12 / peak, "gemm_fp8_frac": flops / (gemm_ms * 1e-3) / 1e12 / peak,
-            "fp8_peak_tflops": peak, "peak_kind": kind, "stage_ms": stage}
+    return {"tokens_per_s": T / (plain * 1e-3), "ms_per_layer": plain, "traced_ms_per_layer": total,
+            "expert_tflops": flops / (plain * 1e-3) / 1e12, "fp8_frac": flops / (plain * 1e-3) / 1e12 / peak,
+            "gemm_fp8_frac": flops / (gemm_ms * 1e-3) / 1e12 / peak, "unique_experts": unique, "bytes": nbytes,
+            "hbm_frac": nbytes / (plain * 1e-3) / 1e9 / hbm_peak, "fp8_peak_tflops": peak, "peak_kind": kind,
+            "stage_ms": stage}
 
 
 def stack_bench(moe, g, hbm_peak, flags):
@@ -606,7 +622,7 @@ def w4_bench(moe, g, args, hbm_peak, n_copies, prefill_too):
             out["w4_decode_T64"]["gate_up_hbm_frac"] = gu_bytes / (stage_ms["gate_up"] * 1e-3) / 1e9 / hbm_peak
     del layers
     if prefill_too:
-        out["w4_prefill_T16384"] = prefill(moe, g, base, 16384, 0)
+        out["w4_prefill_T16384"] = prefill(moe, g, base, 16384, 0, expert_bytes=EXPERT_BYTES_W4)
     torch.cuda.empty_cache()
     return out
 
@@ -680,7 +696,11 @@ def prefill_forced_chunks(moe, g, layer, flags, T=2048, chunk=512, iters=10):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / iters
-    return {"tokens_per_s": T / (ms * 1e-3), "ms_per_2048_tokens": ms, "calls": T // chunk}
+    idh = ids.cpu().numpy()
+    nbytes = sum((len(np.unique(idh[c:c + chunk])) + 1) * EXPERT_BYTES + ROUTER_BYTES + 2 * chunk * D
+                 for c in range(0, T, chunk))
+    return {"tokens_per_s": T / (ms * 1e-3), "ms_per_2048_tokens": ms, "calls": T // chunk, "bytes": nbytes,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks()[0]}
 
 
 # ---------------------------------------------------------------------------- oracle ------
