@@ -39,6 +39,8 @@ constexpr int kRtThreads = (2 + kRtEpiWarps) * 32;
 constexpr size_t kRtMergeBytes = size_t(kRtEpiParts - 1) * 128 * kTopK * 12;
 // split mode: each of ranks 1 .. P-1 hands rank 0 its merged lists, [128][kTopK] score, logit, id
 constexpr size_t kRtRecvBytes = size_t(128) * kTopK * 12;
+// the router bias row in shared memory (E <= 512 floats)
+constexpr size_t kRtBiasBytes = 512 * 4;
 // CTAs per cluster in split mode.  Measured (moe_route, 600-8192 tokens): 4 is 3 us faster
 // than 2 up to 2048 tokens; 8 is no faster anywhere and at 2048 tokens its sixteen 8-CTA
 // clusters of ~213 KB CTAs do not all fit at once (111 us against 56).
@@ -108,6 +110,32 @@ struct RtCtl {
   int epi_ok[2][4][kRtEpiParts];  // per tile parity: each epilogue warp's accumulator wait succeeded
 };
 
+// One token's running top-k list: scores tv (descending), logits tl, expert ids ti; an empty
+// slot holds a NaN score.  Candidates are offered in increasing expert index (a scan visits its
+// experts in order, and the lists it merges cover ever higher experts), so a candidate whose
+// score equals a listed one goes in below it: the lower index ranks first.  The candidate
+// takes the first slot whose score is below its own (or empty) and the slots from there down
+// shift by one.  Every slot's new value is a select on the candidate's compares with the old
+// list, so no slot waits on another.  A NaN candidate never enters.  Returns whether the
+// candidate entered (it beat the last slot).
+__device__ __forceinline__ bool rt_list_insert(float (&tv)[kTopK], float (&tl)[kTopK], int (&ti)[kTopK], float s,
+                                               float l, int e) {
+  bool gt[kTopK];
+  const bool real = s == s;
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) gt[j] = real && !(s <= tv[j]);  // below s, or empty
+#pragma unroll
+  for (int j = kTopK - 1; j > 0; --j) {
+    tv[j] = gt[j] ? (gt[j - 1] ? tv[j - 1] : s) : tv[j];
+    tl[j] = gt[j] ? (gt[j - 1] ? tl[j - 1] : l) : tl[j];
+    ti[j] = gt[j] ? (gt[j - 1] ? ti[j - 1] : e) : ti[j];
+  }
+  tv[0] = gt[0] ? s : tv[0];
+  tl[0] = gt[0] ? l : tl[0];
+  ti[0] = gt[0] ? e : ti[0];
+  return gt[kTopK - 1];
+}
+
 template <bool split>
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_router_tc(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ w_split,
@@ -130,6 +158,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   RtCtl* ctl = reinterpret_cast<RtCtl*>(ring_b + size_t(n_b) * b_stage_bytes);
   uint8_t* merge = reinterpret_cast<uint8_t*>(ctl) + (sizeof(RtCtl) + 15) / 16 * 16;  // kRtMergeBytes
   uint8_t* recv = merge + kRtMergeBytes;                                               // (P-1) kRtRecvBytes (split)
+  float* s_bias = reinterpret_cast<float*>(recv + (split ? size_t(P - 1) * kRtRecvBytes : 0));  // E floats
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = split ? int(cluster_ctarank()) : 0;
   // the CTA (split mode: the cluster) takes tiles unit, unit + n_units, ...
@@ -264,12 +293,17 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   } else {  // epilogue: one token per TMEM lane, logits = acc + bias
     // With ids != nullptr the epilogue also selects.  The four warps of a lane quarter each scan
     // a quarter of the experts (consecutive 16-column chunks) and keep a sorted list of the
-    // kTopK best scores (larger first, lower index first on equal scores; a scan visits its
-    // experts in increasing index, so an equal later score never displaces an earlier one).
-    // A chunk whose best score is below the list's last is skipped whole.  Part 0 merges the
-    // four lists in that same order, then forms the softmax over the selected logits, summed
+    // kTopK best scores (larger first, lower index first on equal scores) with rt_list_insert.
+    // A chunk whose best score is not above the list's last is skipped whole.  Part 0 merges
+    // the four lists in expert order, then forms the softmax over the selected logits, summed
     // in slot order.  The score is the logit, plus sel_bias in the selection-only bias mode.
+    // The bias row (whichever of the two is set) is read once into shared memory.
     const int q = warp & 3, part = (warp - 2) >> 2;
+    const float* brow = bias ? bias : sel_bias;
+    if (brow) {
+      for (int i = int(threadIdx.x) - 64; i < E; i += kRtEpiWarps * 32) s_bias[i] = brow[i];
+      named_bar_sync(5, kRtEpiWarps * 32);
+    }
     float* m_sc = reinterpret_cast<float*>(merge);                       // [3][128][kTopK]
     float* m_lg = m_sc + (kRtEpiParts - 1) * 128 * kTopK;
     int* m_id = reinterpret_cast<int*>(m_lg + (kRtEpiParts - 1) * 128 * kTopK);
@@ -301,7 +335,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       int ti[kTopK];
 #pragma unroll
       for (int i = 0; i < kTopK; ++i) {
-        tv[i] = -INFINITY;
+        tv[i] = __int_as_float(0x7fc00000);  // empty
         tl[i] = -INFINITY;
         ti[i] = 0x7fffffff;
       }
@@ -315,35 +349,15 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int e = c0 + i;
-            v[i] = e < E ? v[i] + (bias ? bias[e] : 0.0f) : -INFINITY;
-            sc[i] = (e < E && sel_bias) ? v[i] + sel_bias[e] : v[i];
+            const float b = (brow && e < E) ? s_bias[e] : 0.0f;
+            v[i] = e < E ? (bias ? v[i] + b : v[i]) : -INFINITY;
+            sc[i] = e < E ? (sel_bias ? v[i] + b : v[i]) : __int_as_float(0x7fc00000);  // past E: never listed
             if (logits && e < E) logits[size_t(t) * E + e] = v[i];
             cmax = fmaxf(cmax, sc[i]);
           }
-          if (ids && !(cmax < tv[kTopK - 1])) {  // some score of the chunk may enter the list
+          if (ids && !(cmax <= tv[kTopK - 1])) {  // some score of the chunk may enter the list
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int e = c0 + i;
-              if (e < E && (sc[i] > tv[kTopK - 1] || (sc[i] == tv[kTopK - 1] && e < ti[kTopK - 1]))) {
-                tv[kTopK - 1] = sc[i];
-                tl[kTopK - 1] = v[i];
-                ti[kTopK - 1] = e;
-#pragma unroll
-                for (int j2 = kTopK - 1; j2 > 0; --j2) {
-                  if (tv[j2] > tv[j2 - 1] || (tv[j2] == tv[j2 - 1] && ti[j2] < ti[j2 - 1])) {
-                    const float fv = tv[j2];
-                    tv[j2] = tv[j2 - 1];
-                    tv[j2 - 1] = fv;
-                    const float fl = tl[j2];
-                    tl[j2] = tl[j2 - 1];
-                    tl[j2 - 1] = fl;
-                    const int fi = ti[j2];
-                    ti[j2] = ti[j2 - 1];
-                    ti[j2 - 1] = fi;
-                  }
-                }
-              }
-            }
+            for (int i = 0; i < 16; ++i) rt_list_insert(tv, tl, ti, sc[i], v[i], c0 + i);
           }
         }
       }
@@ -363,32 +377,13 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         }
         named_bar_sync(1 + q, kRtEpiParts * 32);  // the quarter's lists are written
         if (part == 0) {
-          // merge parts 1..3 into this list, one candidate at a time, with the scan's order
+          // merge parts 1..3 (ever higher experts) into this list; a list is sorted, so once one
+          // of its candidates stays out the rest do
           for (int p2 = 1; p2 < kRtEpiParts; ++p2) {
 #pragma unroll
             for (int i = 0; i < kTopK; ++i) {
               const int o = ((p2 - 1) * 128 + row) * kTopK + i;
-              const float s = m_sc[o], lgv = m_lg[o];
-              const int e = m_id[o];
-              if (s > tv[kTopK - 1] || (s == tv[kTopK - 1] && e < ti[kTopK - 1])) {
-                tv[kTopK - 1] = s;
-                tl[kTopK - 1] = lgv;
-                ti[kTopK - 1] = e;
-#pragma unroll
-                for (int j2 = kTopK - 1; j2 > 0; --j2) {
-                  if (tv[j2] > tv[j2 - 1] || (tv[j2] == tv[j2 - 1] && ti[j2] < ti[j2 - 1])) {
-                    const float fv = tv[j2];
-                    tv[j2] = tv[j2 - 1];
-                    tv[j2 - 1] = fv;
-                    const float fl = tl[j2];
-                    tl[j2] = tl[j2 - 1];
-                    tl[j2 - 1] = fl;
-                    const int fi = ti[j2];
-                    ti[j2] = ti[j2 - 1];
-                    ti[j2 - 1] = fi;
-                  }
-                }
-              }
+              if (!rt_list_insert(tv, tl, ti, m_sc[o], m_lg[o], m_id[o])) break;
             }
           }
           if (split && rank >= 1) {  // hand the list to rank 0, which merges and writes
@@ -410,32 +405,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               const float* r_sc = reinterpret_cast<const float*>(recv + size_t(src) * kRtRecvBytes);
               const float* r_lg = r_sc + 128 * kTopK;
               const int* r_id = reinterpret_cast<const int*>(r_lg + 128 * kTopK);
-              bool open = true;  // a list is sorted: once one candidate stays out, the rest do
 #pragma unroll
-              for (int i = 0; i < kTopK; ++i) {
+              for (int i = 0; i < kTopK; ++i) {  // rank src + 1 covers higher experts than the list
                 const int o = row * kTopK + i;
-                const float s = r_sc[o], lgv = r_lg[o];
-                const int e = r_id[o];
-                open = open && (s > tv[kTopK - 1] || (s == tv[kTopK - 1] && e < ti[kTopK - 1]));
-                if (open) {
-                  tv[kTopK - 1] = s;
-                  tl[kTopK - 1] = lgv;
-                  ti[kTopK - 1] = e;
-#pragma unroll
-                  for (int j2 = kTopK - 1; j2 > 0; --j2) {
-                    if (tv[j2] > tv[j2 - 1] || (tv[j2] == tv[j2 - 1] && ti[j2] < ti[j2 - 1])) {
-                      const float fv = tv[j2];
-                      tv[j2] = tv[j2 - 1];
-                      tv[j2 - 1] = fv;
-                      const float fl = tl[j2];
-                      tl[j2] = tl[j2 - 1];
-                      tl[j2 - 1] = fl;
-                      const int fi = ti[j2];
-                      ti[j2] = ti[j2 - 1];
-                      ti[j2 - 1] = fi;
-                    }
-                  }
-                }
+                if (!rt_list_insert(tv, tl, ti, r_sc[o], r_lg[o], r_id[o])) break;
               }
             }
           }
@@ -488,7 +461,8 @@ int rt_sm_count() {
 // the merge buffers (at most kRtMaxStages each).  False unless both rings get two stages.
 bool rt_rings(bool split, int n_part, int P, int* n_a, int* n_b, size_t* smem) {
   const size_t b_stage = size_t(3) * n_part * 128;
-  const size_t fixed = 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes + (split ? size_t(P - 1) * kRtRecvBytes : 0);
+  const size_t fixed = 1024 + (sizeof(RtCtl) + 15) / 16 * 16 + kRtMergeBytes + (split ? size_t(P - 1) * kRtRecvBytes : 0) +
+                       kRtBiasBytes;
   const size_t rings = std::min(kRtSmemBudget, 227 * 1024 - fixed);
   if (rings < 2 * b_stage + 2 * size_t(kRtATile)) return false;
   if (split && P >= 4) {  // one weight stage per x slice: rings of equal depth
