@@ -71,25 +71,30 @@ struct DispatchOut {
 // T <= kDispatchChunk and E < 512: the whole dispatch in one CTA of kLeanWarps warps,
 // everything in shared memory (lean_dispatch_smem_ints(T, E, k) ints at smem).  The ids are
 // staged first, read through L2 (they may have been written by other CTAs of the caller's
-// grid); warp w owns the run of tokens [w*tpw, (w+1)*tpw); per-warp counts become per-warp
-// row bases by a prefix over the warps, then over the experts.
+// grid), unless the caller staged them already (ids_staged: T * k ints at
+// smem + lean_dispatch_ids_offset(E)); warp w owns the run of tokens [w*tpw, (w+1)*tpw).
+// Per-warp counts become per-warp row bases within each expert by a prefix over the warps;
+// one scan over the experts then gives both the row offsets and the tile indices: each
+// expert's (rows << 16 | tiles) is scanned as one int (rows <= 6144 and tiles <= 6656 here, so
+// neither half carries into the other).  The shared expert's tiles come first.
 constexpr int kLeanWarps = 8;
+__host__ __device__ constexpr int lean_dispatch_ids_offset(int E) { return kLeanWarps * E + 3 * (E + 1); }
 __host__ __device__ constexpr int lean_dispatch_smem_ints(int T, int E, int k) {
-  return kLeanWarps * E + 3 * (E + 1) + T * k + 33;
+  return lean_dispatch_ids_offset(E) + T * k + 33;
 }
 
 __device__ __forceinline__ void dispatch_lean_body(const int32_t* ids_g, int T, int E, int k, int rows_per_tile,
-                                                   const DispatchOut& o, int* smem) {
+                                                   const DispatchOut& o, int* smem, bool ids_staged = false) {
   int* wcnt = smem;                  // [kLeanWarps][E]
-  int* tot = smem + kLeanWarps * E;  // [E + 1] counts, then offsets
-  int* cnt = tot + E + 1;            // [E + 1] counts (the tile list reads them here, not back from global)
-  int* ntile = cnt + E + 1;          // [E + 1] tiles per group (shared expert first), then their prefix
-  int* ids = ntile + E + 1;          // [T * k], the staged ids
+  int* pk = smem + kLeanWarps * E;   // [E + 1] packed rows and tiles per expert, then their exclusive prefix
+  int* cnt = pk + E + 1;             // [E + 1] rows per expert
+  int* ids = smem + lean_dispatch_ids_offset(E);  // [T * k], the staged ids
   int* warp_tot = ids + T * k;       // [33]
   const int warp = threadIdx.x >> 5;
   const int tpw = (T + kLeanWarps - 1) / kLeanWarps;
   const int t0 = min(T, warp * tpw), t1 = min(T, t0 + tpw);
-  for (int i = threadIdx.x; i < T * k; i += blockDim.x) ids[i] = __ldcg(ids_g + i);
+  if (!ids_staged)
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) ids[i] = __ldcg(ids_g + i);
   for (int i = threadIdx.x; i < kLeanWarps * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   warp_walk(ids, t0, t1, k, E, wcnt + warp * E, [](int, int, int) {});
@@ -101,45 +106,43 @@ __device__ __forceinline__ void dispatch_lean_body(const int32_t* ids_g, int T, 
       wcnt[w * E + e] = run;
       run += v;
     }
-    tot[e] = run;
     cnt[e] = run;
     o.counts[e] = run;
+    pk[e] = (run << 16) | ((run + rows_per_tile - 1) / rows_per_tile);
   }
   __syncthreads();
-  block_exclusive_scan(tot, E, warp_tot);  // tot[e] = offset of expert e
+  const int total = block_exclusive_scan(pk, E, warp_tot);
+  const int sh_tiles = (T + rows_per_tile - 1) / rows_per_tile;  // the shared expert's, first
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    o.offsets[e] = tot[e];
-    for (int w = 0; w < kLeanWarps; ++w) wcnt[w * E + e] += tot[e];
-  }
-  if (threadIdx.x == 0) {
-    o.counts[E] = T;
-    o.offsets[E] = k * T;
-    o.offsets[E + 1] = (k + 1) * T;
-  }
-  __syncthreads();
-  // tile list, shared expert first: tile counts per group, scanned
-  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
-    const int g = q == 0 ? E : q - 1;
-    const int c = g == E ? T : cnt[g];
-    ntile[q] = (c + rows_per_tile - 1) / rows_per_tile;
-  }
-  __syncthreads();
-  const int total_tiles = block_exclusive_scan(ntile, E + 1, warp_tot);
-  for (int q = threadIdx.x; q <= E; q += blockDim.x) {
-    const int g = q == 0 ? E : q - 1;
-    const int c = g == E ? T : cnt[g];
-    const int base_row = g == E ? k * T : tot[g];
-    int ti = ntile[q];
+    const int off = pk[e] >> 16, c = cnt[e];
+    o.offsets[e] = off;
+    for (int w = 0; w < kLeanWarps; ++w) wcnt[w * E + e] += off;
+    int ti = sh_tiles + (pk[e] & 0xffff);
     for (int r = 0; r < c; r += rows_per_tile, ++ti) {
       Tile tl;
-      tl.group = g;
-      tl.row0 = base_row + r;
+      tl.group = e;
+      tl.row0 = off + r;
       tl.nrows = min(rows_per_tile, c - r);
       tl.pad = 0;
       o.tiles[ti] = tl;
     }
   }
-  if (threadIdx.x == 0) *o.n_tiles = total_tiles;
+  if (threadIdx.x == 0) {
+    o.counts[E] = T;
+    o.offsets[E] = k * T;
+    o.offsets[E + 1] = (k + 1) * T;
+    int ti = 0;
+    for (int r = 0; r < T; r += rows_per_tile, ++ti) {
+      Tile tl;
+      tl.group = E;
+      tl.row0 = k * T + r;
+      tl.nrows = min(rows_per_tile, T - r);
+      tl.pad = 0;
+      o.tiles[ti] = tl;
+    }
+    *o.n_tiles = sh_tiles + (total & 0xffff);
+  }
+  __syncthreads();
   // rows: invalid slots get pos = -1; valid ones are placed in token order
   for (int i = (threadIdx.x & 31); i < (t1 - t0) * k; i += 32) {
     const int t = t0 + i / k;
@@ -154,6 +157,5 @@ __device__ __forceinline__ void dispatch_lean_body(const int32_t* ids_g, int T, 
   });
   for (int t = threadIdx.x; t < T; t += blockDim.x) perm[size_t(k) * T + t] = t;
 }
-
 
 }  // namespace moe

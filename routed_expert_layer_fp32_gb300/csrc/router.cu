@@ -177,7 +177,11 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
 // memory in rank order (deterministic) and writes logits + bias.  With ids != NULL, the CTAs
 // that wrote token sub-block r of token block z then count themselves on a ticket; the last of
 // them (every expert group's logits for those tokens are written by then) picks top-k and
-// weights for those tokens, a warp per token, as k_select does, and resets the ticket.
+// weights for those tokens, a warp per token, as k_select does, and resets the ticket.  With
+// one token block of at most kRdOneRank tokens, rank 0 takes them all: its selecting CTA then
+// holds every token's ids, keeps them in shared memory and runs the dispatch at once, with no
+// second ticket and no second read of the ids.
+constexpr int kRdOneRank = kRdThreads / 32;  // a token per warp
 __device__ __forceinline__ void decode_router_tail(const float* part, int T, int Tb, int E,
                                                    const float* __restrict__ bias, const float* sel_bias, float* logits,
                                                    int k, int32_t* __restrict__ ids, float* __restrict__ wts,
@@ -190,7 +194,8 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int T, int
   const int e0 = blockIdx.x * kRdE, t_base = blockIdx.z * kRdT;
   cluster.sync();
   const int n_slice = int(cluster.num_blocks()), rank = int(cluster.block_rank());
-  const int per = (Tb + n_slice - 1) / n_slice;
+  const bool one = gridDim.z == 1 && Tb <= kRdOneRank;
+  const int per = one ? Tb : (Tb + n_slice - 1) / n_slice;
   const int t_lo = min(Tb, rank * per), t_hi = min(Tb, t_lo + per);
   for (int i = tid; i < (t_hi - t_lo) * kRdE; i += kRdThreads) {  // one pass unless the cluster has < 4 slices
     const int t = t_lo + i / kRdE, e = i % kRdE;
@@ -229,7 +234,7 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int T, int
   // this CTA is done reading its peers' partials; it waits for them to be done with its own
   // only before it exits
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  if (ids) {
+  if (ids && (!one || rank == 0)) {  // (one token block: ranks 1.. hold no tokens)
     __syncthreads();  // the CTA's logits are written ...
     if (tid == 0) {
       // ... released device-wide by the ticket, which also acquires what the earlier CTAs released
@@ -243,11 +248,16 @@ __device__ __forceinline__ void decode_router_tail(const float* part, int T, int
     __syncthreads();
     if (*last_flag) {
       const int warp = tid >> 5, lane = tid & 31;
+      int* stage = (one && dsp.counts) ? scratch + lean_dispatch_ids_offset(E) : nullptr;
       for (int t = t_lo + warp; t < t_hi; t += kRdThreads / 32) {
         const size_t row = size_t(t_base + t);
-        select_write_free(logits + row * E, E, lane, ids + row * k, wts + row * k, sel_bias);
+        select_write_free(logits + row * E, E, lane, ids + row * k, wts + row * k, sel_bias,
+                          stage ? stage + row * k : nullptr);
       }
-      if (dsp.counts) {
+      if (stage) {  // every token's ids are in this CTA: dispatch now
+        __syncthreads();
+        dispatch_lean_body(ids, T, E, k, rows_per_tile, dsp, scratch, true);
+      } else if (dsp.counts) {
         // the selecting CTAs count themselves; the last (every token's ids written by then)
         // runs the dispatch in this CTA, on its staging memory
         __syncthreads();

@@ -19,20 +19,40 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
+// The largest of keys[lo, lo + n) and the lowest j holding it, as a balanced tree (a shallow
+// dependency chain; equal keys keep the left, lower, j).
+template <int n>
+__device__ __forceinline__ void key_argmax(const uint32_t* keys, int lo, uint32_t& best, int& bj) {
+  if constexpr (n == 1) {
+    best = keys[lo];
+    bj = lo;
+  } else {
+    uint32_t b0, b1;
+    int j0, j1;
+    key_argmax<n / 2>(keys, lo, b0, j0);
+    key_argmax<n - n / 2>(keys, lo + n / 2, b1, j1);
+    const bool right = b1 > b0;
+    best = right ? b1 : b0;
+    bj = right ? j1 : j0;
+  }
+}
+
 // Free selection of one token by one warp, written out with its weights.  Lane l holds the keys
-// of experts l + 32 j (j < kPer).  With sel_bias (the selection-only bias mode) the keys rank
-// logit + bias while the weights use the logits alone.  Each of the kTopK rounds takes the warp's largest key (one
-// warp reduction), then the lowest expert index holding it (a second reduction), and the lane
-// owning that expert drops it: the same experts in the same order as kTopK rounds of "larger
-// logit, or equal logit and lower index" over all E logits (softmax is monotone in the logit,
-// so choosing on logits chooses on probabilities).  Every lane ends with all kTopK choices, so
-// the weights need no further exchange: softmax over the selected logits, the largest (slot
-// 0) subtracted, summed in slot order.  A slot without a selectable expert gets id -1 and
-// weight 0.  The row is read through L2, so logits that other CTAs of the same grid wrote
-// (made visible by a fence and a ticket) are seen.
+// of experts l + 32 j (j < kPer) and tracks its largest key and the lowest j holding it.  With
+// sel_bias (the selection-only bias mode) the keys rank logit + bias while the weights use the
+// logits alone.  Each of the kTopK rounds takes the warp's largest key (one warp reduction),
+// then the lowest expert index holding it (a second reduction over the lanes' own best
+// indices), and the lane owning that expert drops it: the same experts in the same order as
+// kTopK rounds of "larger logit, or equal logit and lower index" over all E logits (softmax is
+// monotone in the logit, so choosing on logits chooses on probabilities).  Every lane ends
+// with all kTopK choices, so the weights need no further exchange: softmax over the selected
+// logits, the largest (slot 0) subtracted, summed in slot order; lane r divides its own slot.
+// A slot without a selectable expert gets id -1 and weight 0.  With ids_stage the ids also go
+// to that shared-memory row.  The row is read through L2, so logits that other CTAs of the
+// same grid wrote (made visible by a fence and a ticket) are seen.
 template <int kPer>
 __device__ __forceinline__ void select_write_free_t(const float* row, int E, int lane, int32_t* ids_row,
-                                                    float* w_row, const float* sel_bias) {
+                                                    float* w_row, const float* sel_bias, int* ids_stage) {
   // every load unconditional and in bounds (a clamped index), so all are in flight at once
   float raw[kPer];
 #pragma unroll
@@ -48,26 +68,20 @@ __device__ __forceinline__ void select_write_free_t(const float* row, int E, int
 #pragma unroll
     for (int j = 0; j < kPer; ++j) key[j] = lane + 32 * j < E ? logit_key(raw[j]) : 0u;
   }
-  uint32_t best = 0u;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) best = max(best, key[j]);
+  uint32_t best;
+  int bj;
+  key_argmax<kPer>(key, 0, best, bj);
   int sel[kTopK];
   float val[kTopK];
 #pragma unroll
   for (int r = 0; r < kTopK; ++r) {
     const uint32_t M = __reduce_max_sync(0xffffffffu, best);
-    uint32_t mine = 0xffffffffu;
+    const uint32_t I = __reduce_min_sync(0xffffffffu, best == M ? uint32_t(lane + 32 * bj) : 0xffffffffu);
+    if (M != 0u && int(I & 31u) == lane) {  // the owner drops the winner and finds its next best
 #pragma unroll
-    for (int j = kPer - 1; j >= 0; --j)
-      if (key[j] == M) mine = uint32_t(lane + 32 * j);
-    const uint32_t I = __reduce_min_sync(0xffffffffu, mine);
-    if (M != 0u && int(I & 31u) == lane) {
-      best = 0u;
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        if (j == int(I >> 5)) key[j] = 0u;
-        best = max(best, key[j]);
-      }
+      for (int j = 0; j < kPer; ++j)
+        if (j == bj) key[j] = 0u;
+      key_argmax<kPer>(key, 0, best, bj);
     }
     sel[r] = M != 0u ? int(I) : -1;
     if (sel_bias) {  // the weight needs the winner's own logit: its lane hands it over
@@ -92,22 +106,27 @@ __device__ __forceinline__ void select_write_free_t(const float* row, int E, int
     ex[r] = sel[r] >= 0 ? expf(val[r] - m) : 0.0f;
     s += ex[r];
   }
+  int my_sel = sel[0];
+  float my_ex = ex[0];
 #pragma unroll
-  for (int r = 0; r < kTopK; ++r) {
-    if (lane == r) {
-      ids_row[r] = sel[r];
-      w_row[r] = sel[r] >= 0 ? ex[r] / s : 0.0f;
-    }
+  for (int r = 1; r < kTopK; ++r) {
+    my_sel = lane == r ? sel[r] : my_sel;
+    my_ex = lane == r ? ex[r] : my_ex;
+  }
+  if (lane < kTopK) {
+    ids_row[lane] = my_sel;
+    w_row[lane] = my_sel >= 0 ? my_ex / s : 0.0f;
+    if (ids_stage) ids_stage[lane] = my_sel;
   }
 }
 
 __device__ __forceinline__ void select_write_free(const float* row, int E, int lane, int32_t* ids_row, float* w_row,
-                                                  const float* sel_bias) {
-  if (E <= 128) select_write_free_t<4>(row, E, lane, ids_row, w_row, sel_bias);
-  else if (E <= 256) select_write_free_t<8>(row, E, lane, ids_row, w_row, sel_bias);
-  else if (E <= 384) select_write_free_t<12>(row, E, lane, ids_row, w_row, sel_bias);
-  else if (E <= 512) select_write_free_t<16>(row, E, lane, ids_row, w_row, sel_bias);
-  else select_write_free_t<kMaxExperts / 32>(row, E, lane, ids_row, w_row, sel_bias);
+                                                  const float* sel_bias, int* ids_stage = nullptr) {
+  if (E <= 128) select_write_free_t<4>(row, E, lane, ids_row, w_row, sel_bias, ids_stage);
+  else if (E <= 256) select_write_free_t<8>(row, E, lane, ids_row, w_row, sel_bias, ids_stage);
+  else if (E <= 384) select_write_free_t<12>(row, E, lane, ids_row, w_row, sel_bias, ids_stage);
+  else if (E <= 512) select_write_free_t<16>(row, E, lane, ids_row, w_row, sel_bias, ids_stage);
+  else select_write_free_t<kMaxExperts / 32>(row, E, lane, ids_row, w_row, sel_bias, ids_stage);
 }
 
 }  // namespace moe
