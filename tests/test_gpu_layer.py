@@ -354,6 +354,24 @@ def test_decode_layer(moe, kolibri, T, path):
     assert moe.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("select_only", [False, True])
+def test_decode_around_the_one_rank_limit(moe, kolibri, select_only):
+    """Free-routing decode at 2, 5, 8, 9, 3, 9 and 1 tokens in turn on one workspace, checked
+    against the oracle.  Up to 8 tokens the decode router's rank 0 takes every token and one
+    CTA selects and dispatches them from shared memory; at 9 the selection is spread over the
+    ranks and a second ticket picks the dispatching CTA.  Switching between the two must leave
+    every ticket at zero for the other (a stale ticket would skip or repeat a selection)."""
+    w = kolibri.w
+    bias_mode = o.BIAS_SELECT if select_only else o.BIAS_SCORE
+    L = moe.Layer.from_host(w, bias_mode=moe.binding.BIAS_SELECT) if select_only else kolibri.for_path("tc")
+    ws = moe.workspace(L, 9)
+    for i, T in enumerate((2, 5, 8, 9, 3, 9, 1)):
+        x = g.make_x(g.SEED_DECODE + 300 + i, T, w.d, bf16=True)
+        y, ids, wt = moe.forward(to_dev_x(x), L, ws)
+        check_free_layer(w, x, y, ids, wt, where=f"T={T} (call {i}, select_only={select_only})", bias_mode=bias_mode)
+    assert moe.get_status(ws) == 0
+
+
 @pytest.mark.parametrize("T", [1, 8, 64])
 def test_back_to_back_forwards_see_their_own_routing(moe, kolibri, T):
     """Forwards on one workspace with different inputs, launched back to back without a host
